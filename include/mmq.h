@@ -1,0 +1,200 @@
+/*
+ * mmq.h -- C ABI of the GB300 (sm_103a) k-quant x q8_0 prefill GEMM library
+ * (libmmq.so).
+ *
+ * The operation is the prefill "MMQ" GEMM of the minfer CUDA optimisation
+ * log:   Y[t][o] = sum_k W[o][k] * X[t][k]
+ * with W stored as q6_K or q4_K super-blocks and X quantized per token into
+ * q8_0 "pad40" blocks.  Three steps, one entry point each:
+ *   mmq_quantize_act     X (fp32)            -> Q (q8_0 pad40 blocks)
+ *   mmq_register_weights W (packed k-quant)  -> handle (internal planes,
+ *                                               optional dense W_exp plane)
+ *   mmq_gemm             handle, Q           -> Y (fp32)
+ *
+ * Conventions for every entry point:
+ *   - Pointers named "device" are CUDA device pointers on the current device;
+ *     the caller owns them.  Nothing is freed or retained by the library
+ *     except inside an mmq_weights_t handle.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream) unless stated otherwise.
+ *   - Return value: MMQ_OK (0) or a negative MMQ_ERR_* code.  Argument
+ *     checks happen on the host before anything is enqueued; no C++
+ *     exception crosses this boundary.
+ *   - A device-side bounded wait that expires records a status word read by
+ *     mmq_last_device_error(); the kernel then returns instead of hanging.
+ */
+#ifndef MMQ_H
+#define MMQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *mmq_stream_t;   /* same type as cudaStream_t */
+typedef struct mmq_weights_s *mmq_weights_t;
+
+/* ---- status codes ------------------------------------------------------ */
+#define MMQ_OK 0
+#define MMQ_ERR_ARG -1             /* null pointer, bad size, id % 256 != 0, ... */
+#define MMQ_ERR_ALIGN -2           /* a pointer misses the alignment stated below */
+#define MMQ_ERR_TYPE -3            /* unknown weight type */
+#define MMQ_ERR_CUDA -4            /* a CUDA runtime call failed */
+#define MMQ_ERR_DEVICE_TIMEOUT -5  /* a bounded device wait expired (see above) */
+#define MMQ_ERR_OOM -6             /* device allocation failed */
+#define MMQ_ERR_UNSUPPORTED -7     /* valid input this build does not handle */
+#define MMQ_ERR_NO_DEVICE -8       /* current device is not a GB300 (sm_103) */
+
+/* ---- weight types (ggml numbering) ------------------------------------- */
+#define MMQ_Q4_K 12
+#define MMQ_Q6_K 14
+
+/* ---- byte layouts (defined once; the library's kernels use these) ------
+ * q8_0 pad40 activation block, one per token t per 32-element chunk c of K,
+ * block (t, c) at byte (t*nb32 + c)*40, nb32 = id/32.
+ * Source: "26 · r21 — Coalesced block-linear A staging", §2.1, and
+ * "25 · r20: Split-phase A staging", §3.2.
+ *   [0,2)  d    fp16, little-endian;  [2,4) zero
+ *   [4,36) qs   32 x int8;            [36,40) ssum int32 = sum of qs        */
+#define MMQ_Q8_BLOCK_BYTES 40
+#define MMQ_Q8_D_OFF 0
+#define MMQ_Q8_QS_OFF 4
+#define MMQ_Q8_SSUM_OFF 36
+/* block_q6_K, 256 weights in 16 sub-blocks of 16, w = d*sc[e/16]*(q-32).
+ * Source: "47 · r44 — W_exp stride mismatch root cause", §2.2; scale bytes
+ * at 192: "46 · r43 — PC-sampling attribution", §3.1.                      */
+#define MMQ_Q6K_BLOCK_BYTES 210
+#define MMQ_Q6K_QL_OFF 0
+#define MMQ_Q6K_QH_OFF 128
+#define MMQ_Q6K_SC_OFF 192
+#define MMQ_Q6K_D_OFF 208
+/* block_q4_K, 256 weights in 8 sub-blocks of 32, w = d*sc*q - dmin*m.  Not
+ * printed on the pages; the ggml layout is the reading taken.              */
+#define MMQ_Q4K_BLOCK_BYTES 144
+#define MMQ_Q4K_D_OFF 0
+#define MMQ_Q4K_DMIN_OFF 2
+#define MMQ_Q4K_SC_OFF 4
+#define MMQ_Q4K_QS_OFF 16
+/* every GEMM entry point requires id % MMQ_QK == 0 ("the NB-BT launch gate",
+ * "47 · r44 — W_exp stride mismatch root cause", §3.1)                     */
+#define MMQ_QK 256
+
+/* ---- registration flags ------------------------------------------------ */
+#define MMQ_REG_WEXP 0x1u  /* also build the dense centered-int8 W_exp plane (q6_K) */
+
+/* ---- GEMM arms (flags of mmq_gemm select one; arm_used reports it) ----- */
+#define MMQ_ARM_AUTO 0     /* library choice */
+#define MMQ_ARM_F16 1      /* operands from the registered fp16 operand plane (TMA copy) */
+
+/*
+ * mmq_quantize_act -- q8_0 quantization of activations.
+ * Source: the pad40 block of "26 · r21 — Coalesced block-linear A staging",
+ * §2.1; the quantizer itself (d = amax/127, q = round-half-away(x/d)) is the
+ * task's workload definition, computed in fp32 with IEEE division.
+ *   X   device, fp32, nt x id row-major, 16-byte aligned.
+ *   nt  tokens (>= 0; 0 is a no-op).   id  K, a positive multiple of 32.
+ *   Q   device, caller-allocated nt*(id/32)*40 bytes, 16-byte aligned;
+ *       fully overwritten (pad bytes [2,4) of each block are written as 0).
+ * Non-finite X, or |X| large enough that amax/127 overflows fp16, is out of
+ * contract (no error is raised; the bytes written are unspecified).
+ * Errors: MMQ_ERR_ARG, MMQ_ERR_ALIGN, MMQ_ERR_NO_DEVICE, MMQ_ERR_CUDA.
+ */
+int mmq_quantize_act(const float *X, int64_t nt, int64_t id, void *Q, mmq_stream_t stream);
+
+/*
+ * mmq_register_weights -- one-time expansion of a packed k-quant weight.
+ * Source: registration-time expansion and the dense W_exp plane of
+ * "46 · r43 — PC-sampling attribution", §3.2, and "47 · r44 — W_exp stride
+ * mismatch root cause", §2.1-2.2 (out[j*id + sb*256 + e] = q - 32, row pitch
+ * id, super-block pitch 256).
+ *   type  MMQ_Q6_K or MMQ_Q4_K.
+ *   W     device, od rows of id/256 packed blocks (210 B q6_K, 144 B q4_K),
+ *         row pitch (id/256)*block bytes, no alignment requirement.  Read
+ *         only during this call; the caller keeps ownership.
+ *   od    output rows (> 0).   id  K, a positive multiple of 256.
+ *   flags MMQ_REG_WEXP: also keep the dense centered-int8 W_exp plane
+ *         (od*id bytes, q6_K only).
+ *   out   receives a handle owning the internal planes (fp16 operand plane
+ *         with sub-block scales folded in, fp32 scale planes, optional
+ *         W_exp) until mmq_release_weights.
+ * Synchronizes `stream` before returning (registration is a one-time cost).
+ * q6_K blocks with a sub-block scale |sc| > 64 are rejected with
+ * MMQ_ERR_UNSUPPORTED: the folded operand sc*(q-32) would not be exact in
+ * fp16.  Errors: MMQ_ERR_ARG, MMQ_ERR_TYPE, MMQ_ERR_OOM, MMQ_ERR_UNSUPPORTED,
+ * MMQ_ERR_NO_DEVICE, MMQ_ERR_CUDA.
+ */
+int mmq_register_weights(int type, const void *W, int64_t od, int64_t id, uint32_t flags,
+                         mmq_stream_t stream, mmq_weights_t *out);
+
+/* Frees a handle and its device planes (synchronizes the device). NULL is
+ * accepted.  Returns MMQ_OK or MMQ_ERR_CUDA. */
+int mmq_release_weights(mmq_weights_t h);
+
+/*
+ * mmq_weights_wexp -- the dense centered-int8 W_exp plane of a q6_K handle
+ * registered with MMQ_REG_WEXP ("46 · r43 — PC-sampling attribution", §3.2):
+ * element (o, k) at plane[o*row_pitch + k], row_pitch == id, super-block
+ * pitch 256.  The pointer is device memory owned by the handle.
+ * Errors: MMQ_ERR_ARG (null argument), MMQ_ERR_UNSUPPORTED (no plane).
+ */
+int mmq_weights_wexp(mmq_weights_t h, const int8_t **plane, int64_t *row_pitch);
+
+/* Sizes of a handle's device planes, in bytes (the VRAM side of the
+ * registration trade-off, "47 · r44 — W_exp stride mismatch root cause",
+ * §2.4).  Any out pointer may be NULL. */
+int mmq_weights_info(mmq_weights_t h, int *type, int64_t *od, int64_t *id,
+                     int64_t *operand_bytes, int64_t *scale_bytes, int64_t *wexp_bytes);
+
+/*
+ * mmq_gemm -- Y = dequant(Q) . dequant(W)^T for a registered weight.
+ * Source: the MMQ contraction with per-sub-block integer dot products
+ * rescaled by d*sc (q6_K: "47 · r44 — W_exp stride mismatch root cause",
+ * §1.1 and §2.1) and the q4_K min correction through ssum.
+ *   h     handle from mmq_register_weights (same device).
+ *   Q     device, nt*(id/32)*40 bytes of pad40 blocks, 16-byte aligned.
+ *   nt    tokens (>= 0; 0 is a no-op).
+ *   Y     device, fp32, nt x od row-major, 16-byte aligned; overwritten.
+ *   flags MMQ_ARM_AUTO or one MMQ_ARM_*; arm_used (may be NULL) receives
+ *         the arm that ran.
+ * Allocates its scratch (nt*id*2 + nt*(id/32)*8 bytes) stream-ordered from a
+ * library-private memory pool and frees it stream-ordered; while `stream` is
+ * being captured into a CUDA graph the scratch becomes a graph memory node
+ * (cudaMallocAsync), so the call can be captured and replayed.
+ * Errors: MMQ_ERR_ARG, MMQ_ERR_ALIGN, MMQ_ERR_UNSUPPORTED, MMQ_ERR_OOM,
+ * MMQ_ERR_NO_DEVICE, MMQ_ERR_CUDA.  A device timeout is reported later by
+ * mmq_last_device_error().
+ */
+int mmq_gemm(mmq_weights_t h, const void *Q, int64_t nt, float *Y, mmq_stream_t stream,
+             uint32_t flags, int *arm_used);
+
+/*
+ * mmq_gemm_profiled -- mmq_gemm that also records two caller-created CUDA
+ * events (cudaEvent_t, either may be NULL) on `stream` immediately before
+ * and after the main GEMM kernel, so the caller can time that kernel alone.
+ * Arguments and errors otherwise as mmq_gemm.
+ */
+int mmq_gemm_profiled(mmq_weights_t h, const void *Q, int64_t nt, float *Y, mmq_stream_t stream,
+                      uint32_t flags, int *arm_used, void *ev_start, void *ev_stop);
+
+/* Synchronizes the current device, then returns and clears the device status
+ * word: MMQ_OK, or MMQ_ERR_DEVICE_TIMEOUT if a bounded wait expired since
+ * the last call. */
+int mmq_last_device_error(void);
+
+/* Limit of every device-side wait, in ns (default 2e9).  Host-global. */
+void mmq_set_wait_timeout_ns(uint64_t ns);
+
+/* Failure-detection self test: launches one CTA that waits on a barrier
+ * nothing arrives at, bounded by timeout_ns, then synchronizes and returns
+ * mmq_last_device_error() -- MMQ_ERR_DEVICE_TIMEOUT when the bound works. */
+int mmq_selftest_wait_timeout(uint64_t timeout_ns, mmq_stream_t stream);
+
+/* Static text for a status code. */
+const char *mmq_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MMQ_H */

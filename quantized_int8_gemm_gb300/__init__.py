@@ -1,0 +1,26 @@
+"""GB300 (sm_103a) k-quant x q8_0 prefill GEMM: Python binding of libmmq.so.
+
+The package holds the CUDA sources (csrc/), their build script (build.py) and
+the ctypes binding (mmq.py); the C ABI is declared in include/mmq.h.
+"""
+from .mmq import (  # noqa: F401
+    ARM_NAMES,
+    MMQ_ARM_AUTO,
+    MMQ_ARM_F16,
+    MMQ_Q4_K,
+    MMQ_Q6_K,
+    MMQ_REG_WEXP,
+    MMQError,
+    Weights,
+    load,
+    mmq_gemm,
+    mmq_gemm_profiled,
+    mmq_last_device_error,
+    mmq_quantize_act,
+    mmq_register_weights,
+    mmq_selftest_wait_timeout,
+    mmq_set_wait_timeout_ns,
+    mmq_strerror,
+    mmq_weights_info,
+    mmq_weights_wexp,
+)

@@ -1,0 +1,351 @@
+// api.cu -- the extern "C" entry points of libmmq.so (declared in mmq.h):
+// argument validation, per-device state, registration bookkeeping, tensor
+// maps and launches.  No arithmetic of the method happens on the host.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "internal.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int64_t kMaxTokens = 65535LL * 128;  // GEMM grid.y limit x token tile
+
+struct DeviceState {
+  bool probed = false;
+  bool usable = false;
+  mmq::DevStatus *words = nullptr;  // device memory
+  cudaMemPool_t pool = nullptr;     // stream-ordered GEMM scratch
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+std::atomic<uint64_t> g_limit_ns{2000000000ull};
+std::atomic<unsigned> g_epoch{1};
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+unsigned next_epoch() {
+  unsigned e = g_epoch.fetch_add(1);
+  if (e == 0) e = g_epoch.fetch_add(1);  // 0 never names a launch
+  return e;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Current device, checked to be an sm_103 part, with its state initialised.
+int device_state(int *dev_out, DeviceState **out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return MMQ_ERR_NO_DEVICE;
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState &d = g_dev[dev];
+  if (!d.probed) {
+    d.probed = true;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return MMQ_ERR_NO_DEVICE;
+    }
+    if (major != 10 || minor != 3) return MMQ_ERR_NO_DEVICE;
+    if (cudaMalloc(&d.words, sizeof(mmq::DevStatus)) != cudaSuccess ||
+        cudaMemset(d.words, 0, sizeof(mmq::DevStatus)) != cudaSuccess) {
+      cudaGetLastError();
+      return MMQ_ERR_CUDA;
+    }
+    cudaMemPoolProps props;
+    std::memset(&props, 0, sizeof(props));
+    props.allocType = cudaMemAllocationTypePinned;
+    props.handleTypes = cudaMemHandleTypeNone;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    if (cudaMemPoolCreate(&d.pool, &props) != cudaSuccess) {
+      cudaGetLastError();
+      return MMQ_ERR_CUDA;
+    }
+    uint64_t keep = UINT64_MAX;  // keep freed scratch cached in the pool
+    cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep);
+    d.usable = true;
+  }
+  if (!d.usable) return MMQ_ERR_NO_DEVICE;
+  *dev_out = dev;
+  *out = &d;
+  return MMQ_OK;
+}
+
+int cuda_rc(cudaError_t e) {
+  if (e == cudaSuccess) return MMQ_OK;
+  cudaGetLastError();
+  return e == cudaErrorMemoryAllocation ? MMQ_ERR_OOM : MMQ_ERR_CUDA;
+}
+
+void free_planes(mmq_weights_s *h) {
+  if (h->b16) cudaFree(h->b16);
+  if (h->dplane) cudaFree(h->dplane);
+  if (h->mmplane) cudaFree(h->mmplane);
+  if (h->wexp) cudaFree(h->wexp);
+  h->b16 = nullptr;
+  h->dplane = h->mmplane = nullptr;
+  h->wexp = nullptr;
+}
+
+}  // namespace
+
+namespace mmq {
+
+bool encode_tmap_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t inner,
+                    uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                    CUtensorMapSwizzle sw) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace mmq
+
+extern "C" {
+
+const char *mmq_strerror(int code) {
+  switch (code) {
+    case MMQ_OK: return "ok";
+    case MMQ_ERR_ARG: return "invalid argument";
+    case MMQ_ERR_ALIGN: return "misaligned pointer";
+    case MMQ_ERR_TYPE: return "unknown weight type";
+    case MMQ_ERR_CUDA: return "CUDA runtime error";
+    case MMQ_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait expired";
+    case MMQ_ERR_OOM: return "device out of memory";
+    case MMQ_ERR_UNSUPPORTED: return "unsupported input for this build";
+    case MMQ_ERR_NO_DEVICE: return "current device is not an sm_103 GPU";
+    default: return "unknown status code";
+  }
+}
+
+void mmq_set_wait_timeout_ns(uint64_t ns) { g_limit_ns.store(ns ? ns : 1); }
+
+int mmq_quantize_act(const float *X, int64_t nt, int64_t id, void *Q, mmq_stream_t stream) {
+  if (nt < 0 || id <= 0 || id % 32 != 0) return MMQ_ERR_ARG;
+  if (nt == 0) return MMQ_OK;
+  if (!X || !Q) return MMQ_ERR_ARG;
+  if (!aligned16(X) || !aligned16(Q)) return MMQ_ERR_ALIGN;
+  int dev;
+  DeviceState *d;
+  if (int rc = device_state(&dev, &d)) return rc;
+  return cuda_rc(mmq::launch_quantize_q8_0(X, nt, id, static_cast<uint8_t *>(Q),
+                                           reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int mmq_register_weights(int type, const void *W, int64_t od, int64_t id, uint32_t flags,
+                         mmq_stream_t stream, mmq_weights_t *out) {
+  if (!out) return MMQ_ERR_ARG;
+  *out = nullptr;
+  if (type != MMQ_Q4_K && type != MMQ_Q6_K) return MMQ_ERR_TYPE;
+  if (!W || od <= 0 || id <= 0 || id % MMQ_QK != 0) return MMQ_ERR_ARG;
+  if (od > 0x7fffffffLL || id / MMQ_QK > 65535) return MMQ_ERR_ARG;
+  if (flags & ~MMQ_REG_WEXP) return MMQ_ERR_ARG;
+  if ((flags & MMQ_REG_WEXP) && type != MMQ_Q6_K) return MMQ_ERR_UNSUPPORTED;
+  int dev;
+  DeviceState *d;
+  if (int rc = device_state(&dev, &d)) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  mmq_weights_s *h = new (std::nothrow) mmq_weights_s();
+  if (!h) return MMQ_ERR_OOM;
+  h->type = type;
+  h->device = dev;
+  h->flags = flags;
+  h->od = od;
+  h->id = id;
+  h->od_pad = (od + mmq::kRowTile - 1) / mmq::kRowTile * mmq::kRowTile;
+  h->nsb = id / MMQ_QK;
+  h->nb32 = id / 32;
+  h->b16_bytes = static_cast<size_t>(h->od_pad) * id * 2;
+  h->dplane_bytes = static_cast<size_t>(h->nsb) * h->od_pad * 4;
+  h->mm_bytes = type == MMQ_Q4_K ? static_cast<size_t>(h->nb32) * h->od_pad * 4 : 0;
+  h->wexp_bytes = (flags & MMQ_REG_WEXP) ? static_cast<size_t>(od) * id : 0;
+
+  int rc = MMQ_OK;
+  int *bad = nullptr;
+  cudaError_t e = cudaMalloc(&h->b16, h->b16_bytes);
+  if (e == cudaSuccess) e = cudaMalloc(&h->dplane, h->dplane_bytes);
+  if (e == cudaSuccess && h->mm_bytes) e = cudaMalloc(&h->mmplane, h->mm_bytes);
+  if (e == cudaSuccess && h->wexp_bytes) e = cudaMalloc(&h->wexp, h->wexp_bytes);
+  if (e == cudaSuccess) e = cudaMalloc(&bad, sizeof(int));
+  if (e == cudaSuccess) e = cudaMemsetAsync(bad, 0, sizeof(int), s);
+  if (e == cudaSuccess) e = mmq::launch_register(h, static_cast<const uint8_t *>(W), bad, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  int bad_h = 0;
+  if (e == cudaSuccess) e = cudaMemcpy(&bad_h, bad, sizeof(int), cudaMemcpyDeviceToHost);
+  if (bad) cudaFree(bad);
+  if (e != cudaSuccess) rc = cuda_rc(e);
+  if (rc == MMQ_OK && bad_h) rc = MMQ_ERR_UNSUPPORTED;
+  if (rc == MMQ_OK) {
+    bool ok = mmq::encode_tmap_2d(&h->tm_b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, h->b16,
+                                  static_cast<uint64_t>(id), static_cast<uint64_t>(h->od_pad),
+                                  static_cast<uint64_t>(id) * 2, 64, mmq::kRowTile,
+                                  CU_TENSOR_MAP_SWIZZLE_128B);
+    ok = ok && mmq::encode_tmap_2d(&h->tm_d, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, h->dplane,
+                                   static_cast<uint64_t>(h->od_pad),
+                                   static_cast<uint64_t>(h->nsb),
+                                   static_cast<uint64_t>(h->od_pad) * 4, mmq::kRowTile, 1,
+                                   CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (ok && h->mmplane)
+      ok = mmq::encode_tmap_2d(&h->tm_mm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, h->mmplane,
+                               static_cast<uint64_t>(h->od_pad), static_cast<uint64_t>(h->nb32),
+                               static_cast<uint64_t>(h->od_pad) * 4, mmq::kRowTile, 2,
+                               CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (!ok) rc = MMQ_ERR_CUDA;
+  }
+  if (rc != MMQ_OK) {
+    free_planes(h);
+    delete h;
+    return rc;
+  }
+  *out = h;
+  return MMQ_OK;
+}
+
+int mmq_release_weights(mmq_weights_t h) {
+  if (!h) return MMQ_OK;
+  int prev = -1;
+  cudaGetDevice(&prev);
+  if (prev != h->device) cudaSetDevice(h->device);
+  cudaError_t e = cudaDeviceSynchronize();
+  free_planes(h);
+  if (prev >= 0 && prev != h->device) cudaSetDevice(prev);
+  delete h;
+  return cuda_rc(e);
+}
+
+int mmq_weights_wexp(mmq_weights_t h, const int8_t **plane, int64_t *row_pitch) {
+  if (!h || !plane || !row_pitch) return MMQ_ERR_ARG;
+  if (!h->wexp) return MMQ_ERR_UNSUPPORTED;
+  *plane = h->wexp;
+  *row_pitch = h->id;
+  return MMQ_OK;
+}
+
+int mmq_weights_info(mmq_weights_t h, int *type, int64_t *od, int64_t *id,
+                     int64_t *operand_bytes, int64_t *scale_bytes, int64_t *wexp_bytes) {
+  if (!h) return MMQ_ERR_ARG;
+  if (type) *type = h->type;
+  if (od) *od = h->od;
+  if (id) *id = h->id;
+  if (operand_bytes) *operand_bytes = static_cast<int64_t>(h->b16_bytes);
+  if (scale_bytes) *scale_bytes = static_cast<int64_t>(h->dplane_bytes + h->mm_bytes);
+  if (wexp_bytes) *wexp_bytes = static_cast<int64_t>(h->wexp_bytes);
+  return MMQ_OK;
+}
+
+static int gemm_impl(mmq_weights_t h, const void *Q, int64_t nt, float *Y, mmq_stream_t stream,
+                     uint32_t flags, int *arm_used, cudaEvent_t ev0, cudaEvent_t ev1) {
+  if (!h || nt < 0 || nt > kMaxTokens) return MMQ_ERR_ARG;
+  if (flags != MMQ_ARM_AUTO && flags != MMQ_ARM_F16) return MMQ_ERR_UNSUPPORTED;
+  if (arm_used) *arm_used = MMQ_ARM_F16;
+  if (nt == 0) return MMQ_OK;
+  if (!Q || !Y) return MMQ_ERR_ARG;
+  if (!aligned16(Q) || !aligned16(Y)) return MMQ_ERR_ALIGN;
+  int dev;
+  DeviceState *d;
+  if (int rc = device_state(&dev, &d)) return rc;
+  if (dev != h->device) return MMQ_ERR_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  const size_t a_bytes = static_cast<size_t>(nt) * h->id * 2;
+  const size_t a_pad = (a_bytes + 255) / 256 * 256;
+  const size_t sc_bytes = static_cast<size_t>(nt) * h->nb32 * 8;
+  // Scratch is stream-ordered: from the library pool, or -- while the stream
+  // is being captured into a CUDA graph -- a graph memory node.
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(s, &cap);
+  if (e != cudaSuccess) return cuda_rc(e);
+  void *scratch = nullptr;
+  e = cap == cudaStreamCaptureStatusActive
+          ? cudaMallocAsync(&scratch, a_pad + sc_bytes, s)
+          : cudaMallocFromPoolAsync(&scratch, a_pad + sc_bytes, d->pool, s);
+  if (e != cudaSuccess) return cuda_rc(e);
+  void *a16 = scratch;
+  void *scp = static_cast<uint8_t *>(scratch) + a_pad;
+
+  e = mmq::launch_gemm_prepass(static_cast<const uint8_t *>(Q), nt, h->id, a16, scp, s);
+  CUtensorMap tm_a;
+  if (e == cudaSuccess &&
+      !mmq::encode_tmap_2d(&tm_a, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a16,
+                           static_cast<uint64_t>(h->id), static_cast<uint64_t>(nt),
+                           static_cast<uint64_t>(h->id) * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+    e = cudaErrorInvalidValue;
+  if (e == cudaSuccess && ev0) e = cudaEventRecord(ev0, s);
+  if (e == cudaSuccess)
+    e = mmq::launch_gemm_f16(h, tm_a, scp, nt, Y, d->words, next_epoch(), g_limit_ns.load(), s);
+  if (e == cudaSuccess && ev1) e = cudaEventRecord(ev1, s);
+  cudaError_t ef = cudaFreeAsync(scratch, s);
+  if (e == cudaSuccess) e = ef;
+  return cuda_rc(e);
+}
+
+int mmq_gemm(mmq_weights_t h, const void *Q, int64_t nt, float *Y, mmq_stream_t stream,
+             uint32_t flags, int *arm_used) {
+  return gemm_impl(h, Q, nt, Y, stream, flags, arm_used, nullptr, nullptr);
+}
+
+int mmq_gemm_profiled(mmq_weights_t h, const void *Q, int64_t nt, float *Y, mmq_stream_t stream,
+                      uint32_t flags, int *arm_used, void *ev_start, void *ev_stop) {
+  return gemm_impl(h, Q, nt, Y, stream, flags, arm_used, static_cast<cudaEvent_t>(ev_start),
+                   static_cast<cudaEvent_t>(ev_stop));
+}
+
+int mmq_last_device_error(void) {
+  int dev;
+  DeviceState *d;
+  if (int rc = device_state(&dev, &d)) return rc;
+  if (cudaDeviceSynchronize() != cudaSuccess) return cuda_rc(cudaErrorUnknown);
+  mmq::DevStatus w;
+  if (cudaMemcpy(&w, d->words, sizeof(w), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return cuda_rc(cudaErrorUnknown);
+  const int zero = 0;
+  if (cudaMemcpy(&d->words->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+    return cuda_rc(cudaErrorUnknown);
+  return w.status ? MMQ_ERR_DEVICE_TIMEOUT : MMQ_OK;
+}
+
+int mmq_selftest_wait_timeout(uint64_t timeout_ns, mmq_stream_t stream) {
+  int dev;
+  DeviceState *d;
+  if (int rc = device_state(&dev, &d)) return rc;
+  cudaError_t e = mmq::launch_wait_selftest(d->words, next_epoch(), timeout_ns ? timeout_ns : 1,
+                                            reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_rc(e);
+  return mmq_last_device_error();
+}
+
+}  // extern "C"

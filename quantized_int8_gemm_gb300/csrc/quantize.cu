@@ -1,0 +1,74 @@
+// quantize.cu -- fp32 activations -> q8_0 "pad40" blocks.
+//
+// Block (t, c) of 32 values, at byte (t*nb32 + c)*40 (the pad40 plane of
+// "26 · r21 — Coalesced block-linear A staging", §2.1):
+//   d = amax/127 (fp32, IEEE division), q_i = roundf(x_i / d) (half away
+//   from zero), stored d16 = fp16_rn(d), bytes [2,4) = 0, ssum = sum q_i.
+//
+// HBM-bound: 128 B read and 40 B written per block.  Eight lanes share a
+// block, each loading one float4 (coalesced 512 B per warp) and storing one
+// 4-byte qs word; lane 0 of the eight also writes the d word and ssum.
+#include <cuda_fp16.h>
+
+#include "internal.h"
+
+namespace mmq {
+namespace {
+
+__global__ void __launch_bounds__(256) quantize_q8_0_kernel(const float4 *__restrict__ X,
+                                                            int64_t nblocks,
+                                                            uint8_t *__restrict__ Q) {
+  const int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t blk = g >> 3;
+  const int part = static_cast<int>(g & 7);
+  const bool valid = blk < nblocks;
+  float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (valid) v = __ldg(X + blk * 8 + part);
+
+  float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+#pragma unroll
+  for (int m = 1; m < 8; m <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+
+  const float d = amax / 127.0f;
+  int q[4] = {0, 0, 0, 0};
+  if (amax != 0.0f) {
+    const float xs[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      int qi = static_cast<int>(roundf(xs[i] / d));
+      q[i] = max(-127, min(127, qi));
+    }
+  }
+  int ssum = q[0] + q[1] + q[2] + q[3];
+#pragma unroll
+  for (int m = 1; m < 8; m <<= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, m);
+
+  if (!valid) return;
+  uint8_t *b = Q + blk * MMQ_Q8_BLOCK_BYTES;
+  const uint32_t word = (static_cast<uint32_t>(q[0]) & 0xFFu) |
+                        ((static_cast<uint32_t>(q[1]) & 0xFFu) << 8) |
+                        ((static_cast<uint32_t>(q[2]) & 0xFFu) << 16) |
+                        ((static_cast<uint32_t>(q[3]) & 0xFFu) << 24);
+  reinterpret_cast<uint32_t *>(b + MMQ_Q8_QS_OFF)[part] = word;
+  if (part == 0) {
+    const uint32_t dbits = amax != 0.0f ? __half_as_ushort(__float2half_rn(d)) : 0u;
+    *reinterpret_cast<uint32_t *>(b + MMQ_Q8_D_OFF) = dbits;  // d16 | zero pad
+    *reinterpret_cast<int32_t *>(b + MMQ_Q8_SSUM_OFF) = ssum;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_q8_0(const float *X, int64_t nt, int64_t id, uint8_t *Q,
+                                 cudaStream_t s) {
+  const int64_t nblocks = nt * (id / 32);
+  if (nblocks == 0) return cudaSuccess;
+  const int64_t threads = nblocks * 8;
+  const int bs = 256;
+  const int64_t grid = (threads + bs - 1) / bs;
+  quantize_q8_0_kernel<<<static_cast<unsigned>(grid), bs, 0, s>>>(
+      reinterpret_cast<const float4 *>(X), nblocks, Q);
+  return cudaGetLastError();
+}
+
+}  // namespace mmq

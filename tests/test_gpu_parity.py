@@ -1,0 +1,215 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Bit-exact for the q8_0 activation blocks and the W_exp plane; for the fp32
+GEMM output  max|Y_gpu - Y_ref| <= 1e-3 * max|Y_ref| + 1e-5  (the tolerance
+the task states), Y_ref in fp64 from the oracle.  Small shapes are compared
+element by element (several tiles, ragged tails); the five workloads at full
+size are compared on sampled outputs the oracle computes one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from synth import gen
+
+pytestmark = pytest.mark.gpu
+
+RTOL_MAX = 1e-3
+ATOL = 1e-5
+QT = {"q4_K": oracle.Q4_K, "q6_K": oracle.Q6_K}
+
+
+@pytest.fixture(scope="module")
+def mmq():
+    from quantized_int8_gemm_gb300 import build
+    build.build()
+    import quantized_int8_gemm_gb300 as m
+    m.load()
+    assert torch.cuda.is_available()
+    return m
+
+
+def _within_tol(y_gpu, y_ref):
+    y_gpu = np.asarray(y_gpu, dtype=np.float64)
+    err = np.abs(y_gpu - y_ref).max() if y_ref.size else 0.0
+    bound = RTOL_MAX * (np.abs(y_ref).max() if y_ref.size else 0.0) + ATOL
+    return err, bound
+
+
+def _run(mmq, qtype, W, od, id_, X, flags=0):
+    dev = torch.device("cuda")
+    Wd = torch.from_numpy(W).to(dev)
+    Xd = torch.from_numpy(X).to(dev)
+    Qd = mmq.mmq_quantize_act(Xd)
+    w = mmq.mmq_register_weights(qtype, Wd, od, id_, flags)
+    Y, arm = mmq.mmq_gemm(w, Qd, X.shape[0], return_arm=True)
+    torch.cuda.synchronize()
+    assert mmq.mmq_last_device_error() == 0
+    return w, Qd.cpu().numpy(), Y.cpu().numpy(), arm
+
+
+# ---------------------------------------------------------------- quantizer
+@pytest.mark.parametrize("cfg", gen.CONFIGS, ids=lambda c: c.name)
+def test_quantize_bit_exact_workloads(mmq, cfg):
+    X = gen.activations(cfg.nt, cfg.id, cfg.seed, cfg.sigma, cfg.outlier_p, cfg.outlier_scale)
+    Q = mmq.mmq_quantize_act(torch.from_numpy(X).cuda()).cpu().numpy()
+    assert np.array_equal(Q, oracle.quantize_q8_0(X))
+
+
+def test_quantize_bit_exact_edge_values(mmq):
+    rng = np.random.default_rng(0)
+    X = rng.standard_normal((37, 256)).astype(np.float32)
+    X[0, :32] = 0.0                                  # all-zero block
+    X[1, :32] = 3.0                                  # all-equal block
+    X[2, :32] = np.arange(32) - 15.5                 # halves
+    X[3, :32] = 0.0
+    X[3, 0] = 127.0
+    X[3, 1:9] = [2.5, -2.5, 0.5, -0.5, 1.5, -1.5, 126.5, -126.5]  # exact ties
+    X[4] *= 1e-30                                    # d16 underflows to zero
+    X[5] *= 1e-6                                     # subnormal d16
+    X[6] *= 7e4                                      # large
+    X[7, 32:64] = -0.0
+    Q = mmq.mmq_quantize_act(torch.from_numpy(X).cuda()).cpu().numpy()
+    assert np.array_equal(Q, oracle.quantize_q8_0(X))
+
+
+# ---------------------------------------------------------------- W_exp plane
+@pytest.mark.parametrize("od,id_", [(256, 512), (70, 256), (3584, 3584), (3584, 18944)])
+def test_wexp_plane_bit_exact(mmq, od, id_):
+    W = gen.weights("q6_K", od, id_, seed=od + id_)
+    w = mmq.mmq_register_weights("q6_K", torch.from_numpy(W).cuda(), od, id_, mmq.MMQ_REG_WEXP)
+    plane = mmq.mmq_weights_wexp(w).cpu().numpy()
+    assert plane.shape == (od, id_)
+    assert np.array_equal(plane, oracle.expand_q6k_dense(W, od, id_))
+    info = mmq.mmq_weights_info(w)
+    assert info["wexp_bytes"] == od * id_
+    w.release()
+
+
+# ---------------------------------------------------------------- GEMM, full compare
+SMALL = [
+    ("q6_K", 256, 512, 16, 0),     # workload 0, the tiny q6_K case
+    ("q6_K", 300, 768, 200, 1),    # ragged rows and tokens, 3 super-blocks
+    ("q4_K", 260, 512, 129, 2),
+    ("q4_K", 131, 256, 1, 3),      # one token, od not a multiple of 4
+    ("q6_K", 5, 256, 130, 4),      # od < 4, one super-block
+    ("q4_K", 384, 1024, 256, 5),   # second token tile starts at i0 = 128
+    ("q6_K", 129, 2048, 127, 6),
+    ("q4_K", 128, 768, 128, 7),
+]
+
+
+@pytest.mark.parametrize("name,od,id_,nt,seed", SMALL)
+def test_gemm_parity_full_compare(mmq, name, od, id_, nt, seed):
+    W = gen.weights(name, od, id_, seed=100 + seed)
+    X = gen.activations(nt, id_, seed=200 + seed, outlier_p=0.01, outlier_scale=20.0)
+    _, Q, Y, arm = _run(mmq, name, W, od, id_, X)
+    Q_ref = oracle.quantize_q8_0(X)
+    assert np.array_equal(Q, Q_ref)
+    Y_ref = oracle.gemm(QT[name], W, od, id_, Q_ref, nt)
+    err, bound = _within_tol(Y, Y_ref)
+    assert err <= bound, (err, bound)
+    assert arm in mmq.ARM_NAMES
+
+
+# ---------------------------------------------------------------- GEMM, the five workloads at full size
+def _sample_entries(nt, od, n, seed):
+    rng = np.random.default_rng(seed)
+    ts = list(rng.integers(0, nt, n))
+    os_ = list(rng.integers(0, od, n))
+    # tile edges and the ragged tail
+    for t in {0, min(127, nt - 1), min(128, nt - 1), nt - 1}:
+        for o in {0, min(127, od - 1), min(128, od - 1), od - 1}:
+            ts.append(t)
+            os_.append(o)
+    return np.array(ts, dtype=np.int64), np.array(os_, dtype=np.int64)
+
+
+@pytest.mark.parametrize("cfg", gen.CONFIGS, ids=lambda c: c.name)
+def test_gemm_parity_workloads_sampled(mmq, cfg):
+    W, X = gen.config_inputs(cfg)
+    _, Q, Y, _ = _run(mmq, cfg.qtype, W, cfg.od, cfg.id, X)
+    Q_ref = oracle.quantize_q8_0(X)
+    assert np.array_equal(Q, Q_ref)
+    n = 3000 if cfg.id <= 4096 else 800
+    ts, os_ = _sample_entries(cfg.nt, cfg.od, n, cfg.seed)
+    y_ref = oracle.gemm_entries(QT[cfg.qtype], W, cfg.od, cfg.id, Q_ref, cfg.nt, ts, os_)
+    err, bound = _within_tol(Y[ts, os_], y_ref)
+    assert err <= bound, (err, bound)
+    assert np.isfinite(Y).all()
+
+
+# ---------------------------------------------------------------- boundary behaviour
+def test_error_codes(mmq):
+    dev = torch.device("cuda")
+    W = torch.from_numpy(gen.weights("q6_K", 8, 256, seed=1)).to(dev)
+    with pytest.raises(mmq.MMQError) as e:
+        mmq.mmq_register_weights("q6_K", W, 8, 300)
+    assert e.value.code == -1
+    with pytest.raises(mmq.MMQError) as e:
+        mmq.mmq_register_weights(7, W, 8, 256)
+    assert e.value.code == -3
+    with pytest.raises(mmq.MMQError) as e:
+        mmq.mmq_register_weights("q4_K", W, 8, 256, mmq.MMQ_REG_WEXP)
+    assert e.value.code == -7
+    # q6_K sub-block scale beyond +-64: sc*(q-32) would not be exact in fp16
+    Wb = gen.weights("q6_K", 8, 256, seed=2).reshape(8, 210)
+    Wb[3, 192 + 5] = np.uint8(np.int8(-100).view(np.uint8))
+    with pytest.raises(mmq.MMQError) as e:
+        mmq.mmq_register_weights("q6_K", torch.from_numpy(Wb.reshape(-1)).to(dev), 8, 256)
+    assert e.value.code == -7
+    # misaligned activations
+    X = torch.zeros(4 * 256 + 4, dtype=torch.float32, device=dev)
+    Qb = torch.empty(4 * 8 * 40, dtype=torch.uint8, device=dev)
+    rc = mmq.load().mmq_quantize_act(X.data_ptr() + 4, 4, 256, Qb.data_ptr(), None)
+    assert rc == -2
+    w = mmq.mmq_register_weights("q6_K", W, 8, 256)
+    Q = mmq.mmq_quantize_act(torch.zeros(4, 256, device=dev))
+    Y = torch.empty(4 * 8 + 4, dtype=torch.float32, device=dev)
+    rc = mmq.load().mmq_gemm(w.handle, Q.data_ptr(), 4, Y.data_ptr() + 4, None, 0, None)
+    assert rc == -2
+    rc = mmq.load().mmq_gemm(w.handle, Q.data_ptr(), 4, Y.data_ptr(), None, 99, None)
+    assert rc == -7
+    # nt == 0 is a no-op
+    assert mmq.load().mmq_gemm(w.handle, Q.data_ptr(), 0, Y.data_ptr(), None, 0, None) == 0
+
+
+def test_zero_and_constant_activations(mmq):
+    od, id_ = 200, 512
+    W = gen.weights("q4_K", od, id_, seed=9)
+    X = np.zeros((3, id_), dtype=np.float32)
+    X[1] = 0.75
+    X[2] = -2.0
+    _, _, Y, _ = _run(mmq, "q4_K", W, od, id_, X)
+    assert not Y[0].any()
+    Y_ref = oracle.gemm(oracle.Q4_K, W, od, id_, oracle.quantize_q8_0(X), 3)
+    err, bound = _within_tol(Y, Y_ref)
+    assert err <= bound
+
+
+def test_bounded_wait_reports_and_context_survives(mmq):
+    rc = mmq.mmq_selftest_wait_timeout(50_000_000)  # 50 ms, nothing ever arrives
+    assert rc == mmq.mmq.MMQ_ERR_DEVICE_TIMEOUT
+    assert mmq.mmq_last_device_error() == 0         # the status word was cleared
+    # the context still works
+    od, id_, nt = 128, 256, 8
+    W = gen.weights("q6_K", od, id_, seed=3)
+    X = gen.activations(nt, id_, seed=4)
+    _, _, Y, _ = _run(mmq, "q6_K", W, od, id_, X)
+    err, bound = _within_tol(Y, oracle.gemm(oracle.Q6_K, W, od, id_, oracle.quantize_q8_0(X), nt))
+    assert err <= bound
+
+
+def test_repeat_calls_are_deterministic(mmq):
+    od, id_, nt = 256, 1024, 300
+    W = gen.weights("q6_K", od, id_, seed=5)
+    X = gen.activations(nt, id_, seed=6)
+    w = mmq.mmq_register_weights("q6_K", torch.from_numpy(W).cuda(), od, id_)
+    Q = mmq.mmq_quantize_act(torch.from_numpy(X).cuda())
+    Y1 = mmq.mmq_gemm(w, Q, nt).clone()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        Y2 = mmq.mmq_gemm(w, Q, nt, stream=s)
+    s.synchronize()
+    assert torch.equal(Y1, Y2)
