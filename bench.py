@@ -1,0 +1,468 @@
+#!/usr/bin/env python
+"""Throughput of the k-quant x q8_0 prefill GEMM hot path on GB300.
+
+One step = the whole hot path over one batch of activations: q8_0
+quantization of X (mmq_quantize_act) and the GEMM against a registered
+weight (mmq_gemm).  Registration is a one-time, per-weight cost (the pages
+call its amortization infinite); it is timed once and reported separately.
+
+Default workload: q4_K q-proj, od = id = 3584, nt = 512.  Inputs rotate over
+enough independent sets (activations, weights, outputs) to exceed twice the
+L2 size, so every step reads its operands from HBM.  The K timed steps are
+captured once into a CUDA graph and launched as one; CUDA events around every
+GEMM kernel give its live average duration.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mine|reference]
+
+For N > 1 (under torchrun) each rank runs its own independent batch of the
+same workload (weak scaling, no data-path collective); rank 0 prints one JSON
+line with the whole-job throughput over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import datetime as _dt
+import glob
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "int8 TOPS and GEMM tokens/s at 1 GB300; % of roofline (q4_K/q6_K x q8_0)"
+UNIT = "TOPS"  # 2*nt*od*id integer multiply-adds counted as 2 ops, per second, / 1e12
+DEFAULT_WORKLOAD = "q4_K_qproj_3584x3584_nt512"
+# The pages' own q4_K q-proj kernel (nt=512, od=id=3584): 555 us after the
+# split-phase A staging step, i.e. 2*512*3584*3584 / 555e-6 = 23.7 TOPS, on an
+# unnamed GPU ("25 · r20: Split-phase A staging", §5).  Context only.
+PAGES_TOPS = {"q4_K_qproj_3584x3584_nt512": 2 * 512 * 3584 * 3584 / 555e-6 / 1e12}
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ---------------------------------------------------------------------- helpers
+def _env_int(name, default):
+    try:
+        return int(os.environ.get(name, default))
+    except ValueError:
+        return default
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def _sha1(path):
+    with open(path, "rb") as f:
+        return hashlib.sha1(f.read()).hexdigest()
+
+
+def _profiled_traffic(workload):
+    """DRAM bytes per GEMM launch from the committed ncu summary of this
+    workload, if it was taken on the current kernel source; else None."""
+    src = os.path.join(ROOT, "quantized_int8_gemm_gb300", "csrc", "gemm.cu")
+    sha = _sha1(src)
+    for p in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
+        text = open(p).read()
+        if workload not in text:
+            continue
+        m_sha = re.search(r"gemm_cu_sha1:\s*([0-9a-f]{40})", text)
+        m_b = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
+        if m_sha and m_b and m_sha.group(1) == sha:
+            return int(m_b.group(1))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples every 100 ms."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def stop(self, t0: float, t1: float) -> dict:
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.out.flush()
+        rows = []
+        with open(self.out.name) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    ts = _dt.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    rows.append((ts, float(parts[1]), float(parts[2]), parts[5:9]))
+                except ValueError:
+                    continue
+        os.unlink(self.out.name)
+        inwin = [r for r in rows if t0 - 0.25 <= r[0] <= t1 + 0.25]
+        use = inwin or rows
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        reasons = sorted({n for r in use for n, v in zip(self.NAMES, r[3]) if v == "Active"})
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
+                "reasons": reasons, "samples": len(use), "samples_in_timed_region": len(inwin)}
+
+
+def _gpu_uuid(dev):
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------------- CPU oracle timing
+def _oracle_sample(cfg, W, X, target_s):
+    """Time the oracle on all nt tokens x a row sample sized to ~target_s.
+    Returns (ops, seconds, n_rows)."""
+    import oracle
+    qt = oracle.Q4_K if cfg.qtype == "q4_K" else oracle.Q6_K
+    bb = 144 if cfg.qtype == "q4_K" else 210
+    row_bytes = (cfg.id // 256) * bb
+    t = time.perf_counter()
+    Q = oracle.quantize_q8_0(X)
+    tq = time.perf_counter() - t
+    probe = 2
+    t = time.perf_counter()
+    oracle.gemm(qt, W[:probe * row_bytes], probe, cfg.id, Q, cfg.nt)
+    per_row = (time.perf_counter() - t) / probe
+    n_rows = int(max(1, min(cfg.od, (target_s - tq) / max(per_row, 1e-9))))
+    t = time.perf_counter()
+    Q = oracle.quantize_q8_0(X)
+    oracle.gemm(qt, W[:n_rows * row_bytes], n_rows, cfg.id, Q, cfg.nt)
+    dt = time.perf_counter() - t
+    return 2 * cfg.nt * n_rows * cfg.id, dt, n_rows
+
+
+def run_reference(args, cfg, rank):
+    """The oracle as it stands, on the host cores.  Each step is a bounded
+    sample of the workload -- q8_0 quantization of nt_s tokens and the fp64
+    GEMM of those tokens against n_rows weight rows -- sized so the whole
+    warm-up + timed run takes about two and a half minutes."""
+    if rank != 0:
+        return
+    import oracle
+    from synth import gen
+    oracle.build()
+    W, X = gen.config_inputs(cfg)
+    qt = oracle.Q4_K if cfg.qtype == "q4_K" else oracle.Q6_K
+    row_bytes = (cfg.id // 256) * (144 if cfg.qtype == "q4_K" else 210)
+    target = max(1e-3, min(2.0, 150.0 / max(1, args.steps + args.warmup)))
+    # calibrate: quantization of all tokens, and one weight row against all tokens
+    t = time.perf_counter()
+    Qf = oracle.quantize_q8_0(X)
+    tq = time.perf_counter() - t
+    t = time.perf_counter()
+    oracle.gemm(qt, W[:2 * row_bytes], 2, cfg.id, Qf, cfg.nt)
+    t_row = (time.perf_counter() - t) / 2
+    # enough rows that the GEMM, not the quantization, dominates each step
+    n_rows = int(min(cfg.od, max(math.ceil(4 * tq / t_row), (target - tq) / t_row, 1)))
+    nt_s = int(min(cfg.nt, max(1, cfg.nt * target / (tq + t_row * n_rows))))
+    Xs = np.ascontiguousarray(X[:nt_s])
+    Ws = W[:n_rows * row_bytes]
+
+    def step():
+        Q = oracle.quantize_q8_0(Xs)
+        oracle.gemm(qt, Ws, n_rows, cfg.id, Q, nt_s)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    ops = 2 * nt_s * n_rows * cfg.id * args.steps
+    value = ops / dt / 1e12
+    sample = (f"per step: oracle q8_0 quantization of {nt_s} of {cfg.nt} tokens (id={cfg.id}) + "
+              f"fp64 GEMM of those tokens x {n_rows} of {cfg.od} weight rows, single thread")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": cfg.name, "qtype": cfg.qtype, "od": cfg.od, "id": cfg.id,
+                   "nt": cfg.nt, "sample_tokens": nt_s, "sample_rows": n_rows},
+        "tokens_per_s": value * 1e12 / (2 * cfg.od * cfg.id),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------- GPU arm
+def run_mine(args, cfg, rank, world):
+    import numpy as np
+    import torch
+
+    import quantized_int8_gemm_gb300 as mmq
+    from quantized_int8_gemm_gb300 import build as mbuild
+    from synth import gen
+
+    mbuild.build()
+    local = _env_int("LOCAL_RANK", 0)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    stream = torch.cuda.Stream()
+    nt, od, id_ = cfg.nt, cfg.od, cfg.id
+    seed = cfg.seed + 1000 * rank
+    W_host = gen.weights(cfg.qtype, od, id_, seed)
+    W_dev = torch.from_numpy(W_host).to(dev)
+
+    # ---- registration (one-time cost, timed once)
+    torch.cuda.synchronize()
+    t = time.perf_counter()
+    w0 = mmq.mmq_register_weights(cfg.qtype, W_dev, od, id_)
+    register_ms = (time.perf_counter() - t) * 1e3
+    info = mmq.mmq_weights_info(w0)
+
+    # ---- rotating input sets > 2 x L2
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    per_set = (nt * id_ * 4 + nt * (id_ // 32) * 40 + nt * od * 4 + info["operand_bytes"]
+               + info["scale_bytes"] + nt * id_ * 2 + nt * (id_ // 32) * 8)
+    n_sets = int(min(64, max(2, math.ceil(2 * l2 / per_set))))
+    ws = [w0] + [mmq.mmq_register_weights(cfg.qtype, W_dev, od, id_) for _ in range(n_sets - 1)]
+    Xs = [torch.from_numpy(gen.activations(nt, id_, seed + 7 * i, cfg.sigma, cfg.outlier_p,
+                                           cfg.outlier_scale)).to(dev) for i in range(n_sets)]
+    Qs = [torch.empty((nt, id_ // 32, 40), dtype=torch.uint8, device=dev) for _ in range(n_sets)]
+    Ys = [torch.empty((nt, od), dtype=torch.float32, device=dev) for _ in range(n_sets)]
+    del W_dev
+
+    def step(i, ev=None):
+        j = i % n_sets
+        mmq.mmq_quantize_act(Xs[j], Qs[j])
+        if ev is None:
+            mmq.mmq_gemm(ws[j], Qs[j], nt, Ys[j])
+        else:
+            mmq.mmq_gemm_profiled(ws[j], Qs[j], nt, Ys[j], ev[0], ev[1])
+
+    K, Wu = args.steps, args.warmup
+    with torch.cuda.stream(stream):
+        for i in range(Wu):
+            step(i)
+    stream.synchronize()
+    if mmq.mmq_last_device_error() != 0:
+        raise RuntimeError("device wait expired during warm-up")
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    with torch.cuda.stream(stream):
+        for a, b in evs:  # torch creates CUDA events lazily, at the first record
+            a.record()
+            b.record()
+    stream.synchronize()
+
+    # K steps captured as CUDA graphs of at most --graph-chunk steps each
+    use_graph = not args.no_graph
+    graphs = []
+    if use_graph:
+        try:
+            for c0 in range(0, K, args.graph_chunk):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    for k in range(c0, min(K, c0 + args.graph_chunk)):
+                        step(k, evs[k])
+                graphs.append(g)
+            with torch.cuda.stream(stream):
+                for g in graphs:  # untimed pass: upload and first-touch costs
+                    g.replay()
+            stream.synchronize()
+        except Exception as e:  # capture unsupported here: time eager launches
+            print(f"[bench] graph capture failed ({e}); timing eager launches", file=sys.stderr)
+            graphs, use_graph = [], False
+            torch.cuda.synchronize()
+
+    sampler = ClockSampler(_gpu_uuid(dev)).start()
+    time.sleep(0.6)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    ev_all0, ev_all1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    with torch.cuda.stream(stream):
+        ev_all0.record()
+        if graphs:
+            for g in graphs:
+                g.replay()
+        else:
+            for k in range(K):
+                step(k, evs[k])
+        ev_all1.record()
+    stream.synchronize()
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop(t_wall0, t_wall1)
+    if mmq.mmq_last_device_error() != 0:
+        raise RuntimeError("device wait expired in the timed region")
+
+    elapsed_ms = ev_all0.elapsed_time(ev_all1)
+    gemm_ms = [a.elapsed_time(b) for a, b in evs]
+    gemm_avg_ms = sum(gemm_ms) / len(gemm_ms)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    ops = cfg.ops
+    value = world * ops * K / (elapsed_ms * 1e-3) / 1e12
+    tokens_per_s = world * nt * K / (elapsed_ms * 1e-3)
+
+    # ---- roofline of the GEMM kernel (tensor-bound: fp16 UMMA carrying exact integers)
+    peaks, peak_src = _peaks()
+    long_region = elapsed_ms > 1000.0
+    peak = peaks["bf16_tflops_sustained" if long_region else "bf16_tflops"]
+    achieved = ops / (gemm_avg_ms * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": _profiled_traffic(cfg.name),
+                "peak_source": f"{peak_src} {'sustained' if long_region else 'burst'} bf16 "
+                               f"(fp16 UMMA runs at the bf16 rate)",
+                "kernel": "mmq_gemm_f16_kernel", "gemm_ms_avg": gemm_avg_ms,
+                "hbm_floor_us": (info["operand_bytes"] + nt * id_ * 2 + nt * od * 4) /
+                                (peaks["hbm_gbs"] * 1e9) * 1e6}
+
+    # ---- end to end through the C ABI with host buffers
+    e2e = None
+    if not args.no_e2e:
+        E = max(5, min(K, args.e2e_steps))
+        Xh = [torch.from_numpy(gen.activations(nt, id_, seed + 7 * i, cfg.sigma, cfg.outlier_p,
+                                               cfg.outlier_scale)).pin_memory()
+              for i in range(2)]
+        Yh = torch.empty((nt, od), dtype=torch.float32).pin_memory()
+
+        def e2e_step(i):
+            j = i % n_sets
+            Xs[j].copy_(Xh[i % 2], non_blocking=True)
+            mmq.mmq_quantize_act(Xs[j], Qs[j])
+            mmq.mmq_gemm(ws[j], Qs[j], nt, Ys[j])
+            Yh.copy_(Ys[j], non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                e2e_step(i)
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record()
+            for i in range(E):
+                e2e_step(i)
+            e1.record()
+        stream.synchronize()
+        e_ms = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([e_ms], device=dev, dtype=torch.float64)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": world * ops * E / (e_ms * 1e-3) / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": nt * id_ * 4, "d2h_bytes_per_step": nt * od * 4,
+               "steps": E, "ms_per_step": e_ms / E,
+               "path": "pinned host X -> device, mmq_quantize_act, mmq_gemm, Y -> pinned host"}
+
+    # ---- the oracle on the host cores (rank 0, N = 1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        ops_s, dt, n_rows = _oracle_sample(cfg, W_host, Xs[0].cpu().numpy(), args.cpu_seconds)
+        cpu = {"value": ops_s / dt / 1e12, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"oracle q8_0 quantization of {nt}x{id_} activations + fp64 GEMM of "
+                         f"{nt} tokens x {n_rows} of {od} weight rows, single thread, "
+                         f"{dt:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": Wu, "ms_per_step": elapsed_ms / K, "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": (value / PAGES_TOPS[cfg.name]) if cfg.name in PAGES_TOPS else None,
+            "dtype": "s8 x k-quant ints on f16 UMMA, f32 accumulate", "data": "synthetic",
+            "config": {"workload": cfg.name, "qtype": cfg.qtype, "od": od, "id": id_, "nt": nt,
+                       "step": "mmq_quantize_act + mmq_gemm",
+                       "cuda_graph": (f"{len(graphs)} graphs of <= {args.graph_chunk} steps"
+                                      if use_graph else False),
+                       "l2": f"inputs larger than L2: {n_sets} rotating sets x "
+                             f"{per_set / 2**20:.1f} MiB > 2 x {l2 / 2**20:.0f} MiB",
+                       "register_ms_once": register_ms,
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "tokens_per_s": tokens_per_s,
+            "impl": "mine",
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": 3 * K,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    for w in ws:
+        w.release()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("mine", "reference"), default="mine")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--graph-chunk", type=int, default=500)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    from synth import gen
+    cfg = gen.config_by_name(args.workload)
+    rank, world = _env_int("RANK", 0), _env_int("WORLD_SIZE", 1)
+    if args.impl == "reference":
+        run_reference(args, cfg, rank)
+    else:
+        run_mine(args, cfg, rank, world)
+
+
+if __name__ == "__main__":
+    main()

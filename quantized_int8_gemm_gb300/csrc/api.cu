@@ -28,25 +28,6 @@ DeviceState g_dev[kMaxDevices];
 std::atomic<uint64_t> g_limit_ns{2000000000ull};
 std::atomic<unsigned> g_epoch{1};
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void *p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  });
-  return fn;
-}
-
 unsigned next_epoch() {
   unsigned e = g_epoch.fetch_add(1);
   if (e == 0) e = g_epoch.fetch_add(1);  // 0 never names a launch
@@ -105,34 +86,13 @@ int cuda_rc(cudaError_t e) {
 }
 
 void free_planes(mmq_weights_s *h) {
-  if (h->b16) cudaFree(h->b16);
-  if (h->dplane) cudaFree(h->dplane);
-  if (h->mmplane) cudaFree(h->mmplane);
+  if (h->bplane) cudaFree(h->bplane);
   if (h->wexp) cudaFree(h->wexp);
-  h->b16 = nullptr;
-  h->dplane = h->mmplane = nullptr;
+  h->bplane = nullptr;
   h->wexp = nullptr;
 }
 
 }  // namespace
-
-namespace mmq {
-
-bool encode_tmap_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t inner,
-                    uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
-                    CUtensorMapSwizzle sw) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[2] = {inner, outer};
-  const cuuint64_t strides[1] = {row_bytes};
-  const cuuint32_t box[2] = {box_inner, box_outer};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-}  // namespace mmq
 
 extern "C" {
 
@@ -189,16 +149,12 @@ int mmq_register_weights(int type, const void *W, int64_t od, int64_t id, uint32
   h->od_pad = (od + mmq::kRowTile - 1) / mmq::kRowTile * mmq::kRowTile;
   h->nsb = id / MMQ_QK;
   h->nb32 = id / 32;
-  h->b16_bytes = static_cast<size_t>(h->od_pad) * id * 2;
-  h->dplane_bytes = static_cast<size_t>(h->nsb) * h->od_pad * 4;
-  h->mm_bytes = type == MMQ_Q4_K ? static_cast<size_t>(h->nb32) * h->od_pad * 4 : 0;
+  h->bplane_bytes = mmq::bplane_bytes(type, od, id);
   h->wexp_bytes = (flags & MMQ_REG_WEXP) ? static_cast<size_t>(od) * id : 0;
 
   int rc = MMQ_OK;
   int *bad = nullptr;
-  cudaError_t e = cudaMalloc(&h->b16, h->b16_bytes);
-  if (e == cudaSuccess) e = cudaMalloc(&h->dplane, h->dplane_bytes);
-  if (e == cudaSuccess && h->mm_bytes) e = cudaMalloc(&h->mmplane, h->mm_bytes);
+  cudaError_t e = cudaMalloc(&h->bplane, h->bplane_bytes);
   if (e == cudaSuccess && h->wexp_bytes) e = cudaMalloc(&h->wexp, h->wexp_bytes);
   if (e == cudaSuccess) e = cudaMalloc(&bad, sizeof(int));
   if (e == cudaSuccess) e = cudaMemsetAsync(bad, 0, sizeof(int), s);
@@ -209,23 +165,6 @@ int mmq_register_weights(int type, const void *W, int64_t od, int64_t id, uint32
   if (bad) cudaFree(bad);
   if (e != cudaSuccess) rc = cuda_rc(e);
   if (rc == MMQ_OK && bad_h) rc = MMQ_ERR_UNSUPPORTED;
-  if (rc == MMQ_OK) {
-    bool ok = mmq::encode_tmap_2d(&h->tm_b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, h->b16,
-                                  static_cast<uint64_t>(id), static_cast<uint64_t>(h->od_pad),
-                                  static_cast<uint64_t>(id) * 2, 64, mmq::kRowTile,
-                                  CU_TENSOR_MAP_SWIZZLE_128B);
-    ok = ok && mmq::encode_tmap_2d(&h->tm_d, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, h->dplane,
-                                   static_cast<uint64_t>(h->od_pad),
-                                   static_cast<uint64_t>(h->nsb),
-                                   static_cast<uint64_t>(h->od_pad) * 4, mmq::kRowTile, 1,
-                                   CU_TENSOR_MAP_SWIZZLE_NONE);
-    if (ok && h->mmplane)
-      ok = mmq::encode_tmap_2d(&h->tm_mm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, h->mmplane,
-                               static_cast<uint64_t>(h->od_pad), static_cast<uint64_t>(h->nb32),
-                               static_cast<uint64_t>(h->od_pad) * 4, mmq::kRowTile, 2,
-                               CU_TENSOR_MAP_SWIZZLE_NONE);
-    if (!ok) rc = MMQ_ERR_CUDA;
-  }
   if (rc != MMQ_OK) {
     free_planes(h);
     delete h;
@@ -261,8 +200,9 @@ int mmq_weights_info(mmq_weights_t h, int *type, int64_t *od, int64_t *id,
   if (type) *type = h->type;
   if (od) *od = h->od;
   if (id) *id = h->id;
-  if (operand_bytes) *operand_bytes = static_cast<int64_t>(h->b16_bytes);
-  if (scale_bytes) *scale_bytes = static_cast<int64_t>(h->dplane_bytes + h->mm_bytes);
+  const int64_t operand = h->od_pad * h->id * 2;
+  if (operand_bytes) *operand_bytes = operand;
+  if (scale_bytes) *scale_bytes = static_cast<int64_t>(h->bplane_bytes) - operand;
   if (wexp_bytes) *wexp_bytes = static_cast<int64_t>(h->wexp_bytes);
   return MMQ_OK;
 }
@@ -281,33 +221,21 @@ static int gemm_impl(mmq_weights_t h, const void *Q, int64_t nt, float *Y, mmq_s
   if (dev != h->device) return MMQ_ERR_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
-  const size_t a_bytes = static_cast<size_t>(nt) * h->id * 2;
-  const size_t a_pad = (a_bytes + 255) / 256 * 256;
-  const size_t sc_bytes = static_cast<size_t>(nt) * h->nb32 * 8;
   // Scratch is stream-ordered: from the library pool, or -- while the stream
   // is being captured into a CUDA graph -- a graph memory node.
   cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
   cudaError_t e = cudaStreamIsCapturing(s, &cap);
   if (e != cudaSuccess) return cuda_rc(e);
+  const bool capturing = cap == cudaStreamCaptureStatusActive;
+  const size_t bytes = mmq::gemm_scratch_bytes(h->type, nt, h->id);
   void *scratch = nullptr;
-  e = cap == cudaStreamCaptureStatusActive
-          ? cudaMallocAsync(&scratch, a_pad + sc_bytes, s)
-          : cudaMallocFromPoolAsync(&scratch, a_pad + sc_bytes, d->pool, s);
+  e = capturing ? cudaMallocAsync(&scratch, bytes, s)
+                : cudaMallocFromPoolAsync(&scratch, bytes, d->pool, s);
   if (e != cudaSuccess) return cuda_rc(e);
-  void *a16 = scratch;
-  void *scp = static_cast<uint8_t *>(scratch) + a_pad;
-
-  e = mmq::launch_gemm_prepass(static_cast<const uint8_t *>(Q), nt, h->id, a16, scp, s);
-  CUtensorMap tm_a;
-  if (e == cudaSuccess &&
-      !mmq::encode_tmap_2d(&tm_a, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a16,
-                           static_cast<uint64_t>(h->id), static_cast<uint64_t>(nt),
-                           static_cast<uint64_t>(h->id) * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
-    e = cudaErrorInvalidValue;
-  if (e == cudaSuccess && ev0) e = cudaEventRecord(ev0, s);
-  if (e == cudaSuccess)
-    e = mmq::launch_gemm_f16(h, tm_a, scp, nt, Y, d->words, next_epoch(), g_limit_ns.load(), s);
-  if (e == cudaSuccess && ev1) e = cudaEventRecord(ev1, s);
+  // inside a capture the events must become real record nodes of the graph
+  const unsigned ev_flags = capturing ? cudaEventRecordExternal : cudaEventRecordDefault;
+  e = mmq::launch_gemm(h, static_cast<const uint8_t *>(Q), nt, Y, scratch, d->words, next_epoch(),
+                       g_limit_ns.load(), s, ev0, ev1, ev_flags);
   cudaError_t ef = cudaFreeAsync(scratch, s);
   if (e == cudaSuccess) e = ef;
   return cuda_rc(e);

@@ -3,265 +3,441 @@
 // The contraction the pages run on int8 IMMA ("25 · r20: Split-phase A
 // staging", §2.2: one m16n8k32 per 4096 MACs) runs here on tcgen05 UMMA of
 // kind::f16.  sm_103a has no kind::i8, so the integers travel as fp16:
-//   A = qs in [-127, 127]           exact in fp16,
-//   B = sc*(q-32) (q6_K, |sc| <= 64) or sc*q (q4_K), |B| <= 2048, exact,
-// and every product is exact in the fp32 accumulator.  A 32-element chunk
-// sums to at most 32 * 127 * 2048 < 2^24, so the per-chunk partial
+//   A = qs in [-127, 127]                              exact in fp16
+//   B = sc*(q-32) (q6_K, |sc| <= 64) or sc*q (q4_K)    |B| <= 2048, exact
+// Every product is exact in the fp32 accumulator and a 32-element chunk sums
+// to at most 32 * 127 * 2048 < 2^24, so each per-chunk partial
 //   S[t][o][c] = sum_{k in c} qs[t][k] * B[o][k]
-// lands in TMEM exactly -- the pages' "integer sub-block dot product" with
-// the sub-block scale already applied.  The epilogue rescales each chunk:
-//   q6_K:  Y += da[t][c] * d[o][sb] * S
-//   q4_K:  Y += da[t][c] * d[o][sb] * S  -  da[t][c]*ssum[t][c] * dmin*m[o][c]
-// (the q4_K min term through ssum, the reason the pad40 block carries it).
+// lands in TMEM exactly: the pages' integer sub-block dot product with the
+// sub-block scale already applied.  The epilogue rescales in two levels:
+//   acc[t][o]  = sum_{c in sb} da'[t][c] * S[t][o][c]          (per chunk)
+//   Y'[t][o] += d[o][sb] * acc[t][o]  -  dmin[o][sb] * MIN[t][o][sb]   (per super-block)
+//   Y[t][o]   = Y'[t][o] * 2^-s_t                                (per tile)
+// The q4_K min term  sum_c da*ssum * dmin*m  runs on the tensor core: per
+// super-block one K=16 UMMA of  g' = da*ssum*2^s_t  split exactly into fp16
+// hi + lo  against the integer mins m  (MIN above); s_t is a per-token power
+// of two that keeps g' in fp16 range, and da' = da*2^s_t carries the same
+// factor so the final scaling by 2^-s_t is exact.
 //
-// Kernel shape: one 128-token x 128-row output tile per CTA, 192 threads.
-//   warp 0      TMA producer: A (fp16 activations), B (fp16 operand plane),
-//               d / dmin*m scale rows, into a 4-stage ring of 64-K stages
-//   warp 1      TMEM owner + single-thread UMMA issuer: per 32-K chunk two
-//               128x128x16 UMMAs into one of two TMEM partial buffers
-//   warps 2..5  epilogue: TMEM -> registers, per-chunk rescale into fp32
-//               accumulators (one token row per thread), then the store
-// Every wait is bounded (see ptx.cuh); a CTA that gives up drains its own
-// TMA copies and UMMAs, frees TMEM and returns.
+// Data movement: operands arrive pre-tiled and pre-swizzled (tiling.h), two
+// bulk copies per 128-K stage (activation block, weight block with its scale
+// rows), issued by two lanes of the producer warp into a 3-stage ring.
+//
+// Kernel shape: persistent, one CTA of 384 threads per SM, 128 x 128 tiles,
+// token tiles fastest so concurrently running CTAs share weight tiles in L2.
+//   warps 0..7  epilogue: warp w reads TMEM lanes 32*(w%4).. and columns
+//               64*(w/4)..: TMEM -> registers -> packed fp32x2 FMAs
+//   warp 8      producer: lane 0 the activation block, lane 1 the weight block
+//   warp 9      TMEM owner + single-thread UMMA issuer: per 32-K chunk two
+//               128x128x16 UMMAs into one slot of a 4-slot TMEM ring
+//               (+ the min-term UMMA per q4_K super-block)
+//   warps 10-11 idle (complete the register-donating warpgroup)
+// Every wait is bounded (ptx.cuh); a CTA that gives up drains its own copies
+// and UMMAs, frees TMEM and returns.
 #include <cuda_fp16.h>
+
+#include <atomic>
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "tiling.h"
 
 namespace mmq {
 namespace {
 
-constexpr int BM = 128;  // tokens per tile   (UMMA M, TMEM lanes)
-constexpr int BN = 128;  // weight rows per tile (UMMA N, TMEM columns)
-constexpr int BK = 64;   // K per pipeline stage: one 128-byte swizzle row of fp16
-constexpr int STAGES = 4;
-constexpr int EPI_WARPS = 4;
-constexpr int THREADS = 64 + 32 * EPI_WARPS;
-constexpr int TMEM_COLS = 2 * BN;  // two per-chunk partial buffers
+using namespace tiling;
 
-constexpr int A_BYTES = BM * BK * 2;
-constexpr int B_BYTES = BN * BK * 2;
-constexpr int D_BYTES = BN * 4;
-constexpr int MM_BYTES = 2 * BN * 4;
+constexpr int STAGES = 3;
+constexpr int RING = 4;  // TMEM slots of kTileN columns
+constexpr int EPI_WARPS = 8;     // warpgroups 0 and 1
+constexpr int PRODUCER_WARP = 8;  // warpgroup 2: producer, UMMA issuer, two idle warps
+constexpr int MMA_WARP = 9;
+constexpr int THREADS = 384;
+// Register split: launched at 168 per thread (384 x 168 = 64512); warpgroup 2
+// drops to 56 and the epilogue warpgroups rise to 216: 2*128*216 + 128*56 =
+// 62464 <= 64512.
+constexpr int REGS_EPI = 216;
+constexpr int REGS_CTL = 56;
+constexpr int TMEM_COLS = RING * kTileN;  // 512
 
-constexpr int A_OFF = 0;
-constexpr int B_OFF = A_OFF + STAGES * A_BYTES;
-constexpr int D_OFF = B_OFF + STAGES * B_BYTES;
-constexpr int MM_OFF = D_OFF + STAGES * D_BYTES;
-constexpr int BAR_OFF = MM_OFF + STAGES * MM_BYTES;
-constexpr int NUM_BARS = 2 * STAGES + 2 + 2 + 1;
-constexpr int SLOT_OFF = BAR_OFF + NUM_BARS * 8;
-constexpr int SMEM_USED = SLOT_OFF + 16;
-constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack for 1024-byte alignment
+template <bool kQ4>
+struct Smem {
+  static constexpr int kA = a_odd_bytes(kQ4);                          // A region per stage
+  static constexpr int kB = ((b_odd_bytes(kQ4) + 1023) / 1024) * 1024;  // B region per stage
+  static constexpr int kStage = kA + kB;
+  static constexpr int kBar = STAGES * kStage;
+  static constexpr int kNumBars = 2 * STAGES + 2 * RING + 1;
+  static constexpr int kSlot = kBar + kNumBars * 8;
+  static constexpr int kUsed = kSlot + 16;
+  static constexpr int kBytes = kUsed + 1024;  // slack for 1024-byte alignment
+  static_assert(kA % 1024 == 0 && kStage % 1024 == 0, "stage buffers must keep 1 KB alignment");
+  static_assert(kBytes <= 227 * 1024, "shared memory budget");
+};
 
-static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle atoms need 1 KB alignment");
-static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
-
-// pad40 -> fp16 operand a16[t][k] = qs, and per (t, c) {da, da*ssum}.
-__global__ void __launch_bounds__(256) gemm_prepass_kernel(const uint8_t *__restrict__ Q,
-                                                           int64_t nblocks,
-                                                           __half *__restrict__ a16,
-                                                           float2 *__restrict__ sc) {
-  const int64_t b = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (b >= nblocks) return;
-  const uint2 *src = reinterpret_cast<const uint2 *>(Q + b * MMQ_Q8_BLOCK_BYTES);
-  const uint2 w0 = __ldg(src + 0), w1 = __ldg(src + 1), w2 = __ldg(src + 2),
-              w3 = __ldg(src + 3), w4 = __ldg(src + 4);
-  // byte 0..1 d16 | 4..35 qs | 36..39 ssum
-  const uint32_t qw[8] = {w0.y, w1.x, w1.y, w2.x, w2.y, w3.x, w3.y, w4.x};
-  uint4 *dst = reinterpret_cast<uint4 *>(a16 + b * 32);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    __half h[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const uint32_t w = qw[2 * i + (j >> 2)];
-      h[j] = __int2half_rn(static_cast<int8_t>((w >> (8 * (j & 3))) & 0xFF));
-    }
-    dst[i] = *reinterpret_cast<const uint4 *>(h);
-  }
-  const float da = __half2float(__ushort_as_half(static_cast<unsigned short>(w0.x & 0xFFFFu)));
-  const int ssum = static_cast<int>(w4.y);
-  sc[b] = make_float2(da, da * static_cast<float>(ssum));  // exact: 11 x 13 bits
+// ---------------------------------------------------------------- small helpers
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
 }
 
-template <bool kQ4K>
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cnt(uint32_t bar, uint32_t cnt) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(cnt) : "memory");
+}
+
+// Shared-memory descriptor for the 32-byte-swizzled K=16 min-term images:
+// rows of 32 B, 8-row groups 256 B apart, swizzle mode 6 (32 B).
+__device__ __forceinline__ uint64_t sdesc_kmajor_sw32(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(1) << 16;
+  d |= static_cast<uint64_t>(256 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(6) << 61;
+  return d;
+}
+
+// ---------------------------------------------------------------- activation prepass
+// One warp per token t < nt: pad40 blocks -> the token's row of every
+// activation block (fp16 qs, swizzled), da' = da*2^s_t, inv = 2^-s_t, and for
+// q4_K the min-term image slots hi/lo of g' = da*ssum*2^s_t.
+template <bool kQ4>
+__global__ void __launch_bounds__(256) gemm_prepass_kernel(const uint8_t *__restrict__ Q,
+                                                           int64_t nt, int64_t nb32,
+                                                           uint8_t *__restrict__ aplane,
+                                                           float *__restrict__ dap,
+                                                           float *__restrict__ invp) {
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= nt) return;
+  const uint8_t *qrow = Q + t * nb32 * MMQ_Q8_BLOCK_BYTES;
+  const int64_t nsb = nb32 / 8;
+  int s = 0;
+  if (kQ4) {  // s_t: largest |g| of the token lands in [2^14, 2^15)
+    float gmax = 0.f;
+    for (int64_t c = lane; c < nb32; c += 32) {
+      const uint8_t *b = qrow + c * MMQ_Q8_BLOCK_BYTES;
+      const float da = __half2float(__ushort_as_half(*reinterpret_cast<const unsigned short *>(b)));
+      const int ssum = *reinterpret_cast<const int *>(b + MMQ_Q8_SSUM_OFF);
+      gmax = fmaxf(gmax, fabsf(da * static_cast<float>(ssum)));
+    }
+#pragma unroll
+    for (int m = 16; m; m >>= 1) gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, m));
+    if (gmax > 0.f) {
+      const int e = static_cast<int>((__float_as_uint(gmax) >> 23) & 0xFF) - 127;
+      s = min(30, max(-30, 14 - e));
+    }
+  }
+  const float scale = __uint_as_float(static_cast<uint32_t>(127 + s) << 23);
+  const int r = static_cast<int>(t & (kTileM - 1));
+  const int64_t tile = t / kTileM;
+  if (lane == 0) invp[t] = __uint_as_float(static_cast<uint32_t>(127 - s) << 23);
+  for (int64_t c = lane; c < nb32; c += 32) {
+    const uint2 *src = reinterpret_cast<const uint2 *>(qrow + c * MMQ_Q8_BLOCK_BYTES);
+    const uint2 w0 = __ldg(src + 0), w1 = __ldg(src + 1), w2 = __ldg(src + 2),
+                w3 = __ldg(src + 3), w4 = __ldg(src + 4);
+    const uint32_t qw[8] = {w0.y, w1.x, w1.y, w2.x, w2.y, w3.x, w3.y, w4.x};
+    const int64_t sb = c >> 3;
+    const int half = static_cast<int>((c >> 2) & 1);
+    uint8_t *blk = aplane + a_block(tile, sb, half, nsb, kQ4);
+    const int k0 = static_cast<int>(c & 3) * 32;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      __half h[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t w = qw[2 * q + (j >> 2)];
+        h[j] = __int2half_rn(static_cast<int8_t>((w >> (8 * (j & 3))) & 0xFF));
+      }
+      *reinterpret_cast<uint4 *>(blk + operand_off(r, k0 + 8 * q)) =
+          *reinterpret_cast<const uint4 *>(h);
+    }
+    const float da = __half2float(__ushort_as_half(static_cast<unsigned short>(w0.x & 0xFFFFu)));
+    dap[t * nb32 + c] = da * scale;
+    if (kQ4) {
+      const float g = da * static_cast<float>(static_cast<int>(w4.y)) * scale;  // exact
+      const __half hi = __float2half_rn(g);
+      const __half lo = __float2half_rn(g - __half2float(hi));
+      uint8_t *mblk = aplane + a_block(tile, sb, 1, nsb, true) + kAMin;
+      const uint32_t pair = static_cast<uint32_t>(__half_as_ushort(hi)) |
+                            (static_cast<uint32_t>(__half_as_ushort(lo)) << 16);
+      *reinterpret_cast<uint32_t *>(mblk + min_off(r, 2 * static_cast<int>(c & 7))) = pair;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- the GEMM
+template <bool kQ4>
 __global__ void __launch_bounds__(THREADS, 1)
-    mmq_gemm_f16_kernel(const __grid_constant__ CUtensorMap tm_a,
-                        const __grid_constant__ CUtensorMap tm_b,
-                        const __grid_constant__ CUtensorMap tm_d,
-                        const __grid_constant__ CUtensorMap tm_mm, const float2 *__restrict__ sc,
-                        int64_t nt, int64_t od, int64_t nb32, float *__restrict__ Y,
-                        WaitCtl wctl) {
+    mmq_gemm_kernel(const uint8_t *__restrict__ aplane, const uint8_t *__restrict__ bplane,
+                    const float *__restrict__ dap, const float *__restrict__ invp, int64_t nt,
+                    int64_t od, int64_t nb32, int n_tt, int n_ot, float *__restrict__ Y,
+                    WaitCtl wctl) {
+  using L = Smem<kQ4>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t *smem = smem_raw + (base - raw);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t o0 = static_cast<int64_t>(blockIdx.x) * BN;
-  const int64_t t0 = static_cast<int64_t>(blockIdx.y) * BM;
-  const int nkb = static_cast<int>(nb32 / 2);
+  const int64_t nsb = nb32 / 8;
+  const int n_tiles = n_tt * n_ot;
 
-  const uint32_t bar = base + BAR_OFF;
+  const uint32_t bar = base + L::kBar;
   auto full = [&](int s) { return bar + 8u * s; };
   auto empty = [&](int s) { return bar + 8u * (STAGES + s); };
-  auto tfull = [&](int b) { return bar + 8u * (2 * STAGES + b); };
-  auto tempty = [&](int b) { return bar + 8u * (2 * STAGES + 2 + b); };
-  const uint32_t done = bar + 8u * (2 * STAGES + 4);
+  auto rfull = [&](int i) { return bar + 8u * (2 * STAGES + i); };
+  auto rempty = [&](int i) { return bar + 8u * (2 * STAGES + RING + i); };
+  const uint32_t done = bar + 8u * (2 * STAGES + 2 * RING);
+  auto a_smem = [&](int s) { return base + s * L::kStage; };
+  auto b_smem = [&](int s) { return base + s * L::kStage + L::kA; };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full(s), 1);
-      mbar_init(empty(s), 1 + EPI_WARPS);  // UMMA commit + epilogue warps (scale reads)
+      mbar_init(empty(s), 1 + EPI_WARPS);  // UMMA commit + 8 epilogue arrivals (scale reads)
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(tfull(b), 1);
-      mbar_init(tempty(b), EPI_WARPS);
+    for (int i = 0; i < RING; ++i) {
+      mbar_init(rfull(i), 1);
+      mbar_init(rempty(i), EPI_WARPS);
     }
     mbar_init(done, 1);
     fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tm_a);
-    tma_prefetch_desc(&tm_b);
-    tma_prefetch_desc(&tm_d);
-    if (kQ4K) tma_prefetch_desc(&tm_mm);
-  }
-  if (warp == 1) {
-    tmem_alloc(base + SLOT_OFF, TMEM_COLS);
+  if (warp == MMA_WARP) {
+    tmem_alloc(base + L::kSlot, TMEM_COLS);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tbase = *reinterpret_cast<volatile uint32_t *>(smem + SLOT_OFF);
-
-  if (warp == 0) {
+  const uint32_t tbase = *reinterpret_cast<volatile uint32_t *>(smem + L::kSlot);
+  if (warp >= PRODUCER_WARP) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_CTL));
+  if (warp == PRODUCER_WARP) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      constexpr uint32_t kTx = A_BYTES + B_BYTES + D_BYTES + (kQ4K ? MM_BYTES : 0);
-      int issued = 0;
+    if (lane < 2) {
+      uint32_t ks = 0, issued = 0;
       bool ok = true;
-      for (int kb = 0; kb < nkb; ++kb) {
-        const int s = kb % STAGES;
-        if (!mbar_wait(empty(s), ((kb / STAGES) & 1) ^ 1, wctl)) {
-          ok = false;
-          break;
+      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+        const int tt = tile % n_tt, ot = tile / n_tt;
+        for (int64_t sb = 0; sb < nsb && ok; ++sb) {
+          for (int half = 0; half < 2; ++half, ++ks) {
+            const int s = static_cast<int>(ks % STAGES);
+            if (!mbar_wait(empty(s), ((ks / STAGES) & 1) ^ 1, wctl)) {
+              ok = false;
+              break;
+            }
+            const uint32_t ab = half ? a_odd_bytes(kQ4) : a_even_bytes();
+            const uint32_t bb = half ? b_odd_bytes(kQ4) : b_even_bytes();
+            if (lane == 0) {
+              mbar_arrive_expect_tx(full(s), ab + bb);
+              bulk_load(a_smem(s), aplane + a_block(tt, sb, half, nsb, kQ4), ab, full(s));
+            } else {
+              bulk_load(b_smem(s), bplane + b_block(ot, sb, half, nsb, kQ4), bb, full(s));
+            }
+            issued = ks + 1;
+          }
         }
-        mbar_arrive_expect_tx(full(s), kTx);
-        tma_load_2d(base + A_OFF + s * A_BYTES, &tm_a, full(s), kb * BK, static_cast<int>(t0));
-        tma_load_2d(base + B_OFF + s * B_BYTES, &tm_b, full(s), kb * BK, static_cast<int>(o0));
-        tma_load_2d(base + D_OFF + s * D_BYTES, &tm_d, full(s), static_cast<int>(o0), kb / 4);
-        if (kQ4K)
-          tma_load_2d(base + MM_OFF + s * MM_BYTES, &tm_mm, full(s), static_cast<int>(o0), kb * 2);
-        issued = kb + 1;
       }
-      if (!ok)  // drain the copies still in flight before the CTA exits
-        for (int kb = issued > STAGES ? issued - STAGES : 0; kb < issued; ++kb)
-          mbar_wait(full(kb % STAGES), (kb / STAGES) & 1, wctl, false);
+      if (!ok)  // drain this CTA's copies still in flight
+        for (uint32_t k = issued > STAGES ? issued - STAGES : 0; k < issued; ++k)
+          mbar_wait(full(k % STAGES), (k / STAGES) & 1, wctl, false);
     }
-  } else if (warp == 1) {
+  } else if (warp == MMA_WARP) {
     // ------------------------------------------------------------ UMMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_f16_f32(BM, BN);
+      constexpr uint32_t idesc = idesc_f16_f32(kTileM, kTileN);
+      uint32_t ks = 0, u = 0;
       bool ok = true;
-      for (int kb = 0; kb < nkb && ok; ++kb) {
-        const int s = kb % STAGES;
-        if (!mbar_wait(full(s), (kb / STAGES) & 1, wctl)) {
-          ok = false;
-          break;
-        }
+      auto next_slot = [&](uint32_t &slot) {
+        slot = u % RING;
+        if (!mbar_wait(rempty(slot), ((u / RING) & 1) ^ 1, wctl)) return false;
         tc_fence_after();
-        const uint32_t a_s = base + A_OFF + s * A_BYTES;
-        const uint32_t b_s = base + B_OFF + s * B_BYTES;
-        for (int h = 0; h < 2; ++h) {
-          const int c = kb * 2 + h, buf = c & 1;
-          if (!mbar_wait(tempty(buf), ((c >> 1) & 1) ^ 1, wctl)) {
-            ok = false;
-            break;
+        return true;
+      };
+      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+        for (int64_t sb = 0; sb < nsb && ok; ++sb) {
+          for (int half = 0; half < 2 && ok; ++half, ++ks) {
+            const int s = static_cast<int>(ks % STAGES);
+            if (!mbar_wait(full(s), (ks / STAGES) & 1, wctl)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t as = a_smem(s), bs = b_smem(s);
+            for (int c = 0; c < 4 && ok; ++c) {
+              uint32_t slot;
+              if (!(ok = next_slot(slot))) break;
+              const uint32_t off = (c >> 1) * 16384 + (c & 1) * 64;
+              umma_f16(tbase + slot * kTileN, sdesc_kmajor_sw128(as + off),
+                       sdesc_kmajor_sw128(bs + off), idesc, 0);
+              umma_f16(tbase + slot * kTileN, sdesc_kmajor_sw128(as + off + 32),
+                       sdesc_kmajor_sw128(bs + off + 32), idesc, 1);
+              umma_commit(rfull(slot));
+              ++u;
+            }
+            if (ok && kQ4 && half == 1) {
+              uint32_t slot;
+              if ((ok = next_slot(slot))) {
+                umma_f16(tbase + slot * kTileN, sdesc_kmajor_sw32(as + kAMin),
+                         sdesc_kmajor_sw32(bs + kBMin), idesc, 0);
+                umma_commit(rfull(slot));
+                ++u;
+              }
+            }
+            if (!ok) break;
+            umma_commit(empty(s));
+            if (half == 0) mbar_arrive_cnt(empty(s), EPI_WARPS);  // epilogue reads odd stages only
           }
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < 2; ++kk) {
-            const uint32_t koff = (h * 2 + kk) * 32;  // 16 fp16 of K per UMMA
-            umma_f16(tbase + buf * BN, sdesc_kmajor_sw128(a_s + koff),
-                     sdesc_kmajor_sw128(b_s + koff), idesc, kk);
-          }
-          umma_commit(tfull(buf));
         }
-        if (ok) umma_commit(empty(s));
       }
       umma_commit(done);  // every UMMA of this CTA has finished once `done` flips
       mbar_wait(done, 0, wctl, false);
     }
+  }
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS_EPI));
     // ------------------------------------------------------------ epilogue
-    const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
+    const int quad = warp & 3;
+    const int chalf = warp >> 2;  // column half 0 / 1
     const int row = quad * 32 + lane;
-    const int64_t t = t0 + row;
-    const bool trow = t < nt;
-    const float2 *scrow = sc + (trow ? t : 0) * nb32;
-    const uint32_t trow_addr = tbase + (static_cast<uint32_t>(quad * 32) << 16);
-    float acc[BN];
-#pragma unroll
-    for (int j = 0; j < BN; ++j) acc[j] = 0.f;
-    float2 s_cur = trow ? __ldg(scrow) : make_float2(0.f, 0.f);
+    const uint32_t taddr = tbase + (static_cast<uint32_t>(quad * 32) << 16) + chalf * 64;
+    uint32_t ks = 0, u = 0;
     bool ok = true;
-    for (int kb = 0; kb < nkb && ok; ++kb) {
-      const int s = kb % STAGES;
-      ok = __all_sync(0xffffffffu, mbar_wait(full(s), (kb / STAGES) & 1, wctl));
-      if (!ok) break;
-      const float *dsc = reinterpret_cast<const float *>(smem + D_OFF + s * D_BYTES);
-      const float *mm = reinterpret_cast<const float *>(smem + MM_OFF + s * MM_BYTES);
-      for (int h = 0; h < 2; ++h) {
-        const int c = kb * 2 + h, buf = c & 1;
-        const float2 s_nxt =
-            (trow && c + 1 < nb32) ? __ldg(scrow + c + 1) : make_float2(0.f, 0.f);
-        ok = __all_sync(0xffffffffu, mbar_wait(tfull(buf), (c >> 1) & 1, wctl));
-        if (!ok) break;
-        tc_fence_after();
+    // Wait for the next ring slot; false (after recording) if the wait expired.
+    auto acquire = [&](uint32_t &slot) {
+      slot = u % RING;
+      const bool got = __all_sync(0xffffffffu, mbar_wait(rfull(slot), (u / RING) & 1, wctl));
+      if (got) tc_fence_after();
+      return got;
+    };
+    auto release = [&](uint32_t slot) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(rempty(slot));
+      ++u;
+    };
+    for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+      const int tt = tile % n_tt, ot = tile / n_tt;
+      const int64_t t = static_cast<int64_t>(tt) * kTileM + row;  // < nt_pad: planes are padded
+      const int64_t o0 = static_cast<int64_t>(ot) * kTileN + chalf * 64;
+      float2 y[32], acc[32];
 #pragma unroll
-        for (int cb = 0; cb < BN / 32; ++cb) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(trow_addr + buf * BN + cb * 32, r);
-          tmem_wait_ld();
+      for (int j = 0; j < 32; ++j) y[j] = make_float2(0.f, 0.f);
+      const float4 *darow = reinterpret_cast<const float4 *>(dap + t * nb32);
+      for (int64_t sb = 0; sb < nsb && ok; ++sb) {
+        const float4 d0 = __ldg(darow + 2 * sb), d1 = __ldg(darow + 2 * sb + 1);
+        const float das[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          uint32_t slot;
+          if (!(ok = acquire(slot))) break;
+          const float2 da2 = make_float2(das[c], das[c]);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int col = cb * 32 + j;
-            float a = acc[col];
-            if (kQ4K) a = fmaf(-s_cur.y, mm[h * BN + col], a);
-            acc[col] = fmaf(s_cur.x * dsc[col], __uint_as_float(r[j]), a);
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(taddr + slot * kTileN + hh * 32, r);
+            tmem_wait_ld();
+            if (c == 0) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                acc[hh * 16 + j] =
+                    fmul2(da2, make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])));
+            } else {
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                acc[hh * 16 + j] = ffma2(
+                    da2, make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])),
+                    acc[hh * 16 + j]);
+            }
           }
+          release(slot);
         }
-        tc_fence_before();
+        if (!ok) break;
+        ks += 1;  // the even stage of this super-block; the odd one holds d (and dmin)
+        const int s = static_cast<int>(ks % STAGES);
+        ok = __all_sync(0xffffffffu, mbar_wait(full(s), (ks / STAGES) & 1, wctl));
+        if (!ok) break;
+        const float *bsm = reinterpret_cast<const float *>(smem + s * L::kStage + L::kA);
+        const float2 *d2 = reinterpret_cast<const float2 *>(bsm + kBD / 4 + chalf * 64);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) y[j] = ffma2(d2[j], acc[j], y[j]);
+        if (kQ4) {
+          uint32_t slot;
+          if (!(ok = acquire(slot))) break;
+          const float2 *dm2 = reinterpret_cast<const float2 *>(bsm + kBDmin / 4 + chalf * 64);
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(taddr + slot * kTileN + hh * 32, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float2 dm = dm2[hh * 16 + j];
+              y[hh * 16 + j] = ffma2(make_float2(-dm.x, -dm.y),
+                                     make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])),
+                                     y[hh * 16 + j]);
+            }
+          }
+          release(slot);
+        }
+        // the stage's scale rows were read through the generic proxy; order
+        // those reads before the TMA (async proxy) that refills the buffer
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
-        if (lane == 0) mbar_arrive(tempty(buf));
-        s_cur = s_nxt;
+        if (lane == 0) mbar_arrive(empty(s));
+        ks += 1;
       }
       if (!ok) break;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty(s));
-    }
-    if (ok && trow) {
-      float *yrow = Y + t * od + o0;
-      if ((od & 3) == 0) {
+      if (t < nt) {
+        const float inv = __ldg(invp + t);
+        const float2 inv2 = make_float2(inv, inv);
+        float *yrow = Y + t * od + o0;
+        if ((od & 3) == 0) {
 #pragma unroll
-        for (int j = 0; j < BN; j += 4)
-          if (o0 + j < od)
-            *reinterpret_cast<float4 *>(yrow + j) =
-                make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
-      } else {
+          for (int j = 0; j < 32; j += 2) {
+            if (o0 + 2 * j < od) {
+              const float2 a = fmul2(y[j], inv2), b = fmul2(y[j + 1], inv2);
+              *reinterpret_cast<float4 *>(yrow + 2 * j) = make_float4(a.x, a.y, b.x, b.y);
+            }
+          }
+        } else {
 #pragma unroll
-        for (int j = 0; j < BN; ++j)
-          if (o0 + j < od) yrow[j] = acc[j];
+          for (int j = 0; j < 32; ++j) {
+            const float2 a = fmul2(y[j], inv2);
+            if (o0 + 2 * j < od) yrow[2 * j] = a.x;
+            if (o0 + 2 * j + 1 < od) yrow[2 * j + 1] = a.y;
+          }
+        }
       }
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == MMA_WARP) {
     tc_fence_after();
     tmem_dealloc(tbase, TMEM_COLS);
   }
@@ -279,31 +455,73 @@ __global__ void wait_selftest_kernel(WaitCtl wctl) {
   }
 }
 
+int g_num_sms[64];
+
 }  // namespace
 
-cudaError_t launch_gemm_prepass(const uint8_t *Q, int64_t nt, int64_t id, void *a16, void *sc,
-                                cudaStream_t s) {
-  const int64_t nblocks = nt * (id / 32);
-  const int bs = 256;
-  gemm_prepass_kernel<<<static_cast<unsigned>((nblocks + bs - 1) / bs), bs, 0, s>>>(
-      Q, nblocks, static_cast<__half *>(a16), static_cast<float2 *>(sc));
-  return cudaGetLastError();
+size_t gemm_scratch_bytes(int type, int64_t nt, int64_t id) {
+  const bool q4 = type == MMQ_Q4_K;
+  const int64_t n_tt = (nt + kTileM - 1) / kTileM, nt_pad = n_tt * kTileM;
+  const int64_t nsb = id / MMQ_QK, nb32 = id / 32;
+  const size_t a = static_cast<size_t>(n_tt * nsb) * a_pair_bytes(q4);
+  const size_t da = static_cast<size_t>(nt_pad * nb32) * 4;
+  const size_t inv = static_cast<size_t>(nt_pad) * 4;
+  return ((a + 255) / 256 + (da + 255) / 256 + (inv + 255) / 256) * 256;
 }
 
-cudaError_t launch_gemm_f16(const mmq_weights_s *h, const CUtensorMap &tm_a, const void *sc,
-                            int64_t nt, float *Y, DevStatus *st, unsigned epoch,
-                            uint64_t limit_ns, cudaStream_t s) {
+cudaError_t launch_gemm(const mmq_weights_s *h, const uint8_t *Q, int64_t nt, float *Y,
+                        void *scratch, DevStatus *st, unsigned epoch, uint64_t limit_ns,
+                        cudaStream_t s, cudaEvent_t ev0, cudaEvent_t ev1, unsigned ev_flags) {
   const bool q4 = h->type == MMQ_Q4_K;
-  auto kern = q4 ? mmq_gemm_f16_kernel<true> : mmq_gemm_f16_kernel<false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       SMEM_BYTES);
+  const int64_t n_tt = (nt + kTileM - 1) / kTileM, nt_pad = n_tt * kTileM;
+  const int64_t nsb = h->nsb, nb32 = h->nb32;
+  const size_t a_bytes = static_cast<size_t>(n_tt * nsb) * a_pair_bytes(q4);
+  uint8_t *aplane = static_cast<uint8_t *>(scratch);
+  float *dap = reinterpret_cast<float *>(aplane + (a_bytes + 255) / 256 * 256);
+  float *invp = dap + ((static_cast<size_t>(nt_pad * nb32) * 4 + 255) / 256 * 64);
+
+  // the last token tile's padding rows must read as zero
+  cudaError_t e = cudaSuccess;
+  if (nt_pad != nt) {
+    const uint64_t tail = static_cast<uint64_t>((n_tt - 1) * nsb) * a_pair_bytes(q4);
+    e = cudaMemsetAsync(aplane + tail, 0, a_bytes - tail, s);
+    if (e == cudaSuccess)
+      e = cudaMemsetAsync(dap + nt * nb32, 0, static_cast<size_t>((nt_pad - nt) * nb32) * 4, s);
+    if (e == cudaSuccess)
+      e = cudaMemsetAsync(invp + nt, 0, static_cast<size_t>(nt_pad - nt) * 4, s);
+    if (e != cudaSuccess) return e;
+  }
+  const unsigned pgrid = static_cast<unsigned>((nt + 7) / 8);
+  if (q4)
+    gemm_prepass_kernel<true><<<pgrid, 256, 0, s>>>(Q, nt, nb32, aplane, dap, invp);
+  else
+    gemm_prepass_kernel<false><<<pgrid, 256, 0, s>>>(Q, nt, nb32, aplane, dap, invp);
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const dim3 grid(static_cast<unsigned>(h->od_pad / BN), static_cast<unsigned>((nt + BM - 1) / BM));
+
+  auto kern = q4 ? mmq_gemm_kernel<true> : mmq_gemm_kernel<false>;
+  const int smem = q4 ? Smem<true>::kBytes : Smem<false>::kBytes;
+  // the shared-memory opt-in and the SM count are read once per device,
+  // outside any stream capture the first call is not part of
+  static std::atomic<uint32_t> attr_done[64][2];
+  const int dev = h->device;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_done[dev][q4].load()) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g_num_sms[dev], cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    attr_done[dev][q4].store(1);
+  }
+  const int n_ot = static_cast<int>(h->od_pad / kTileN);
+  const int n_tiles = static_cast<int>(n_tt) * n_ot;
+  const int grid = n_tiles < g_num_sms[dev] ? n_tiles : g_num_sms[dev];
   WaitCtl w{&st->status, &st->abort_epoch, epoch, limit_ns};
-  kern<<<grid, THREADS, SMEM_BYTES, s>>>(tm_a, h->tm_b, h->tm_d, q4 ? h->tm_mm : h->tm_d,
-                                         static_cast<const float2 *>(sc), nt, h->od, h->nb32, Y,
-                                         w);
-  return cudaGetLastError();
+  if (ev0 && (e = cudaEventRecordWithFlags(ev0, s, ev_flags)) != cudaSuccess) return e;
+  kern<<<grid, THREADS, smem, s>>>(aplane, static_cast<const uint8_t *>(h->bplane), dap, invp, nt,
+                                   h->od, nb32, static_cast<int>(n_tt), n_ot, Y, w);
+  e = cudaGetLastError();
+  if (e == cudaSuccess && ev1) e = cudaEventRecordWithFlags(ev1, s, ev_flags);
+  return e;
 }
 
 cudaError_t launch_wait_selftest(DevStatus *st, unsigned epoch, uint64_t limit_ns,

@@ -1,24 +1,30 @@
 // register.cu -- one-time expansion of packed k-quant weights.
 //
 // The pages move the q6_K recombination out of the GEMM loop into a
-// registration-time plane ("46 · r43 — PC-sampling attribution", §3.2; the
-// dense layout contract of "47 · r44 — W_exp stride mismatch root cause",
-// §2.2).  Here registration writes, per weight element (o, k):
-//   b16[o][k]      fp16 operand with the sub-block scale folded in
-//                  q6_K: sc[k/16] * (q - 32)   (|.| <= 64*32, exact in fp16)
-//                  q4_K: sc[k/32] * q          (<= 63*15, exact in fp16)
-//   wexp[o*id + k] int8 q - 32 (q6_K, optional): the pages' dense W_exp,
-//                  row pitch id, super-block pitch 256
-// and per block the fp32 scale planes dplane[sb][o] = d and (q4_K)
-// mmplane[sb*8 + j][o] = dmin * m_j.
+// registration-time plane ("46 · r43 — PC-sampling attribution", §3.2) with
+// a dense layout contract ("47 · r44 — W_exp stride mismatch root cause",
+// §2.2: element (j, sb, e) at j*id + sb*256 + e).  Registration here writes
+// the GEMM's pre-tiled weight plane (tiling.h), per weight element (o, k):
+//   operand  fp16  q6_K: sc[k/16] * (q - 32)   (|.| <= 64*32, exact)
+//                  q4_K: sc[k/32] * q          (<= 63*15, exact)
+// and per (row, super-block) the fp32 scale d, plus for q4_K dmin and the
+// integer mins m of the eight sub-blocks (the min-term image).
+//
+// With MMQ_REG_WEXP the dense centered-int8 plane wexp[o*id + k] = q - 32 is
+// written first and the q6_K operand is then built by reading it back with
+// the dense strides, so every GEMM run on such a handle checks the plane's
+// offsets (the pages' consumer-side gate), not only its bytes.
 //
 // One CTA of 256 threads per packed block, thread e = element e.
 #include <cuda_fp16.h>
 
 #include "internal.h"
+#include "tiling.h"
 
 namespace mmq {
 namespace {
+
+using namespace tiling;
 
 // q6_K element e: low nibble from ql[(e/128)*64 + e%64] (nibble (e%128)/64),
 // 2-bit high part from qh[(e/128)*32 + e%32] (field (e%128)/32).
@@ -40,74 +46,90 @@ __device__ __forceinline__ void q4k_scale_min(const uint8_t *s, int j, int &sc, 
   }
 }
 
-__global__ void __launch_bounds__(256) register_q6k_kernel(
-    const uint8_t *__restrict__ W, int64_t od, int64_t id, int64_t od_pad, __half *__restrict__ b16,
-    float *__restrict__ dplane, int8_t *__restrict__ wexp, int *__restrict__ bad_scale) {
+__device__ __forceinline__ float f16_at(const uint8_t *p) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(p[0] | (p[1] << 8))));
+}
+
+// dense W_exp plane, element (o, sb*256 + e) at o*id + sb*256 + e
+__global__ void __launch_bounds__(256) expand_wexp_kernel(const uint8_t *__restrict__ W,
+                                                          int64_t id, int8_t *__restrict__ wexp) {
   __shared__ uint8_t blk[MMQ_Q6K_BLOCK_BYTES + 2];
   const int64_t nsb = id / MMQ_QK;
   const int64_t o = blockIdx.x, sb = blockIdx.y;
-  const uint8_t *src = W + (o * nsb + sb) * MMQ_Q6K_BLOCK_BYTES;
   const int e = threadIdx.x;
-  if (e < MMQ_Q6K_BLOCK_BYTES) blk[e] = src[e];
+  if (e < MMQ_Q6K_BLOCK_BYTES) blk[e] = W[(o * nsb + sb) * MMQ_Q6K_BLOCK_BYTES + e];
   __syncthreads();
-  const int c = q6k_centered(blk, e);
-  const int sc = static_cast<int8_t>(blk[MMQ_Q6K_SC_OFF + (e >> 4)]);
-  const int64_t k = sb * MMQ_QK + e;
-  b16[o * id + k] = __int2half_rn(sc * c);
-  if (wexp) wexp[o * id + k] = static_cast<int8_t>(c);
-  if ((e & 15) == 0 && (sc > 64 || sc < -64)) atomicOr(bad_scale, 1);
-  if (e == 0) {
-    const __half d = __ushort_as_half(static_cast<unsigned short>(
-        blk[MMQ_Q6K_D_OFF] | (blk[MMQ_Q6K_D_OFF + 1] << 8)));
-    dplane[sb * od_pad + o] = __half2float(d);
-  }
+  wexp[o * id + sb * MMQ_QK + e] = static_cast<int8_t>(q6k_centered(blk, e));
 }
 
-__global__ void __launch_bounds__(256) register_q4k_kernel(
-    const uint8_t *__restrict__ W, int64_t od, int64_t id, int64_t od_pad, __half *__restrict__ b16,
-    float *__restrict__ dplane, float *__restrict__ mmplane) {
-  __shared__ uint8_t blk[MMQ_Q4K_BLOCK_BYTES];
+template <bool kQ4, bool kFromWexp>
+__global__ void __launch_bounds__(256) register_kernel(const uint8_t *__restrict__ W,
+                                                       const int8_t *__restrict__ wexp, int64_t id,
+                                                       uint8_t *__restrict__ bplane,
+                                                       int *__restrict__ bad_scale) {
+  constexpr int kBytes = kQ4 ? MMQ_Q4K_BLOCK_BYTES : MMQ_Q6K_BLOCK_BYTES;
+  __shared__ uint8_t blk[kBytes + 2];
   const int64_t nsb = id / MMQ_QK;
   const int64_t o = blockIdx.x, sb = blockIdx.y;
-  const uint8_t *src = W + (o * nsb + sb) * MMQ_Q4K_BLOCK_BYTES;
   const int e = threadIdx.x;
-  if (e < MMQ_Q4K_BLOCK_BYTES) blk[e] = src[e];
+  if (e < kBytes) blk[e] = W[(o * nsb + sb) * kBytes + e];
   __syncthreads();
-  const int j = e >> 5;
-  const int byte = blk[MMQ_Q4K_QS_OFF + 32 * (j >> 1) + (e & 31)];
-  const int q = (j & 1) ? (byte >> 4) : (byte & 0xF);
-  int sc, m;
-  q4k_scale_min(blk + MMQ_Q4K_SC_OFF, j, sc, m);
-  b16[o * id + sb * MMQ_QK + e] = __int2half_rn(sc * q);
-  if ((e & 31) == 0) {
-    const float dmin = __half2float(__ushort_as_half(static_cast<unsigned short>(
-        blk[MMQ_Q4K_DMIN_OFF] | (blk[MMQ_Q4K_DMIN_OFF + 1] << 8))));
-    mmplane[(sb * 8 + j) * od_pad + o] = dmin * static_cast<float>(m);  // exact: 11 x 6 bits
+  const int64_t ot = o / kTileN;
+  const int r = static_cast<int>(o % kTileN);
+  const int half = e >> 7, k = e & 127;
+  uint8_t *dst = bplane + b_block(ot, sb, half, nsb, kQ4);
+  uint8_t *odd = bplane + b_block(ot, sb, 1, nsb, kQ4);
+  int val;
+  float d;
+  if constexpr (kQ4) {
+    const int j = e >> 5;
+    const int byte = blk[MMQ_Q4K_QS_OFF + 32 * (j >> 1) + (e & 31)];
+    const int q = (j & 1) ? (byte >> 4) : (byte & 0xF);
+    int sc, m;
+    q4k_scale_min(blk + MMQ_Q4K_SC_OFF, j, sc, m);
+    val = sc * q;
+    d = f16_at(blk + MMQ_Q4K_D_OFF);
+    if ((e & 31) == 0) {  // min image: slots 2j and 2j+1 both hold m_j
+      const uint32_t mh = __half_as_ushort(__int2half_rn(m));
+      *reinterpret_cast<uint32_t *>(odd + kBMin + min_off(r, 2 * j)) = mh | (mh << 16);
+    }
+    if (e == 0)
+      reinterpret_cast<float *>(odd + kBDmin)[r] = f16_at(blk + MMQ_Q4K_DMIN_OFF);
+  } else {
+    int c;
+    if constexpr (kFromWexp) c = wexp[o * id + sb * MMQ_QK + e];
+    else c = q6k_centered(blk, e);
+    const int sc = static_cast<int8_t>(blk[MMQ_Q6K_SC_OFF + (e >> 4)]);
+    if ((e & 15) == 0 && (sc > 64 || sc < -64)) atomicOr(bad_scale, 1);
+    val = sc * c;
+    d = f16_at(blk + MMQ_Q6K_D_OFF);
   }
-  if (e == 0) {
-    dplane[sb * od_pad + o] = __half2float(__ushort_as_half(
-        static_cast<unsigned short>(blk[MMQ_Q4K_D_OFF] | (blk[MMQ_Q4K_D_OFF + 1] << 8))));
-  }
+  *reinterpret_cast<__half *>(dst + operand_off(r, k)) = __int2half_rn(val);
+  if (k == 0) reinterpret_cast<float *>(dst + kBD)[r] = d;
 }
 
 }  // namespace
 
+size_t bplane_bytes(int type, int64_t od, int64_t id) {
+  const bool q4 = type == MMQ_Q4_K;
+  const int64_t n_ot = (od + kTileN - 1) / kTileN;
+  return static_cast<size_t>(n_ot * (id / MMQ_QK)) * b_pair_bytes(q4);
+}
+
 cudaError_t launch_register(const mmq_weights_s *h, const uint8_t *W, int *bad_scale,
                             cudaStream_t s) {
-  // padded rows and padding columns of the scale planes stay zero
-  cudaError_t e = cudaMemsetAsync(h->b16, 0, h->b16_bytes, s);
-  if (e == cudaSuccess) e = cudaMemsetAsync(h->dplane, 0, h->dplane_bytes, s);
-  if (e == cudaSuccess && h->mmplane) e = cudaMemsetAsync(h->mmplane, 0, h->mm_bytes, s);
+  // rows od..od_pad-1 of the last weight tile stay zero
+  cudaError_t e = cudaMemsetAsync(h->bplane, 0, h->bplane_bytes, s);
   if (e != cudaSuccess) return e;
   const dim3 grid(static_cast<unsigned>(h->od), static_cast<unsigned>(h->nsb));
-  if (h->type == MMQ_Q6_K) {
-    register_q6k_kernel<<<grid, 256, 0, s>>>(W, h->od, h->id, h->od_pad,
-                                             static_cast<__half *>(h->b16), h->dplane, h->wexp,
-                                             bad_scale);
+  uint8_t *bp = static_cast<uint8_t *>(h->bplane);
+  if (h->type == MMQ_Q4_K) {
+    register_kernel<true, false><<<grid, 256, 0, s>>>(W, nullptr, h->id, bp, bad_scale);
+  } else if (h->wexp) {
+    expand_wexp_kernel<<<grid, 256, 0, s>>>(W, h->id, h->wexp);
+    register_kernel<false, true><<<grid, 256, 0, s>>>(W, h->wexp, h->id, bp, bad_scale);
   } else {
-    register_q4k_kernel<<<grid, 256, 0, s>>>(W, h->od, h->id, h->od_pad,
-                                             static_cast<__half *>(h->b16), h->dplane,
-                                             h->mmplane);
+    register_kernel<false, false><<<grid, 256, 0, s>>>(W, nullptr, h->id, bp, bad_scale);
   }
   return cudaGetLastError();
 }

@@ -1,0 +1,77 @@
+// tiling.h -- the pre-tiled operand planes the GEMM streams with 1-D bulk
+// copies, defined once for their producers (registration, activation
+// prepass) and their consumer (the GEMM kernel).
+//
+// The GEMM runs 128 (tokens) x 128 (weight rows) output tiles over K in
+// stages of 128; two stages make one 256-element super-block.  Every
+// (tile, super-block, half) owns one contiguous block in global memory laid
+// out exactly as the kernel's shared-memory stage buffer, so one bulk copy
+// per operand per stage moves it.
+//
+// Operand image (both A and B): two K-blocks of 64 fp16 (k = 0..63, 64..127
+// of the stage), each 128 rows x 128 B with the 128-byte swizzle that UMMA's
+// SWIZZLE_128B descriptor expects: row r of a K-block at (r/8)*1024 + (r%8)*128,
+// its 16-byte chunk j stored at chunk position j ^ (r%8).
+//
+// Min-term image (q4_K, odd half only): 128 rows x 16 fp16 (32 B per row)
+// with the 32-byte swizzle (SWIZZLE_32B descriptor): row r at
+// (r/8)*256 + (r%8)*32, 16-byte chunk j stored at j ^ ((r%8)/4).
+//   A side: slot 2c = hi(g'), slot 2c+1 = lo(g') of 32-chunk c of the super-block
+//   B side: slots 2c and 2c+1 both = m (the 6-bit min of sub-block c)
+//
+// Block layouts (byte offsets inside one block):
+//   A even: [operand 32768]
+//   A odd : [operand 32768][q4_K: A min 4096]
+//   B even: [operand 32768][d 128 x f32]
+//   B odd : [operand 32768][d 128 x f32][q4_K: dmin 128 x f32][q4_K: B min 4096]
+// Blocks of one tile are ordered (super-block, half).
+#pragma once
+#include <cstdint>
+
+namespace mmq {
+namespace tiling {
+
+constexpr int kTileM = 128;  // tokens per tile
+constexpr int kTileN = 128;  // weight rows per tile
+constexpr int kStageK = 128;
+constexpr int kOperandBytes = kTileM * kStageK * 2;  // 32768 (kTileM == kTileN)
+constexpr int kMinBytes = 128 * 32;                  // 4096
+constexpr int kScaleBytes = kTileN * 4;              // 512
+
+__host__ __device__ constexpr int a_even_bytes() { return kOperandBytes; }
+__host__ __device__ constexpr int a_odd_bytes(bool q4) { return kOperandBytes + (q4 ? kMinBytes : 0); }
+__host__ __device__ constexpr int b_even_bytes() { return kOperandBytes + kScaleBytes; }
+__host__ __device__ constexpr int b_odd_bytes(bool q4) {
+  return kOperandBytes + kScaleBytes + (q4 ? kScaleBytes + kMinBytes : 0);
+}
+__host__ __device__ constexpr int a_pair_bytes(bool q4) { return a_even_bytes() + a_odd_bytes(q4); }
+__host__ __device__ constexpr int b_pair_bytes(bool q4) { return b_even_bytes() + b_odd_bytes(q4); }
+
+// offsets inside B blocks
+constexpr int kBD = kOperandBytes;                    // d
+constexpr int kBDmin = kOperandBytes + kScaleBytes;   // dmin (odd, q4_K)
+constexpr int kBMin = kOperandBytes + 2 * kScaleBytes;  // B min image (odd, q4_K)
+constexpr int kAMin = kOperandBytes;                  // A min image (odd, q4_K)
+
+// byte offset of element (row, k) of a stage operand image, k in [0, 128)
+__host__ __device__ constexpr uint32_t operand_off(int row, int k) {
+  return static_cast<uint32_t>((k >> 6) * 16384 + (row >> 3) * 1024 + (row & 7) * 128 +
+                               ((((k & 63) >> 3) ^ (row & 7)) << 4) + (k & 7) * 2);
+}
+// byte offset of slot j in [0,16) of row r in a min-term image
+__host__ __device__ constexpr uint32_t min_off(int row, int j) {
+  return static_cast<uint32_t>((row >> 3) * 256 + (row & 7) * 32 +
+                               (((j >> 3) ^ ((row & 7) >> 2)) << 4) + (j & 7) * 2);
+}
+// first byte of block (tile, sb, half) in a plane of `nsb` super-blocks per tile
+__host__ __device__ constexpr uint64_t a_block(int64_t tile, int64_t sb, int half, int64_t nsb,
+                                               bool q4) {
+  return static_cast<uint64_t>((tile * nsb + sb) * a_pair_bytes(q4) + (half ? a_even_bytes() : 0));
+}
+__host__ __device__ constexpr uint64_t b_block(int64_t tile, int64_t sb, int half, int64_t nsb,
+                                               bool q4) {
+  return static_cast<uint64_t>((tile * nsb + sb) * b_pair_bytes(q4) + (half ? b_even_bytes() : 0));
+}
+
+}  // namespace tiling
+}  // namespace mmq

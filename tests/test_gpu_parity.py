@@ -113,6 +113,21 @@ def test_gemm_parity_full_compare(mmq, name, od, id_, nt, seed):
     assert arm in mmq.ARM_NAMES
 
 
+@pytest.mark.parametrize("od,id_,nt", [(256, 256, 130), (300, 768, 129), (131, 3584, 64)])
+def test_gemm_consumes_wexp_plane_with_dense_strides(mmq, od, id_, nt):
+    """Offsets gate for the pre-expanded plane: with MMQ_REG_WEXP the q6_K
+    operand is rebuilt from the dense W_exp plane, so the GEMM only matches
+    the oracle if the plane is read with row pitch id and super-block pitch
+    256 (a padded-pitch read shifts every row but row 0)."""
+    W = gen.weights("q6_K", od, id_, seed=300 + od)
+    X = gen.activations(nt, id_, seed=301 + od)
+    w, Q, Y, _ = _run(mmq, "q6_K", W, od, id_, X, flags=mmq.MMQ_REG_WEXP)
+    assert np.array_equal(mmq.mmq_weights_wexp(w).cpu().numpy(), oracle.expand_q6k_dense(W, od, id_))
+    Y_ref = oracle.gemm(oracle.Q6_K, W, od, id_, oracle.quantize_q8_0(X), nt)
+    err, bound = _within_tol(Y, Y_ref)
+    assert err <= bound, (err, bound)
+
+
 # ---------------------------------------------------------------- GEMM, the five workloads at full size
 def _sample_entries(nt, od, n, seed):
     rng = np.random.default_rng(seed)
@@ -199,6 +214,21 @@ def test_bounded_wait_reports_and_context_survives(mmq):
     _, _, Y, _ = _run(mmq, "q6_K", W, od, id_, X)
     err, bound = _within_tol(Y, oracle.gemm(oracle.Q6_K, W, od, id_, oracle.quantize_q8_0(X), nt))
     assert err <= bound
+
+
+@pytest.mark.parametrize("name,od,id_,nt", [("q6_K", 3584, 18944, 2630), ("q4_K", 18944, 3584, 2630)])
+def test_persistent_tiles_deterministic_with_outliers(mmq, name, od, id_, nt):
+    """Many tiles per persistent CTA, outlier activations: repeated runs must
+    agree bit for bit (a stage buffer refilled too early shows up here first)."""
+    W = gen.weights(name, od, id_, seed=7)
+    X = gen.activations(nt, id_, seed=8, outlier_p=0.01, outlier_scale=20.0)
+    w = mmq.mmq_register_weights(name, torch.from_numpy(W).cuda(), od, id_)
+    Q = mmq.mmq_quantize_act(torch.from_numpy(X).cuda())
+    Y0 = mmq.mmq_gemm(w, Q, nt).clone()
+    for _ in range(3):
+        assert torch.equal(mmq.mmq_gemm(w, Q, nt), Y0)
+    assert mmq.mmq_last_device_error() == 0
+    w.release()
 
 
 def test_repeat_calls_are_deterministic(mmq):
