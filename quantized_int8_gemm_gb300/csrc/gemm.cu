@@ -28,9 +28,10 @@
 //   warps 0..7  epilogue: warp w reads TMEM lanes 32*(w%4).. and columns
 //               64*(w/4)..: TMEM -> registers -> packed fp32x2 FMAs
 //   warp 8      producer: lane 0 the activation block, lane 1 the weight block
-//   warp 9      TMEM owner + single-thread UMMA issuer: per 32-K chunk two
-//               128x128x16 UMMAs into one slot of a 4-slot TMEM ring
-//               (+ the min-term UMMA per q4_K super-block)
+//   warp 9      TMEM owner + UMMA issuer (one elected lane of a warp-uniform
+//               loop): per 32-K chunk two 128x128x16 UMMAs; chunks go in pairs
+//               into a ring of two TMEM slot pairs, one commit per pair
+//               (+ the min-term UMMA per q4_K super-block, in a pair of its own)
 //   warps 10-11 idle (complete the register-donating warpgroup)
 // Every wait is bounded (ptx.cuh); a CTA that gives up drains its own copies
 // and UMMAs, frees TMEM and returns.
@@ -48,7 +49,7 @@ namespace {
 using namespace tiling;
 
 constexpr int STAGES = 3;
-constexpr int RING = 4;  // TMEM slots of kTileN columns
+constexpr int RING = 2;  // TMEM slot pairs, 2 x kTileN columns each (one hand-off per 2 chunks)
 constexpr int EPI_WARPS = 8;     // warpgroups 0 and 1
 constexpr int PRODUCER_WARP = 8;  // warpgroup 2: producer, UMMA issuer, two idle warps
 constexpr int MMA_WARP = 9;
@@ -58,7 +59,7 @@ constexpr int THREADS = 384;
 // 62464 <= 64512.
 constexpr int REGS_EPI = 216;
 constexpr int REGS_CTL = 56;
-constexpr int TMEM_COLS = RING * kTileN;  // 512
+constexpr int TMEM_COLS = RING * 2 * kTileN;  // 512
 
 template <bool kQ4>
 struct Smem {
@@ -237,85 +238,101 @@ __global__ void __launch_bounds__(THREADS, 1)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_CTL));
   if (warp == PRODUCER_WARP) {
     // ------------------------------------------------------------ producer
-    if (lane < 2) {
-      uint32_t ks = 0, issued = 0;
-      bool ok = true;
-      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-        const int tt = tile % n_tt, ot = tile / n_tt;
-        for (int64_t sb = 0; sb < nsb && ok; ++sb) {
-          for (int half = 0; half < 2; ++half, ++ks) {
-            const int s = static_cast<int>(ks % STAGES);
-            if (!mbar_wait(empty(s), ((ks / STAGES) & 1) ^ 1, wctl)) {
-              ok = false;
-              break;
-            }
-            const uint32_t ab = half ? a_odd_bytes(kQ4) : a_even_bytes();
-            const uint32_t bb = half ? b_odd_bytes(kQ4) : b_even_bytes();
-            if (lane == 0) {
-              mbar_arrive_expect_tx(full(s), ab + bb);
-              bulk_load(a_smem(s), aplane + a_block(tt, sb, half, nsb, kQ4), ab, full(s));
-            } else {
-              bulk_load(b_smem(s), bplane + b_block(ot, sb, half, nsb, kQ4), bb, full(s));
-            }
-            issued = ks + 1;
+    // The whole warp runs the loop (warp-uniform control flow); lane 0 copies
+    // the activation block, lane 1 the weight block.
+    uint32_t ks = 0, issued = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+      const int tt = tile % n_tt, ot = tile / n_tt;
+      for (int64_t sb = 0; sb < nsb && ok; ++sb) {
+        for (int half = 0; half < 2; ++half, ++ks) {
+          const int s = static_cast<int>(ks % STAGES);
+          ok = __all_sync(0xffffffffu, mbar_wait(empty(s), ((ks / STAGES) & 1) ^ 1, wctl));
+          if (!ok) break;
+          const uint32_t ab = half ? a_odd_bytes(kQ4) : a_even_bytes();
+          const uint32_t bb = half ? b_odd_bytes(kQ4) : b_even_bytes();
+          if (lane == 0) {
+            mbar_arrive_expect_tx(full(s), ab + bb);
+            bulk_load(a_smem(s), aplane + a_block(tt, sb, half, nsb, kQ4), ab, full(s));
+          } else if (lane == 1) {
+            bulk_load(b_smem(s), bplane + b_block(ot, sb, half, nsb, kQ4), bb, full(s));
           }
+          __syncwarp();
+          issued = ks + 1;
         }
       }
-      if (!ok)  // drain this CTA's copies still in flight
-        for (uint32_t k = issued > STAGES ? issued - STAGES : 0; k < issued; ++k)
-          mbar_wait(full(k % STAGES), (k / STAGES) & 1, wctl, false);
     }
+    if (!ok)  // drain this CTA's copies still in flight
+      for (uint32_t k = issued > STAGES ? issued - STAGES : 0; k < issued; ++k)
+        mbar_wait(full(k % STAGES), (k / STAGES) & 1, wctl, false);
   } else if (warp == MMA_WARP) {
     // ------------------------------------------------------------ UMMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_f16_f32(kTileM, kTileN);
-      uint32_t ks = 0, u = 0;
-      bool ok = true;
-      auto next_slot = [&](uint32_t &slot) {
-        slot = u % RING;
-        if (!mbar_wait(rempty(slot), ((u / RING) & 1) ^ 1, wctl)) return false;
-        tc_fence_after();
-        return true;
-      };
-      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-        for (int64_t sb = 0; sb < nsb && ok; ++sb) {
-          for (int half = 0; half < 2 && ok; ++half, ++ks) {
-            const int s = static_cast<int>(ks % STAGES);
-            if (!mbar_wait(full(s), (ks / STAGES) & 1, wctl)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t as = a_smem(s), bs = b_smem(s);
-            for (int c = 0; c < 4 && ok; ++c) {
-              uint32_t slot;
-              if (!(ok = next_slot(slot))) break;
-              const uint32_t off = (c >> 1) * 16384 + (c & 1) * 64;
-              umma_f16(tbase + slot * kTileN, sdesc_kmajor_sw128(as + off),
-                       sdesc_kmajor_sw128(bs + off), idesc, 0);
-              umma_f16(tbase + slot * kTileN, sdesc_kmajor_sw128(as + off + 32),
-                       sdesc_kmajor_sw128(bs + off + 32), idesc, 1);
-              umma_commit(rfull(slot));
-              ++u;
-            }
-            if (ok && kQ4 && half == 1) {
-              uint32_t slot;
-              if ((ok = next_slot(slot))) {
-                umma_f16(tbase + slot * kTileN, sdesc_kmajor_sw32(as + kAMin),
-                         sdesc_kmajor_sw32(bs + kBMin), idesc, 0);
-                umma_commit(rfull(slot));
-                ++u;
+    // The whole warp runs the loop and waits; one elected lane issues the
+    // UMMAs and commits (keeps the issue path warp-uniform).  Chunks go in
+    // pairs into a ring of two slot pairs: one hand-off per 64 of K.
+    uint32_t elected;
+    asm volatile("{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(elected));
+    constexpr uint32_t idesc = idesc_f16_f32(kTileM, kTileN);
+    constexpr uint64_t kStageDesc = L::kStage >> 4;  // descriptor address field step per stage
+    const uint64_t a0 = sdesc_kmajor_sw128(a_smem(0)), b0 = sdesc_kmajor_sw128(b_smem(0));
+    const uint64_t am0 = sdesc_kmajor_sw32(a_smem(0) + kAMin), bm0 = sdesc_kmajor_sw32(b_smem(0) + kBMin);
+    uint32_t ks = 0, p = 0;
+    bool ok = true;
+    auto next_pair = [&](uint32_t &ps) {
+      ps = p % RING;
+      const bool got = __all_sync(0xffffffffu, mbar_wait(rempty(ps), ((p / RING) & 1) ^ 1, wctl));
+      if (got) tc_fence_after();
+      return got;
+    };
+    for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+      for (int64_t sb = 0; sb < nsb && ok; ++sb) {
+        for (int half = 0; half < 2 && ok; ++half, ++ks) {
+          const int s = static_cast<int>(ks % STAGES);
+          ok = __all_sync(0xffffffffu, mbar_wait(full(s), (ks / STAGES) & 1, wctl));
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t as = a0 + s * kStageDesc, bs = b0 + s * kStageDesc;
+#pragma unroll
+          for (int cp = 0; cp < 2; ++cp) {
+            uint32_t ps;
+            if (!(ok = next_pair(ps))) break;
+            if (elected) {
+#pragma unroll
+              for (int cc = 0; cc < 2; ++cc) {
+                const int c = 2 * cp + cc;  // chunk in the stage: K = 32c .. 32c+31
+                const uint64_t off = (c >> 1) * (16384 >> 4) + (c & 1) * (64 >> 4);
+                const uint32_t d = tbase + (ps * 2 + cc) * kTileN;
+                umma_f16(d, as + off, bs + off, idesc, 0);
+                umma_f16(d, as + off + 2, bs + off + 2, idesc, 1);
               }
+              umma_commit(rfull(ps));
             }
-            if (!ok) break;
+            __syncwarp();
+            ++p;
+          }
+          if (ok && kQ4 && half == 1) {
+            uint32_t ps;
+            if ((ok = next_pair(ps))) {
+              if (elected) {
+                umma_f16(tbase + ps * 2 * kTileN, am0 + s * kStageDesc, bm0 + s * kStageDesc, idesc, 0);
+                umma_commit(rfull(ps));
+              }
+              __syncwarp();
+              ++p;
+            }
+          }
+          if (!ok) break;
+          if (elected) {
             umma_commit(empty(s));
             if (half == 0) mbar_arrive_cnt(empty(s), EPI_WARPS);  // epilogue reads odd stages only
           }
+          __syncwarp();
         }
       }
-      umma_commit(done);  // every UMMA of this CTA has finished once `done` flips
-      mbar_wait(done, 0, wctl, false);
     }
+    if (elected) umma_commit(done);  // every UMMA of this CTA has finished once `done` flips
+    mbar_wait(done, 0, wctl, false);
   }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS_EPI));
@@ -326,17 +343,17 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t taddr = tbase + (static_cast<uint32_t>(quad * 32) << 16) + chalf * 64;
     uint32_t ks = 0, u = 0;
     bool ok = true;
-    // Wait for the next ring slot; false (after recording) if the wait expired.
-    auto acquire = [&](uint32_t &slot) {
-      slot = u % RING;
-      const bool got = __all_sync(0xffffffffu, mbar_wait(rfull(slot), (u / RING) & 1, wctl));
+    // Wait for the next slot pair; false (after recording) if the wait expired.
+    auto acquire = [&](uint32_t &ps) {
+      ps = u % RING;
+      const bool got = __all_sync(0xffffffffu, mbar_wait(rfull(ps), (u / RING) & 1, wctl));
       if (got) tc_fence_after();
       return got;
     };
-    auto release = [&](uint32_t slot) {
+    auto release = [&](uint32_t ps) {
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(rempty(slot));
+      if (lane == 0) mbar_arrive(rempty(ps));
       ++u;
     };
     for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
@@ -350,30 +367,33 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int64_t sb = 0; sb < nsb && ok; ++sb) {
         const float4 d0 = __ldg(darow + 2 * sb), d1 = __ldg(darow + 2 * sb + 1);
         const float das[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
-#pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
-          uint32_t slot;
-          if (!(ok = acquire(slot))) break;
-          const float2 da2 = make_float2(das[c], das[c]);
+        // Four 32-column quarters per slot pair (chunk c then c+1, low then
+        // high columns), software-pipelined: the load of quarter q+1 is in
+        // flight while quarter q is folded into acc.
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(taddr + slot * kTileN + hh * 32, r);
-            tmem_wait_ld();
-            if (c == 0) {
+        for (int c = 0; c < 8; c += 2) {
+          uint32_t ps;
+          if (!(ok = acquire(ps))) break;
+          uint32_t r[2][32];
+          tmem_ld_32x32b_x32(taddr + (ps * 2) * kTileN, r[0]);
+          tmem_wait_ld(r[0]);
 #pragma unroll
-              for (int j = 0; j < 16; ++j)
-                acc[hh * 16 + j] =
-                    fmul2(da2, make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])));
-            } else {
+          for (int q = 0; q < 4; ++q) {
+            if (q < 3)
+              tmem_ld_32x32b_x32(taddr + (ps * 2 + ((q + 1) >> 1)) * kTileN + ((q + 1) & 1) * 32,
+                                 r[(q + 1) & 1]);
+            const int cc = c + (q >> 1);
+            const float2 da2 = make_float2(das[cc], das[cc]);
+            const uint32_t(&v)[32] = r[q & 1];
 #pragma unroll
-              for (int j = 0; j < 16; ++j)
-                acc[hh * 16 + j] = ffma2(
-                    da2, make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])),
-                    acc[hh * 16 + j]);
+            for (int j = 0; j < 16; ++j) {
+              const float2 x = make_float2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+              float2 &a = acc[(q & 1) * 16 + j];
+              a = cc == 0 ? fmul2(da2, x) : ffma2(da2, x, a);
             }
+            if (q < 3) tmem_wait_ld(r[(q + 1) & 1]);
+            if (q == 2) release(ps);  // every quarter of the pair is in registers
           }
-          release(slot);
         }
         if (!ok) break;
         ks += 1;  // the even stage of this super-block; the odd one holds d (and dmin)
@@ -385,14 +405,15 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int j = 0; j < 32; ++j) y[j] = ffma2(d2[j], acc[j], y[j]);
         if (kQ4) {
-          uint32_t slot;
-          if (!(ok = acquire(slot))) break;
+          uint32_t ps;
+          if (!(ok = acquire(ps))) break;
           const float2 *dm2 = reinterpret_cast<const float2 *>(bsm + kBDmin / 4 + chalf * 64);
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
             uint32_t r[32];
-            tmem_ld_32x32b_x32(taddr + slot * kTileN + hh * 32, r);
-            tmem_wait_ld();
+            tmem_ld_32x32b_x32(taddr + ps * 2 * kTileN + hh * 32, r);
+            tmem_wait_ld(r);
+            if (hh == 1) release(ps);
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               const float2 dm = dm2[hh * 16 + j];
@@ -401,7 +422,6 @@ __global__ void __launch_bounds__(THREADS, 1)
                                      y[hh * 16 + j]);
             }
           }
-          release(slot);
         }
         // the stage's scale rows were read through the generic proxy; order
         // those reads before the TMA (async proxy) that refills the buffer
