@@ -46,6 +46,7 @@ typedef struct mmq_weights_s *mmq_weights_t;
 #define MMQ_ERR_OOM -6             /* device allocation failed */
 #define MMQ_ERR_UNSUPPORTED -7     /* valid input this build does not handle */
 #define MMQ_ERR_NO_DEVICE -8       /* current device is not a GB300 (sm_103) */
+#define MMQ_ERR_SCRATCH_LIMIT -9   /* problem exceeds mmq_gemm_noalloc's fixed scratch */
 
 /* ---- weight types (ggml numbering) ------------------------------------- */
 #define MMQ_Q4_K 12
@@ -177,6 +178,33 @@ int mmq_gemm(mmq_weights_t h, const void *Q, int64_t nt, float *Y, mmq_stream_t 
  */
 int mmq_gemm_profiled(mmq_weights_t h, const void *Q, int64_t nt, float *Y, mmq_stream_t stream,
                       uint32_t flags, int *arm_used, void *ev_start, void *ev_stop);
+
+/*
+ * mmq_gemm_noalloc -- mmq_gemm for callers that cannot allocate device
+ * memory: a caller whose GPU memory is entirely owned by another allocator
+ * (for example a framework's caching allocator that reserved the device),
+ * or one on a path where cudaMalloc's implicit device synchronization is not
+ * acceptable.  The log pages have no counterpart to this entry point.
+ * It allocates nothing: its scratch is a fixed 16 MiB device array compiled
+ * into the library, which every device that loads the library holds until
+ * the process exits.  The caller still passes Q and Y (as for mmq_gemm) and
+ * a handle from mmq_register_weights, which must have run on the current
+ * device first.
+ *   - Problems whose scratch exceeds 16 MiB are rejected with
+ *     MMQ_ERR_SCRATCH_LIMIT.  Scratch per token, with nt rounded up to a
+ *     multiple of 128: id*2 + (id/32)*4 + 4 bytes, plus (id/256)*32 for q4_K;
+ *     e.g. id = 3584 allows up to 2048 (q4_K) or 2176 (q6_K) tokens.
+ *   - The first call on a device looks up the array's device address (once
+ *     per device); make that first call before any stream capture.
+ *   - Every call shares the one array, which keeps the previous call's
+ *     contents; each call rewrites or clears everything it reads.  Calls
+ *     that can overlap on the GPU (different streams, no ordering) race on
+ *     the array: order them on one stream or with events.
+ * Always runs the MMQ_ARM_F16 arm.  Errors: MMQ_ERR_ARG, MMQ_ERR_ALIGN,
+ * MMQ_ERR_SCRATCH_LIMIT, MMQ_ERR_NO_DEVICE, MMQ_ERR_CUDA; a device timeout is
+ * reported by mmq_last_device_error().
+ */
+int mmq_gemm_noalloc(mmq_weights_t h, const void *Q, int64_t nt, float *Y, mmq_stream_t stream);
 
 /* Synchronizes the current device, then returns and clears the device status
  * word: MMQ_OK, or MMQ_ERR_DEVICE_TIMEOUT if a bounded wait expired since

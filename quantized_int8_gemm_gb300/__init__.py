@@ -14,6 +14,7 @@ from .mmq import (  # noqa: F401
     Weights,
     load,
     mmq_gemm,
+    mmq_gemm_noalloc,
     mmq_gemm_profiled,
     mmq_last_device_error,
     mmq_quantize_act,

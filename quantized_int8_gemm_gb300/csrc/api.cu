@@ -107,6 +107,8 @@ const char *mmq_strerror(int code) {
     case MMQ_ERR_OOM: return "device out of memory";
     case MMQ_ERR_UNSUPPORTED: return "unsupported input for this build";
     case MMQ_ERR_NO_DEVICE: return "current device is not an sm_103 GPU";
+    case MMQ_ERR_SCRATCH_LIMIT:
+      return "problem needs more scratch than mmq_gemm_noalloc's fixed 16 MiB buffer";
     default: return "unknown status code";
   }
 }
@@ -250,6 +252,36 @@ int mmq_gemm_profiled(mmq_weights_t h, const void *Q, int64_t nt, float *Y, mmq_
                       uint32_t flags, int *arm_used, void *ev_start, void *ev_stop) {
   return gemm_impl(h, Q, nt, Y, stream, flags, arm_used, static_cast<cudaEvent_t>(ev_start),
                    static_cast<cudaEvent_t>(ev_stop));
+}
+
+int mmq_gemm_noalloc(mmq_weights_t h, const void *Q, int64_t nt, float *Y, mmq_stream_t stream) {
+  if (!h || nt < 0 || nt > kMaxTokens) return MMQ_ERR_ARG;
+  if (nt == 0) return MMQ_OK;
+  if (!Q || !Y) return MMQ_ERR_ARG;
+  if (!aligned16(Q) || !aligned16(Y)) return MMQ_ERR_ALIGN;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return MMQ_ERR_NO_DEVICE;
+  }
+  if (dev != h->device) return MMQ_ERR_ARG;
+  // A valid handle means registration already set up this device's state;
+  // look it up without ever initialising (initialising would allocate).
+  DeviceState *d = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_dev[dev].usable) d = &g_dev[dev];
+  }
+  if (!d) return MMQ_ERR_ARG;
+  if (mmq::gemm_scratch_bytes(h->type, nt, h->id) > mmq::kNoallocScratchBytes)
+    return MMQ_ERR_SCRATCH_LIMIT;
+  void *scratch = nullptr;
+  cudaError_t e = mmq::noalloc_scratch(dev, &scratch);
+  if (e == cudaSuccess)
+    e = mmq::launch_gemm(h, static_cast<const uint8_t *>(Q), nt, Y, scratch, d->words,
+                         next_epoch(), g_limit_ns.load(), reinterpret_cast<cudaStream_t>(stream),
+                         nullptr, nullptr, cudaEventRecordDefault);
+  return cuda_rc(e);
 }
 
 int mmq_last_device_error(void) {

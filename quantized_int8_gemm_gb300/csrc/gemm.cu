@@ -38,6 +38,7 @@
 #include <cuda_fp16.h>
 
 #include <atomic>
+#include <mutex>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -478,6 +479,29 @@ __global__ void wait_selftest_kernel(WaitCtl wctl) {
 int g_num_sms[64];
 
 }  // namespace
+
+// Scratch for mmq_gemm_noalloc: a fixed device array in this module, so that
+// entry point allocates nothing.  Every device that loads the library holds
+// it until the process exits.  Its contents persist between calls; the
+// launch below clears every part that must start at zero.
+__device__ __align__(256) uint8_t g_noalloc_scratch[kNoallocScratchBytes];
+
+cudaError_t noalloc_scratch(int dev, void **out) {
+  // host code sees g_noalloc_scratch only as a stand-in: fetch the real
+  // device address once per device, with that device current
+  static void *addr[64];
+  static std::mutex mu;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!addr[dev]) {
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return cudaSuccess;
+}
 
 size_t gemm_scratch_bytes(int type, int64_t nt, int64_t id) {
   const bool q4 = type == MMQ_Q4_K;

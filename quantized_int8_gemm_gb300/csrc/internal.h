@@ -55,4 +55,8 @@ cudaError_t launch_gemm(const mmq_weights_s *h, const uint8_t *Q, int64_t nt, fl
 cudaError_t launch_wait_selftest(DevStatus *st, unsigned epoch, uint64_t limit_ns,
                                  cudaStream_t s);
 
+// Fixed scratch of mmq_gemm_noalloc (a static device array in gemm.cu).
+constexpr size_t kNoallocScratchBytes = size_t(16) << 20;
+cudaError_t noalloc_scratch(int dev, void **out);
+
 }  // namespace mmq

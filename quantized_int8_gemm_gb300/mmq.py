@@ -25,6 +25,7 @@ MMQ_ERR_DEVICE_TIMEOUT = -5
 MMQ_ERR_OOM = -6
 MMQ_ERR_UNSUPPORTED = -7
 MMQ_ERR_NO_DEVICE = -8
+MMQ_ERR_SCRATCH_LIMIT = -9
 
 MMQ_Q4_K = 12
 MMQ_Q6_K = 14
@@ -40,7 +41,8 @@ BLOCK_BYTES = {MMQ_Q4_K: 144, MMQ_Q6_K: 210}
 
 EXPORTS = [
     "mmq_quantize_act", "mmq_register_weights", "mmq_release_weights", "mmq_weights_wexp",
-    "mmq_weights_info", "mmq_gemm", "mmq_gemm_profiled", "mmq_last_device_error", "mmq_set_wait_timeout_ns",
+    "mmq_weights_info", "mmq_gemm", "mmq_gemm_profiled", "mmq_gemm_noalloc",
+    "mmq_last_device_error", "mmq_set_wait_timeout_ns",
     "mmq_selftest_wait_timeout", "mmq_strerror",
 ]
 
@@ -74,6 +76,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
                                        ctypes.POINTER(i64), ctypes.POINTER(i64)]
         L.mmq_gemm.argtypes = [vp, vp, i64, vp, vp, u32, ctypes.POINTER(i32)]
         L.mmq_gemm_profiled.argtypes = [vp, vp, i64, vp, vp, u32, ctypes.POINTER(i32), vp, vp]
+        L.mmq_gemm_noalloc.argtypes = [vp, vp, i64, vp, vp]
         L.mmq_last_device_error.argtypes = []
         L.mmq_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
         L.mmq_set_wait_timeout_ns.restype = None
@@ -206,6 +209,14 @@ def mmq_gemm_profiled(w: Weights, Q: torch.Tensor, nt: int, Y: torch.Tensor,
                                     ctypes.c_void_p(ev_start.cuda_event),
                                     ctypes.c_void_p(ev_stop.cuda_event)), "mmq_gemm_profiled")
     return arm.value
+
+
+def mmq_gemm_noalloc(w: Weights, Q: torch.Tensor, nt: int, Y: torch.Tensor, stream=None):
+    """mmq_gemm that allocates no device memory (fixed 16 MiB library scratch);
+    for callers that cannot allocate.  Y must be preallocated."""
+    _check(load().mmq_gemm_noalloc(w.handle, _dev_ptr(Q, "Q"), nt, _dev_ptr(Y, "Y"), _stream(stream)),
+           "mmq_gemm_noalloc")
+    return Y
 
 
 def mmq_last_device_error() -> int:
