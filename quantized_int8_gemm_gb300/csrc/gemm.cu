@@ -121,24 +121,24 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw32(uint32_t saddr) {
 }
 
 // ---------------------------------------------------------------- activation prepass
-// One warp per token t < nt: pad40 blocks -> the token's row of every
-// activation block (fp16 qs, swizzled), da' = da*2^s_t, inv = 2^-s_t, and for
-// q4_K the min-term image slots hi/lo of g' = da*ssum*2^s_t.
+// One CTA of 128 threads per token t < nt: pad40 blocks -> the token's row of
+// every activation block (fp16 qs, swizzled), da' = da*2^s_t, inv = 2^-s_t,
+// and for q4_K the min-term image slots hi/lo of g' = da*ssum*2^s_t.
 template <bool kQ4>
-__global__ void __launch_bounds__(256) gemm_prepass_kernel(const uint8_t *__restrict__ Q,
+__global__ void __launch_bounds__(128) gemm_prepass_kernel(const uint8_t *__restrict__ Q,
                                                            int64_t nt, int64_t nb32,
                                                            uint8_t *__restrict__ aplane,
                                                            float *__restrict__ dap,
                                                            float *__restrict__ invp) {
-  const int64_t t = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (t >= nt) return;
+  const int64_t t = blockIdx.x;
+  const int tid = threadIdx.x;
   const uint8_t *qrow = Q + t * nb32 * MMQ_Q8_BLOCK_BYTES;
   const int64_t nsb = nb32 / 8;
   int s = 0;
-  if (kQ4) {  // s_t: largest |g| of the token lands in [2^14, 2^15)
+  if (kQ4) {  // s_t: the token's largest |g| lands in [2^14, 2^15)
+    __shared__ float wmax[4];
     float gmax = 0.f;
-    for (int64_t c = lane; c < nb32; c += 32) {
+    for (int64_t c = tid; c < nb32; c += 128) {
       const uint8_t *b = qrow + c * MMQ_Q8_BLOCK_BYTES;
       const float da = __half2float(__ushort_as_half(*reinterpret_cast<const unsigned short *>(b)));
       const int ssum = *reinterpret_cast<const int *>(b + MMQ_Q8_SSUM_OFF);
@@ -146,6 +146,9 @@ __global__ void __launch_bounds__(256) gemm_prepass_kernel(const uint8_t *__rest
     }
 #pragma unroll
     for (int m = 16; m; m >>= 1) gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, m));
+    if ((tid & 31) == 0) wmax[tid >> 5] = gmax;
+    __syncthreads();
+    gmax = fmaxf(fmaxf(wmax[0], wmax[1]), fmaxf(wmax[2], wmax[3]));
     if (gmax > 0.f) {
       const int e = static_cast<int>((__float_as_uint(gmax) >> 23) & 0xFF) - 127;
       s = min(30, max(-30, 14 - e));
@@ -154,8 +157,8 @@ __global__ void __launch_bounds__(256) gemm_prepass_kernel(const uint8_t *__rest
   const float scale = __uint_as_float(static_cast<uint32_t>(127 + s) << 23);
   const int r = static_cast<int>(t & (kTileM - 1));
   const int64_t tile = t / kTileM;
-  if (lane == 0) invp[t] = __uint_as_float(static_cast<uint32_t>(127 - s) << 23);
-  for (int64_t c = lane; c < nb32; c += 32) {
+  if (tid == 0) invp[t] = __uint_as_float(static_cast<uint32_t>(127 - s) << 23);
+  for (int64_t c = tid; c < nb32; c += 128) {
     const uint2 *src = reinterpret_cast<const uint2 *>(qrow + c * MMQ_Q8_BLOCK_BYTES);
     const uint2 w0 = __ldg(src + 0), w1 = __ldg(src + 1), w2 = __ldg(src + 2),
                 w3 = __ldg(src + 3), w4 = __ldg(src + 4);
@@ -535,11 +538,11 @@ cudaError_t launch_gemm(const mmq_weights_s *h, const uint8_t *Q, int64_t nt, fl
       e = cudaMemsetAsync(invp + nt, 0, static_cast<size_t>(nt_pad - nt) * 4, s);
     if (e != cudaSuccess) return e;
   }
-  const unsigned pgrid = static_cast<unsigned>((nt + 7) / 8);
+  const unsigned pgrid = static_cast<unsigned>(nt);
   if (q4)
-    gemm_prepass_kernel<true><<<pgrid, 256, 0, s>>>(Q, nt, nb32, aplane, dap, invp);
+    gemm_prepass_kernel<true><<<pgrid, 128, 0, s>>>(Q, nt, nb32, aplane, dap, invp);
   else
-    gemm_prepass_kernel<false><<<pgrid, 256, 0, s>>>(Q, nt, nb32, aplane, dap, invp);
+    gemm_prepass_kernel<false><<<pgrid, 128, 0, s>>>(Q, nt, nb32, aplane, dap, invp);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 

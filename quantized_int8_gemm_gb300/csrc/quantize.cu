@@ -6,8 +6,8 @@
 //   from zero), stored d16 = fp16_rn(d), bytes [2,4) = 0, ssum = sum q_i.
 //
 // HBM-bound: 128 B read and 40 B written per block.  Eight lanes share a
-// block, each loading one float4 (coalesced 512 B per warp) and storing one
-// 4-byte qs word; lane 0 of the eight also writes the d word and ssum.
+// block, each loading one float4 and storing one 4-byte qs word; lane 0 of
+// the eight also writes the d word and ssum.
 #include <cuda_fp16.h>
 
 #include "internal.h"
@@ -15,34 +15,25 @@
 namespace mmq {
 namespace {
 
-__global__ void __launch_bounds__(256) quantize_q8_0_kernel(const float4 *__restrict__ X,
-                                                            int64_t nblocks,
-                                                            uint8_t *__restrict__ Q) {
-  const int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int64_t blk = g >> 3;
-  const int part = static_cast<int>(g & 7);
-  const bool valid = blk < nblocks;
-  float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (valid) v = __ldg(X + blk * 8 + part);
-
+// One 32-value block handled by 8 lanes (one float4 each).
+__device__ __forceinline__ void quantize_block(float4 v, int64_t blk, bool valid, int part,
+                                               uint8_t *__restrict__ Q) {
   float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
 #pragma unroll
   for (int m = 1; m < 8; m <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
-
   const float d = amax / 127.0f;
   int q[4] = {0, 0, 0, 0};
   if (amax != 0.0f) {
     const float xs[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      int qi = static_cast<int>(roundf(xs[i] / d));
+      const int qi = static_cast<int>(roundf(xs[i] / d));
       q[i] = max(-127, min(127, qi));
     }
   }
   int ssum = q[0] + q[1] + q[2] + q[3];
 #pragma unroll
   for (int m = 1; m < 8; m <<= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, m);
-
   if (!valid) return;
   uint8_t *b = Q + blk * MMQ_Q8_BLOCK_BYTES;
   const uint32_t word = (static_cast<uint32_t>(q[0]) & 0xFFu) |
@@ -57,15 +48,39 @@ __global__ void __launch_bounds__(256) quantize_q8_0_kernel(const float4 *__rest
   }
 }
 
+// Grid-stride over groups of 16 blocks per warp: the four float4 loads of a
+// lane are issued before any block is reduced, so each lane keeps 64 B of
+// loads in flight.
+__global__ void __launch_bounds__(256) quantize_q8_0_kernel(const float4 *__restrict__ X,
+                                                            int64_t nblocks,
+                                                            uint8_t *__restrict__ Q) {
+  const int lane = threadIdx.x & 31, part = lane & 7, grp = lane >> 3;
+  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t base = warp * 16; base < nblocks; base += nwarps * 16) {
+    float4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t blk = base + u * 4 + grp;
+      v[u] = blk < nblocks ? __ldg(X + blk * 8 + part) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t blk = base + u * 4 + grp;
+      quantize_block(v[u], blk, blk < nblocks, part, Q);
+    }
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_quantize_q8_0(const float *X, int64_t nt, int64_t id, uint8_t *Q,
                                  cudaStream_t s) {
   const int64_t nblocks = nt * (id / 32);
   if (nblocks == 0) return cudaSuccess;
-  const int64_t threads = nblocks * 8;
-  const int bs = 256;
-  const int64_t grid = (threads + bs - 1) / bs;
+  const int bs = 256;  // 8 warps, 128 blocks per CTA pass
+  const int64_t want = (nblocks + 127) / 128;
+  const int64_t grid = want < 152 * 16 ? want : 152 * 16;
   quantize_q8_0_kernel<<<static_cast<unsigned>(grid), bs, 0, s>>>(
       reinterpret_cast<const float4 *>(X), nblocks, Q);
   return cudaGetLastError();
