@@ -202,7 +202,7 @@ int mmq_weights_info(mmq_weights_t h, int *type, int64_t *od, int64_t *id,
   if (type) *type = h->type;
   if (od) *od = h->od;
   if (id) *id = h->id;
-  const int64_t operand = h->od_pad * h->id * 2;
+  const int64_t operand = static_cast<int64_t>(mmq::bplane_operand_bytes(h->type, h->od, h->id));
   if (operand_bytes) *operand_bytes = operand;
   if (scale_bytes) *scale_bytes = static_cast<int64_t>(h->bplane_bytes) - operand;
   if (wexp_bytes) *wexp_bytes = static_cast<int64_t>(h->wexp_bytes);

@@ -20,18 +20,24 @@
 // factor so the final scaling by 2^-s_t is exact.
 //
 // Data movement: operands arrive pre-tiled and pre-swizzled (tiling.h), two
-// bulk copies per 128-K stage (activation block, weight block with its scale
-// rows), issued by two lanes of the producer warp into a 3-stage ring.
+// bulk copies per 128-K stage (activation block, weight block) into a
+// 3-stage ring that only the tensor core releases, plus one small copy per
+// super-block of the weight scales (d, dmin) into a 4-entry scale ring that
+// the epilogue releases.
 //
 // Kernel shape: persistent, one CTA of 384 threads per SM, 128 x 128 tiles,
 // token tiles fastest so concurrently running CTAs share weight tiles in L2.
 //   warps 0..7  epilogue: warp w reads TMEM lanes 32*(w%4).. and columns
-//               64*(w/4)..: TMEM -> registers -> packed fp32x2 FMAs
-//   warp 8      producer: lane 0 the activation block, lane 1 the weight block
+//               64*(w/4)..: TMEM -> registers (one 64-column load per chunk)
+//               -> packed fp32x2 FMAs
+//   warp 8      producer: lane 0 the activation block, lane 1 the weight
+//               block, lane 2 the scale block
 //   warp 9      TMEM owner + UMMA issuer (one elected lane of a warp-uniform
-//               loop): per 32-K chunk two 128x128x16 UMMAs; chunks go in pairs
-//               into a ring of two TMEM slot pairs, one commit per pair
-//               (+ the min-term UMMA per q4_K super-block, in a pair of its own)
+//               loop): per 32-K chunk two 128x128x16 UMMAs into one of four
+//               TMEM chunk slots, committed per chunk; the slots go in two
+//               groups of two, and a group is refilled as soon as the
+//               epilogue has loaded both of its chunks into registers
+//               (+ the min-term UMMA per q4_K super-block, in a group alone)
 //   warps 10-11 idle (complete the register-donating warpgroup)
 // Every wait is bounded (ptx.cuh); a CTA that gives up drains its own copies
 // and UMMAs, frees TMEM and returns.
@@ -50,25 +56,29 @@ namespace {
 using namespace tiling;
 
 constexpr int STAGES = 3;
-constexpr int RING = 2;  // TMEM slot pairs, 2 x kTileN columns each (one hand-off per 2 chunks)
-constexpr int EPI_WARPS = 8;     // warpgroups 0 and 1
-constexpr int PRODUCER_WARP = 8;  // warpgroup 2: producer, UMMA issuer, two idle warps
-constexpr int MMA_WARP = 9;
+constexpr int SLOTS = 4;          // TMEM chunk slots of kTileN columns (512 columns)
+constexpr int SRING = 4;          // per-super-block scale ring entries
+constexpr int EPI_WARPS = 8;      // warpgroups 0 and 1
+constexpr int PRODUCER_WARP = 8;  // warpgroup 2: producer, two UMMA issuers, one idle warp
+constexpr int ISSUER_WARP = 9;    // issuers 9 and 10; issuer i owns TMEM slots 2i and 2i+1
+constexpr int ISSUERS = 2;
 constexpr int THREADS = 384;
 // Register split: launched at 168 per thread (384 x 168 = 64512); warpgroup 2
-// drops to 56 and the epilogue warpgroups rise to 216: 2*128*216 + 128*56 =
-// 62464 <= 64512.
-constexpr int REGS_EPI = 216;
+// drops to 56 and the epilogue warpgroups rise to 224: 2*128*224 + 128*56 =
+// 64512.
+constexpr int REGS_EPI = 224;
 constexpr int REGS_CTL = 56;
-constexpr int TMEM_COLS = RING * 2 * kTileN;  // 512
+constexpr int TMEM_COLS = SLOTS * kTileN;  // 512
 
 template <bool kQ4>
 struct Smem {
   static constexpr int kA = a_odd_bytes(kQ4);                          // A region per stage
   static constexpr int kB = ((b_odd_bytes(kQ4) + 1023) / 1024) * 1024;  // B region per stage
   static constexpr int kStage = kA + kB;
-  static constexpr int kBar = STAGES * kStage;
-  static constexpr int kNumBars = 2 * STAGES + 2 * RING + 1;
+  static constexpr int kScale = scale_block_bytes(kQ4);                // one scale ring entry
+  static constexpr int kScaleRing = STAGES * kStage;
+  static constexpr int kBar = kScaleRing + SRING * kScale;
+  static constexpr int kNumBars = 2 * STAGES + 2 * SLOTS + 2 * SRING + 1;
   static constexpr int kSlot = kBar + kNumBars * 8;
   static constexpr int kUsed = kSlot + 16;
   static constexpr int kBytes = kUsed + 1024;  // slack for 1024-byte alignment
@@ -77,25 +87,6 @@ struct Smem {
 };
 
 // ---------------------------------------------------------------- small helpers
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-  float2 d;
-  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
-      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
-      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-      : "=f"(d.x), "=f"(d.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
-  return d;
-}
-__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
-  float2 d;
-  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
-      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-      : "=f"(d.x), "=f"(d.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-  return d;
-}
-
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
                                           uint32_t bar) {
   asm volatile(
@@ -103,9 +94,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
           dst),
       "l"(src), "r"(bytes), "r"(bar)
       : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_cnt(uint32_t bar, uint32_t cnt) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(cnt) : "memory");
 }
 
 // Shared-memory descriptor for the 32-byte-swizzled K=16 min-term images:
@@ -193,12 +181,35 @@ __global__ void __launch_bounds__(128) gemm_prepass_kernel(const uint8_t *__rest
 }
 
 // ---------------------------------------------------------------- the GEMM
+// acc[h*16 ..] = da * S (first chunk of a super-block) or += da * S, on one
+// 32-column half h of a chunk.
+__device__ __forceinline__ void fold_half(float2 (&acc)[32], int h, const uint32_t (&r)[32], float da,
+                                          bool first) {
+  const float2 da2 = make_float2(da, da);
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const float2 x = make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+    acc[h * 16 + j] = first ? __fmul2_rn(da2, x) : __ffma2_rn(da2, x, acc[h * 16 + j]);
+  }
+}
+
+// Makes the compiler treat r as written here, so code that reads r is not
+// moved above this point.
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                 "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+                 "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]),
+                 "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]),
+                 "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
+}
+
 template <bool kQ4>
 __global__ void __launch_bounds__(THREADS, 1)
     mmq_gemm_kernel(const uint8_t *__restrict__ aplane, const uint8_t *__restrict__ bplane,
-                    const float *__restrict__ dap, const float *__restrict__ invp, int64_t nt,
-                    int64_t od, int64_t nb32, int n_tt, int n_ot, float *__restrict__ Y,
-                    WaitCtl wctl) {
+                    const uint8_t *__restrict__ bscale, const float *__restrict__ dap,
+                    const float *__restrict__ invp, int64_t nt, int64_t od, int64_t nb32, int n_tt,
+                    int n_ot, float *__restrict__ Y, WaitCtl wctl) {
   using L = Smem<kQ4>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
@@ -212,25 +223,32 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t bar = base + L::kBar;
   auto full = [&](int s) { return bar + 8u * s; };
   auto empty = [&](int s) { return bar + 8u * (STAGES + s); };
-  auto rfull = [&](int i) { return bar + 8u * (2 * STAGES + i); };
-  auto rempty = [&](int i) { return bar + 8u * (2 * STAGES + RING + i); };
-  const uint32_t done = bar + 8u * (2 * STAGES + 2 * RING);
+  auto rfull = [&](uint32_t i) { return bar + 8u * (2 * STAGES + i); };
+  auto rempty = [&](uint32_t i) { return bar + 8u * (2 * STAGES + SLOTS + i); };
+  auto sfull = [&](int e) { return bar + 8u * (2 * STAGES + 2 * SLOTS + e); };
+  auto sempty = [&](int e) { return bar + 8u * (2 * STAGES + 2 * SLOTS + SRING + e); };
+  const uint32_t done = bar + 8u * (2 * STAGES + 2 * SLOTS + 2 * SRING);
   auto a_smem = [&](int s) { return base + s * L::kStage; };
   auto b_smem = [&](int s) { return base + s * L::kStage + L::kA; };
+  auto s_smem = [&](int e) { return base + L::kScaleRing + e * L::kScale; };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full(s), 1);
-      mbar_init(empty(s), 1 + EPI_WARPS);  // UMMA commit + 8 epilogue arrivals (scale reads)
+      mbar_init(empty(s), ISSUERS);  // one commit per issuer frees a stage
     }
-    for (int i = 0; i < RING; ++i) {
+    for (uint32_t i = 0; i < SLOTS; ++i) {
       mbar_init(rfull(i), 1);
       mbar_init(rempty(i), EPI_WARPS);
     }
-    mbar_init(done, 1);
+    for (int e = 0; e < SRING; ++e) {
+      mbar_init(sfull(e), 1);
+      mbar_init(sempty(e), EPI_WARPS);
+    }
+    mbar_init(done, ISSUERS);
     fence_mbar_init();
   }
-  if (warp == MMA_WARP) {
+  if (warp == ISSUER_WARP) {
     tmem_alloc(base + L::kSlot, TMEM_COLS);
     tmem_relinquish();
   }
@@ -243,12 +261,22 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == PRODUCER_WARP) {
     // ------------------------------------------------------------ producer
     // The whole warp runs the loop (warp-uniform control flow); lane 0 copies
-    // the activation block, lane 1 the weight block.
-    uint32_t ks = 0, issued = 0;
+    // the activation block, lane 1 the weight block, lane 2 the super-block's
+    // scale block into the scale ring.
+    uint32_t ks = 0, ns = 0, issued = 0, s_issued = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
       const int tt = tile % n_tt, ot = tile / n_tt;
-      for (int64_t sb = 0; sb < nsb && ok; ++sb) {
+      for (int64_t sb = 0; sb < nsb && ok; ++sb, ++ns) {
+        const int e = static_cast<int>(ns % SRING);
+        ok = __all_sync(0xffffffffu, mbar_wait(sempty(e), ((ns / SRING) & 1) ^ 1, wctl));
+        if (!ok) break;
+        if (lane == 2) {
+          mbar_arrive_expect_tx(sfull(e), L::kScale);
+          bulk_load(s_smem(e), bscale + b_scale_block(ot, sb, nsb, kQ4), L::kScale, sfull(e));
+        }
+        __syncwarp();
+        s_issued = ns + 1;
         for (int half = 0; half < 2; ++half, ++ks) {
           const int s = static_cast<int>(ks % STAGES);
           ok = __all_sync(0xffffffffu, mbar_wait(empty(s), ((ks / STAGES) & 1) ^ 1, wctl));
@@ -266,14 +294,21 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
     }
-    if (!ok)  // drain this CTA's copies still in flight
+    if (!ok) {  // drain this CTA's copies still in flight
       for (uint32_t k = issued > STAGES ? issued - STAGES : 0; k < issued; ++k)
         mbar_wait(full(k % STAGES), (k / STAGES) & 1, wctl, false);
-  } else if (warp == MMA_WARP) {
-    // ------------------------------------------------------------ UMMA issuer
-    // The whole warp runs the loop and waits; one elected lane issues the
-    // UMMAs and commits (keeps the issue path warp-uniform).  Chunks go in
-    // pairs into a ring of two slot pairs: one hand-off per 64 of K.
+      for (uint32_t k = s_issued > SRING ? s_issued - SRING : 0; k < s_issued; ++k)
+        mbar_wait(sfull(k % SRING), (k / SRING) & 1, wctl, false);
+    }
+  } else if (warp < ISSUER_WARP + ISSUERS) {
+    // ------------------------------------------------------------ UMMA issuers
+    // Two warps issue, each from one elected lane of a warp-uniform loop: of
+    // the eight 32-K chunks of a super-block, issuer 0 takes 0, 2, 4, 6 (and
+    // the q4_K min term after chunk 7) and issuer 1 takes 1, 3, 5, 7.  An
+    // issuer's items alternate between its two TMEM slots; each is committed
+    // on its slot's barrier.  The tensor pipe queues little work, so while
+    // one issuer waits for a slot or a stage the other keeps it fed.
+    const int iw = warp - ISSUER_WARP;
     uint32_t elected;
     asm volatile("{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
                  : "=r"(elected));
@@ -281,12 +316,23 @@ __global__ void __launch_bounds__(THREADS, 1)
     constexpr uint64_t kStageDesc = L::kStage >> 4;  // descriptor address field step per stage
     const uint64_t a0 = sdesc_kmajor_sw128(a_smem(0)), b0 = sdesc_kmajor_sw128(b_smem(0));
     const uint64_t am0 = sdesc_kmajor_sw32(a_smem(0) + kAMin), bm0 = sdesc_kmajor_sw32(b_smem(0) + kBMin);
-    uint32_t ks = 0, p = 0;
+    uint32_t ks = 0, j = 0;  // stages consumed, items issued
     bool ok = true;
-    auto next_pair = [&](uint32_t &ps) {
-      ps = p % RING;
-      const bool got = __all_sync(0xffffffffu, mbar_wait(rempty(ps), ((p / RING) & 1) ^ 1, wctl));
-      if (got) tc_fence_after();
+    // one item: wait for the slot, 1 or 2 UMMAs, commit on the slot
+    auto item = [&](uint64_t ad, uint64_t bd, bool two) {
+      const uint32_t slot = 2 * iw + (j & 1);
+      const bool got = __all_sync(0xffffffffu, mbar_wait(rempty(slot), ((j >> 1) & 1) ^ 1, wctl));
+      if (got) {
+        tc_fence_after();
+        if (elected) {
+          const uint32_t d = tbase + slot * kTileN;
+          umma_f16(d, ad, bd, idesc, 0);
+          if (two) umma_f16(d, ad + 2, bd + 2, idesc, 1);
+          umma_commit(rfull(slot));
+        }
+        __syncwarp();
+        ++j;
+      }
       return got;
     };
     for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
@@ -298,67 +344,51 @@ __global__ void __launch_bounds__(THREADS, 1)
           tc_fence_after();
           const uint64_t as = a0 + s * kStageDesc, bs = b0 + s * kStageDesc;
 #pragma unroll
-          for (int cp = 0; cp < 2; ++cp) {
-            uint32_t ps;
-            if (!(ok = next_pair(ps))) break;
-            if (elected) {
-#pragma unroll
-              for (int cc = 0; cc < 2; ++cc) {
-                const int c = 2 * cp + cc;  // chunk in the stage: K = 32c .. 32c+31
-                const uint64_t off = (c >> 1) * (16384 >> 4) + (c & 1) * (64 >> 4);
-                const uint32_t d = tbase + (ps * 2 + cc) * kTileN;
-                umma_f16(d, as + off, bs + off, idesc, 0);
-                umma_f16(d, as + off + 2, bs + off + 2, idesc, 1);
-              }
-              umma_commit(rfull(ps));
-            }
-            __syncwarp();
-            ++p;
+          for (int q = 0; q < 2 && ok; ++q) {
+            const int lc = iw + 2 * q;  // chunk in the stage: K = 32*lc .. 32*lc+31
+            const uint64_t off = (lc >> 1) * (16384 >> 4) + (lc & 1) * (64 >> 4);
+            ok = item(as + off, bs + off, true);
           }
-          if (ok && kQ4 && half == 1) {
-            uint32_t ps;
-            if ((ok = next_pair(ps))) {
-              if (elected) {
-                umma_f16(tbase + ps * 2 * kTileN, am0 + s * kStageDesc, bm0 + s * kStageDesc, idesc, 0);
-                umma_commit(rfull(ps));
-              }
-              __syncwarp();
-              ++p;
-            }
-          }
+          if (ok && kQ4 && half == 1 && iw == 0)
+            ok = item(am0 + s * kStageDesc, bm0 + s * kStageDesc, false);
           if (!ok) break;
-          if (elected) {
-            umma_commit(empty(s));
-            if (half == 0) mbar_arrive_cnt(empty(s), EPI_WARPS);  // epilogue reads odd stages only
-          }
+          if (elected) umma_commit(empty(s));
           __syncwarp();
         }
       }
     }
-    if (elected) umma_commit(done);  // every UMMA of this CTA has finished once `done` flips
+    if (elected) umma_commit(done);  // all UMMAs of both issuers have finished once `done` flips
+    __syncwarp();
     mbar_wait(done, 0, wctl, false);
   }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS_EPI));
     // ------------------------------------------------------------ epilogue
+    // Software-pipelined over 32-column halves: while the packed FMAs of one
+    // half run, the TMEM load of the next half and the barrier test of the
+    // next item are in flight.  A slot is handed back as soon as both halves
+    // of its chunk are in registers.
     const int quad = warp & 3;
     const int chalf = warp >> 2;  // column half 0 / 1
     const int row = quad * 32 + lane;
     const uint32_t taddr = tbase + (static_cast<uint32_t>(quad * 32) << 16) + chalf * 64;
-    uint32_t ks = 0, u = 0;
+    uint32_t jj[ISSUERS] = {0, 0}, ns = 0;  // items taken from each issuer, scale entries used
     bool ok = true;
-    // Wait for the next slot pair; false (after recording) if the wait expired.
-    auto acquire = [&](uint32_t &ps) {
-      ps = u % RING;
-      const bool got = __all_sync(0xffffffffu, mbar_wait(rfull(ps), (u / RING) & 1, wctl));
+    // slot and phase of the next item of issuer iw
+    auto next_item = [&](int iw, uint32_t &slot, uint32_t &par) {
+      slot = 2 * iw + (jj[iw] & 1);
+      par = (jj[iw] >> 1) & 1;
+      ++jj[iw];
+    };
+    auto wait_item = [&](uint32_t slot, uint32_t par, bool ready) {
+      const bool got = __all_sync(0xffffffffu, ready || mbar_wait(rfull(slot), par, wctl));
       if (got) tc_fence_after();
       return got;
     };
-    auto release = [&](uint32_t ps) {
+    auto give = [&](uint32_t slot) {
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(rempty(ps));
-      ++u;
+      if (lane == 0) mbar_arrive(rempty(slot));
     };
     for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
       const int tt = tile % n_tt, ot = tile / n_tt;
@@ -366,73 +396,83 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int64_t o0 = static_cast<int64_t>(ot) * kTileN + chalf * 64;
       float2 y[32], acc[32];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) y[j] = make_float2(0.f, 0.f);
+      for (int i = 0; i < 32; ++i) y[i] = make_float2(0.f, 0.f);
       const float4 *darow = reinterpret_cast<const float4 *>(dap + t * nb32);
+      float4 nx0 = __ldg(darow), nx1 = __ldg(darow + 1);  // da' of the next super-block
       for (int64_t sb = 0; sb < nsb && ok; ++sb) {
-        const float4 d0 = __ldg(darow + 2 * sb), d1 = __ldg(darow + 2 * sb + 1);
-        const float das[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
-        // Four 32-column quarters per slot pair (chunk c then c+1, low then
-        // high columns), software-pipelined: the load of quarter q+1 is in
-        // flight while quarter q is folded into acc.
+        const float das[8] = {nx0.x, nx0.y, nx0.z, nx0.w, nx1.x, nx1.y, nx1.z, nx1.w};
+        if (sb + 1 < nsb) {
+          nx0 = __ldg(darow + 2 * sb + 2);
+          nx1 = __ldg(darow + 2 * sb + 3);
+        }
+        uint32_t r0[32], r1[32];
+        uint32_t slot, par;
+        next_item(0, slot, par);
+        if (!(ok = wait_item(slot, par, false))) break;
+        tmem_ld_32x32b_x32(taddr + slot * kTileN, r0);
+        tmem_wait_ld(r0);
 #pragma unroll
-        for (int c = 0; c < 8; c += 2) {
-          uint32_t ps;
-          if (!(ok = acquire(ps))) break;
-          uint32_t r[2][32];
-          tmem_ld_32x32b_x32(taddr + (ps * 2) * kTileN, r[0]);
-          tmem_wait_ld(r[0]);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            if (q < 3)
-              tmem_ld_32x32b_x32(taddr + (ps * 2 + ((q + 1) >> 1)) * kTileN + ((q + 1) & 1) * 32,
-                                 r[(q + 1) & 1]);
-            const int cc = c + (q >> 1);
-            const float2 da2 = make_float2(das[cc], das[cc]);
-            const uint32_t(&v)[32] = r[q & 1];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float2 x = make_float2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
-              float2 &a = acc[(q & 1) * 16 + j];
-              a = cc == 0 ? fmul2(da2, x) : ffma2(da2, x, a);
-            }
-            if (q < 3) tmem_wait_ld(r[(q + 1) & 1]);
-            if (q == 2) release(ps);  // every quarter of the pair is in registers
+        for (int c = 0; c < 8; ++c) {
+          // second half of chunk c, and an early test of chunk c+1
+          tmem_ld_32x32b_x32(taddr + slot * kTileN + 32, r1);
+          uint32_t nslot = 0, npar = 0;
+          bool ready = true;
+          if (c < 7) {
+            next_item((c + 1) & 1, nslot, npar);
+            ready = mbar_try_wait(rfull(nslot), npar);
           }
+          reg_fence(r0);
+          fold_half(acc, 0, r0, das[c], c == 0);
+          tmem_wait_ld(r1);
+          give(slot);
+          if (c < 7) {
+            if (!(ok = wait_item(nslot, npar, ready))) break;
+            tmem_ld_32x32b_x32(taddr + nslot * kTileN, r0);
+            slot = nslot;
+          }
+          fold_half(acc, 1, r1, das[c], c == 0);
+          if (c < 7) tmem_wait_ld(r0);
         }
         if (!ok) break;
-        ks += 1;  // the even stage of this super-block; the odd one holds d (and dmin)
-        const int s = static_cast<int>(ks % STAGES);
-        ok = __all_sync(0xffffffffu, mbar_wait(full(s), (ks / STAGES) & 1, wctl));
+        // super-block end: y += d * acc  (- dmin * MIN for q4_K)
+        const int e = static_cast<int>(ns % SRING);
+        ok = __all_sync(0xffffffffu, mbar_wait(sfull(e), (ns / SRING) & 1, wctl));
         if (!ok) break;
-        const float *bsm = reinterpret_cast<const float *>(smem + s * L::kStage + L::kA);
-        const float2 *d2 = reinterpret_cast<const float2 *>(bsm + kBD / 4 + chalf * 64);
+        const uint8_t *sblk = smem + (s_smem(e) - base);
+        const float4 *d4 = reinterpret_cast<const float4 *>(sblk) + chalf * 16;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) y[j] = ffma2(d2[j], acc[j], y[j]);
+        for (int i = 0; i < 16; ++i) {
+          const float4 d = d4[i];
+          y[2 * i] = __ffma2_rn(make_float2(d.x, d.y), acc[2 * i], y[2 * i]);
+          y[2 * i + 1] = __ffma2_rn(make_float2(d.z, d.w), acc[2 * i + 1], y[2 * i + 1]);
+        }
         if (kQ4) {
-          uint32_t ps;
-          if (!(ok = acquire(ps))) break;
-          const float2 *dm2 = reinterpret_cast<const float2 *>(bsm + kBDmin / 4 + chalf * 64);
+          next_item(0, slot, par);
+          if (!(ok = wait_item(slot, par, false))) break;
+          tmem_ld_32x32b_x32(taddr + slot * kTileN, r0);
+          tmem_ld_32x32b_x32(taddr + slot * kTileN + 32, r1);
+          tmem_wait_ld(r0);
+          reg_fence(r1);
+          give(slot);
+          const float4 *m4 = reinterpret_cast<const float4 *>(sblk + kSDmin) + chalf * 16;
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(taddr + ps * 2 * kTileN + hh * 32, r);
-            tmem_wait_ld(r);
-            if (hh == 1) release(ps);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float2 dm = dm2[hh * 16 + j];
-              y[hh * 16 + j] = ffma2(make_float2(-dm.x, -dm.y),
-                                     make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])),
-                                     y[hh * 16 + j]);
-            }
+          for (int i = 0; i < 16; ++i) {
+            const float4 dm = m4[i];
+            const uint32_t(&rr)[32] = i < 8 ? r0 : r1;
+            const int q = (i & 7) * 4;
+            y[2 * i] = __ffma2_rn(make_float2(-dm.x, -dm.y),
+                                  make_float2(__uint_as_float(rr[q]), __uint_as_float(rr[q + 1])), y[2 * i]);
+            y[2 * i + 1] = __ffma2_rn(make_float2(-dm.z, -dm.w),
+                                      make_float2(__uint_as_float(rr[q + 2]), __uint_as_float(rr[q + 3])),
+                                      y[2 * i + 1]);
           }
         }
-        // the stage's scale rows were read through the generic proxy; order
-        // those reads before the TMA (async proxy) that refills the buffer
+        // the scale block was read through the generic proxy; order those
+        // reads before the bulk copy (async proxy) that refills the entry
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
-        if (lane == 0) mbar_arrive(empty(s));
-        ks += 1;
+        if (lane == 0) mbar_arrive(sempty(e));
+        ++ns;
       }
       if (!ok) break;
       if (t < nt) {
@@ -441,18 +481,18 @@ __global__ void __launch_bounds__(THREADS, 1)
         float *yrow = Y + t * od + o0;
         if ((od & 3) == 0) {
 #pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            if (o0 + 2 * j < od) {
-              const float2 a = fmul2(y[j], inv2), b = fmul2(y[j + 1], inv2);
-              *reinterpret_cast<float4 *>(yrow + 2 * j) = make_float4(a.x, a.y, b.x, b.y);
+          for (int i = 0; i < 32; i += 2) {
+            if (o0 + 2 * i < od) {
+              const float2 a = __fmul2_rn(y[i], inv2), b = __fmul2_rn(y[i + 1], inv2);
+              *reinterpret_cast<float4 *>(yrow + 2 * i) = make_float4(a.x, a.y, b.x, b.y);
             }
           }
         } else {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float2 a = fmul2(y[j], inv2);
-            if (o0 + 2 * j < od) yrow[2 * j] = a.x;
-            if (o0 + 2 * j + 1 < od) yrow[2 * j + 1] = a.y;
+          for (int i = 0; i < 32; ++i) {
+            const float2 a = __fmul2_rn(y[i], inv2);
+            if (o0 + 2 * i < od) yrow[2 * i] = a.x;
+            if (o0 + 2 * i + 1 < od) yrow[2 * i + 1] = a.y;
           }
         }
       }
@@ -461,7 +501,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == MMA_WARP) {
+  if (warp == ISSUER_WARP) {
     tc_fence_after();
     tmem_dealloc(tbase, TMEM_COLS);
   }
@@ -564,7 +604,8 @@ cudaError_t launch_gemm(const mmq_weights_s *h, const uint8_t *Q, int64_t nt, fl
   const int grid = n_tiles < g_num_sms[dev] ? n_tiles : g_num_sms[dev];
   WaitCtl w{&st->status, &st->abort_epoch, epoch, limit_ns};
   if (ev0 && (e = cudaEventRecordWithFlags(ev0, s, ev_flags)) != cudaSuccess) return e;
-  kern<<<grid, THREADS, smem, s>>>(aplane, static_cast<const uint8_t *>(h->bplane), dap, invp, nt,
+  const uint8_t *bp = static_cast<const uint8_t *>(h->bplane);
+  kern<<<grid, THREADS, smem, s>>>(aplane, bp, bp + b_scale_region(n_ot, nsb, q4), dap, invp, nt,
                                    h->od, nb32, static_cast<int>(n_tt), n_ot, Y, w);
   e = cudaGetLastError();
   if (e == cudaSuccess && ev1) e = cudaEventRecordWithFlags(ev1, s, ev_flags);

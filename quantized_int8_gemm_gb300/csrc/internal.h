@@ -10,8 +10,9 @@
 // A registered weight.  Device memory owned by the handle:
 //   bplane  the GEMM's pre-tiled weight plane (tiling.h): per 128-row tile,
 //           super-block and half, the fp16 operand image with the sub-block
-//           scale folded in, the d row and, for q4_K, the dmin row and the
-//           integer-min image.  Rows od..od_pad-1 are zero.
+//           scale folded in and, for q4_K, the integer-min image; then the
+//           scale region (d and, for q4_K, dmin rows).  Rows od..od_pad-1
+//           are zero.
 //   wexp    optional dense centered q6_K plane, int8 [od][id], q - 32
 struct mmq_weights_s {
   int type = 0;
@@ -41,6 +42,7 @@ cudaError_t launch_quantize_q8_0(const float *X, int64_t nt, int64_t id, uint8_t
 // Registration: bytes of the tiled weight plane, and the expansion kernels.
 // *bad_scale (device int) becomes nonzero if a q6_K sub-block scale |sc| > 64.
 size_t bplane_bytes(int type, int64_t od, int64_t id);
+size_t bplane_operand_bytes(int type, int64_t od, int64_t id);  // without the scale region
 cudaError_t launch_register(const mmq_weights_s *h, const uint8_t *W, int *bad_scale,
                             cudaStream_t s);
 

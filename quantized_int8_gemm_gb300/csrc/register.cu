@@ -7,8 +7,9 @@
 // the GEMM's pre-tiled weight plane (tiling.h), per weight element (o, k):
 //   operand  fp16  q6_K: sc[k/16] * (q - 32)   (|.| <= 64*32, exact)
 //                  q4_K: sc[k/32] * q          (<= 63*15, exact)
-// and per (row, super-block) the fp32 scale d, plus for q4_K dmin and the
-// integer mins m of the eight sub-blocks (the min-term image).
+// and per (row, super-block) the fp32 scale d, plus for q4_K dmin (both in
+// the plane's scale region) and the integer mins m of the eight sub-blocks
+// (the min-term image).
 //
 // With MMQ_REG_WEXP the dense centered-int8 plane wexp[o*id + k] = q - 32 is
 // written first and the q6_K operand is then built by reading it back with
@@ -66,6 +67,7 @@ template <bool kQ4, bool kFromWexp>
 __global__ void __launch_bounds__(256) register_kernel(const uint8_t *__restrict__ W,
                                                        const int8_t *__restrict__ wexp, int64_t id,
                                                        uint8_t *__restrict__ bplane,
+                                                       uint64_t scale_region,
                                                        int *__restrict__ bad_scale) {
   constexpr int kBytes = kQ4 ? MMQ_Q4K_BLOCK_BYTES : MMQ_Q6K_BLOCK_BYTES;
   __shared__ uint8_t blk[kBytes + 2];
@@ -79,6 +81,7 @@ __global__ void __launch_bounds__(256) register_kernel(const uint8_t *__restrict
   const int half = e >> 7, k = e & 127;
   uint8_t *dst = bplane + b_block(ot, sb, half, nsb, kQ4);
   uint8_t *odd = bplane + b_block(ot, sb, 1, nsb, kQ4);
+  float *scl = reinterpret_cast<float *>(bplane + scale_region + b_scale_block(ot, sb, nsb, kQ4));
   int val;
   float d;
   if constexpr (kQ4) {
@@ -93,8 +96,7 @@ __global__ void __launch_bounds__(256) register_kernel(const uint8_t *__restrict
       const uint32_t mh = __half_as_ushort(__int2half_rn(m));
       *reinterpret_cast<uint32_t *>(odd + kBMin + min_off(r, 2 * j)) = mh | (mh << 16);
     }
-    if (e == 0)
-      reinterpret_cast<float *>(odd + kBDmin)[r] = f16_at(blk + MMQ_Q4K_DMIN_OFF);
+    if (e == 0) scl[kSDmin / 4 + r] = f16_at(blk + MMQ_Q4K_DMIN_OFF);
   } else {
     int c;
     if constexpr (kFromWexp) c = wexp[o * id + sb * MMQ_QK + e];
@@ -105,15 +107,20 @@ __global__ void __launch_bounds__(256) register_kernel(const uint8_t *__restrict
     d = f16_at(blk + MMQ_Q6K_D_OFF);
   }
   *reinterpret_cast<__half *>(dst + operand_off(r, k)) = __int2half_rn(val);
-  if (k == 0) reinterpret_cast<float *>(dst + kBD)[r] = d;
+  if (e == 0) scl[r] = d;
 }
 
 }  // namespace
 
 size_t bplane_bytes(int type, int64_t od, int64_t id) {
   const bool q4 = type == MMQ_Q4_K;
+  const int64_t n_ot = (od + kTileN - 1) / kTileN, nsb = id / MMQ_QK;
+  return static_cast<size_t>(b_scale_region(n_ot, nsb, q4) + b_scale_block(n_ot, 0, nsb, q4));
+}
+
+size_t bplane_operand_bytes(int type, int64_t od, int64_t id) {
   const int64_t n_ot = (od + kTileN - 1) / kTileN;
-  return static_cast<size_t>(n_ot * (id / MMQ_QK)) * b_pair_bytes(q4);
+  return static_cast<size_t>(b_scale_region(n_ot, id / MMQ_QK, type == MMQ_Q4_K));
 }
 
 cudaError_t launch_register(const mmq_weights_s *h, const uint8_t *W, int *bad_scale,
@@ -123,13 +130,15 @@ cudaError_t launch_register(const mmq_weights_s *h, const uint8_t *W, int *bad_s
   if (e != cudaSuccess) return e;
   const dim3 grid(static_cast<unsigned>(h->od), static_cast<unsigned>(h->nsb));
   uint8_t *bp = static_cast<uint8_t *>(h->bplane);
-  if (h->type == MMQ_Q4_K) {
-    register_kernel<true, false><<<grid, 256, 0, s>>>(W, nullptr, h->id, bp, bad_scale);
+  const bool q4 = h->type == MMQ_Q4_K;
+  const uint64_t sr = b_scale_region(h->od_pad / kTileN, h->nsb, q4);
+  if (q4) {
+    register_kernel<true, false><<<grid, 256, 0, s>>>(W, nullptr, h->id, bp, sr, bad_scale);
   } else if (h->wexp) {
     expand_wexp_kernel<<<grid, 256, 0, s>>>(W, h->id, h->wexp);
-    register_kernel<false, true><<<grid, 256, 0, s>>>(W, h->wexp, h->id, bp, bad_scale);
+    register_kernel<false, true><<<grid, 256, 0, s>>>(W, h->wexp, h->id, bp, sr, bad_scale);
   } else {
-    register_kernel<false, false><<<grid, 256, 0, s>>>(W, nullptr, h->id, bp, bad_scale);
+    register_kernel<false, false><<<grid, 256, 0, s>>>(W, nullptr, h->id, bp, sr, bad_scale);
   }
   return cudaGetLastError();
 }

@@ -22,9 +22,14 @@
 // Block layouts (byte offsets inside one block):
 //   A even: [operand 32768]
 //   A odd : [operand 32768][q4_K: A min 4096]
-//   B even: [operand 32768][d 128 x f32]
-//   B odd : [operand 32768][d 128 x f32][q4_K: dmin 128 x f32][q4_K: B min 4096]
+//   B even: [operand 32768]
+//   B odd : [operand 32768][q4_K: B min 4096]
 // Blocks of one tile are ordered (super-block, half).
+//
+// The weight plane ends with a scale region: per (weight tile, super-block)
+// one scale block [d 128 x f32][q4_K: dmin 128 x f32], ordered like the
+// operand pairs.  The GEMM's epilogue reads it through its own small ring,
+// so the operand stages are freed by the tensor core alone.
 #pragma once
 #include <cstdint>
 
@@ -40,18 +45,16 @@ constexpr int kScaleBytes = kTileN * 4;              // 512
 
 __host__ __device__ constexpr int a_even_bytes() { return kOperandBytes; }
 __host__ __device__ constexpr int a_odd_bytes(bool q4) { return kOperandBytes + (q4 ? kMinBytes : 0); }
-__host__ __device__ constexpr int b_even_bytes() { return kOperandBytes + kScaleBytes; }
-__host__ __device__ constexpr int b_odd_bytes(bool q4) {
-  return kOperandBytes + kScaleBytes + (q4 ? kScaleBytes + kMinBytes : 0);
-}
+__host__ __device__ constexpr int b_even_bytes() { return kOperandBytes; }
+__host__ __device__ constexpr int b_odd_bytes(bool q4) { return kOperandBytes + (q4 ? kMinBytes : 0); }
 __host__ __device__ constexpr int a_pair_bytes(bool q4) { return a_even_bytes() + a_odd_bytes(q4); }
 __host__ __device__ constexpr int b_pair_bytes(bool q4) { return b_even_bytes() + b_odd_bytes(q4); }
+// one scale block: d (and dmin for q4_K) of the 128 rows of a weight tile
+__host__ __device__ constexpr int scale_block_bytes(bool q4) { return kScaleBytes * (q4 ? 2 : 1); }
 
-// offsets inside B blocks
-constexpr int kBD = kOperandBytes;                    // d
-constexpr int kBDmin = kOperandBytes + kScaleBytes;   // dmin (odd, q4_K)
-constexpr int kBMin = kOperandBytes + 2 * kScaleBytes;  // B min image (odd, q4_K)
-constexpr int kAMin = kOperandBytes;                  // A min image (odd, q4_K)
+constexpr int kAMin = kOperandBytes;   // A min image in an odd A block (q4_K)
+constexpr int kBMin = kOperandBytes;   // B min image in an odd B block (q4_K)
+constexpr int kSDmin = kScaleBytes;    // dmin row in a scale block (q4_K)
 
 // byte offset of element (row, k) of a stage operand image, k in [0, 128)
 __host__ __device__ constexpr uint32_t operand_off(int row, int k) {
@@ -71,6 +74,14 @@ __host__ __device__ constexpr uint64_t a_block(int64_t tile, int64_t sb, int hal
 __host__ __device__ constexpr uint64_t b_block(int64_t tile, int64_t sb, int half, int64_t nsb,
                                                bool q4) {
   return static_cast<uint64_t>((tile * nsb + sb) * b_pair_bytes(q4) + (half ? b_even_bytes() : 0));
+}
+// first byte of the scale region of a weight plane with n_ot tiles
+__host__ __device__ constexpr uint64_t b_scale_region(int64_t n_ot, int64_t nsb, bool q4) {
+  return static_cast<uint64_t>(n_ot * nsb) * b_pair_bytes(q4);
+}
+// scale block (tile, sb), relative to the scale region
+__host__ __device__ constexpr uint64_t b_scale_block(int64_t tile, int64_t sb, int64_t nsb, bool q4) {
+  return static_cast<uint64_t>((tile * nsb + sb) * scale_block_bytes(q4));
 }
 
 }  // namespace tiling
