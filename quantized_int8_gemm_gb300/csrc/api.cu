@@ -229,15 +229,15 @@ static int gemm_impl(mmq_weights_t h, const void *Q, int64_t nt, float *Y, mmq_s
   cudaError_t e = cudaStreamIsCapturing(s, &cap);
   if (e != cudaSuccess) return cuda_rc(e);
   const bool capturing = cap == cudaStreamCaptureStatusActive;
-  const size_t bytes = mmq::gemm_scratch_bytes(h->type, nt, h->id);
+  const size_t bytes = mmq::gemm_scratch_bytes(h, nt, true);
   void *scratch = nullptr;
   e = capturing ? cudaMallocAsync(&scratch, bytes, s)
                 : cudaMallocFromPoolAsync(&scratch, bytes, d->pool, s);
   if (e != cudaSuccess) return cuda_rc(e);
   // inside a capture the events must become real record nodes of the graph
   const unsigned ev_flags = capturing ? cudaEventRecordExternal : cudaEventRecordDefault;
-  e = mmq::launch_gemm(h, static_cast<const uint8_t *>(Q), nt, Y, scratch, d->words, next_epoch(),
-                       g_limit_ns.load(), s, ev0, ev1, ev_flags);
+  e = mmq::launch_gemm(h, static_cast<const uint8_t *>(Q), nt, Y, scratch, true, d->words,
+                       next_epoch(), g_limit_ns.load(), s, ev0, ev1, ev_flags);
   cudaError_t ef = cudaFreeAsync(scratch, s);
   if (e == cudaSuccess) e = ef;
   return cuda_rc(e);
@@ -273,12 +273,12 @@ int mmq_gemm_noalloc(mmq_weights_t h, const void *Q, int64_t nt, float *Y, mmq_s
     if (g_dev[dev].usable) d = &g_dev[dev];
   }
   if (!d) return MMQ_ERR_ARG;
-  if (mmq::gemm_scratch_bytes(h->type, nt, h->id) > mmq::kNoallocScratchBytes)
+  if (mmq::gemm_scratch_bytes(h, nt, false) > mmq::kNoallocScratchBytes)
     return MMQ_ERR_SCRATCH_LIMIT;
   void *scratch = nullptr;
   cudaError_t e = mmq::noalloc_scratch(dev, &scratch);
   if (e == cudaSuccess)
-    e = mmq::launch_gemm(h, static_cast<const uint8_t *>(Q), nt, Y, scratch, d->words,
+    e = mmq::launch_gemm(h, static_cast<const uint8_t *>(Q), nt, Y, scratch, false, d->words,
                          next_epoch(), g_limit_ns.load(), reinterpret_cast<cudaStream_t>(stream),
                          nullptr, nullptr, cudaEventRecordDefault);
   return cuda_rc(e);

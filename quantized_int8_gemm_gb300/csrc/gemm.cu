@@ -204,12 +204,54 @@ __device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
                  "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
 }
 
-template <bool kQ4>
+// The work of one CTA as segments (tile, super-blocks [sb0, sb1)).
+// Tile mode: whole tiles blockIdx.x, blockIdx.x + gridDim.x, ...
+// Stream-K mode: the (tile, super-block) units are split into gridDim.x
+// contiguous ranges of nearly equal length; a tile cut between CTAs is
+// finished by the CTA that holds its first super-block (its owner).
+struct Work {
+  int64_t u, u_end;  // stream-K: current and end unit
+  int tile;          // tile mode: next tile
+  bool sk;
+};
+__device__ __forceinline__ int64_t sk_begin(int64_t units, int cta, int ctas) {
+  return units * cta / ctas;
+}
+__device__ __forceinline__ Work work_begin(bool sk, int64_t units) {
+  Work w;
+  w.sk = sk;
+  w.u = sk_begin(units, blockIdx.x, gridDim.x);
+  w.u_end = sk_begin(units, blockIdx.x + 1, gridDim.x);
+  w.tile = blockIdx.x;
+  return w;
+}
+__device__ __forceinline__ bool work_next(Work &w, int n_tiles, int64_t nsb, int &tile, int64_t &sb0,
+                                          int64_t &sb1) {
+  if (w.sk) {
+    if (w.u >= w.u_end) return false;
+    tile = static_cast<int>(w.u / nsb);
+    sb0 = w.u % nsb;
+    sb1 = min(nsb, sb0 + (w.u_end - w.u));
+    w.u += sb1 - sb0;
+    return true;
+  }
+  if (w.tile >= n_tiles) return false;
+  tile = w.tile;
+  sb0 = 0;
+  sb1 = nsb;
+  w.tile += gridDim.x;
+  return true;
+}
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+template <bool kQ4, bool kSK>
 __global__ void __launch_bounds__(THREADS, 1)
     mmq_gemm_kernel(const uint8_t *__restrict__ aplane, const uint8_t *__restrict__ bplane,
                     const uint8_t *__restrict__ bscale, const float *__restrict__ dap,
                     const float *__restrict__ invp, int64_t nt, int64_t od, int64_t nb32, int n_tt,
-                    int n_ot, float *__restrict__ Y, WaitCtl wctl) {
+                    int n_ot, float *__restrict__ Y, WaitCtl wctl, float4 *__restrict__ ws,
+                    unsigned *__restrict__ flags) {
   using L = Smem<kQ4>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
@@ -265,9 +307,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     // scale block into the scale ring.
     uint32_t ks = 0, ns = 0, issued = 0, s_issued = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+    Work wk = work_begin(kSK, static_cast<int64_t>(n_tiles) * nsb);
+    int tile;
+    int64_t sb0, sb1;
+    while (ok && work_next(wk, n_tiles, nsb, tile, sb0, sb1)) {
       const int tt = tile % n_tt, ot = tile / n_tt;
-      for (int64_t sb = 0; sb < nsb && ok; ++sb, ++ns) {
+      for (int64_t sb = sb0; sb < sb1 && ok; ++sb, ++ns) {
         const int e = static_cast<int>(ns % SRING);
         ok = __all_sync(0xffffffffu, mbar_wait(sempty(e), ((ns / SRING) & 1) ^ 1, wctl));
         if (!ok) break;
@@ -335,8 +380,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       return got;
     };
-    for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-      for (int64_t sb = 0; sb < nsb && ok; ++sb) {
+    Work wk = work_begin(kSK, static_cast<int64_t>(n_tiles) * nsb);
+    int tile;
+    int64_t sb0, sb1;
+    while (ok && work_next(wk, n_tiles, nsb, tile, sb0, sb1)) {
+      for (int64_t sb = sb0; sb < sb1 && ok; ++sb) {
         for (int half = 0; half < 2 && ok; ++half, ++ks) {
           const int s = static_cast<int>(ks % STAGES);
           ok = __all_sync(0xffffffffu, mbar_wait(full(s), (ks / STAGES) & 1, wctl));
@@ -390,7 +438,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(rempty(slot));
     };
-    for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+    const int64_t units = static_cast<int64_t>(n_tiles) * nsb;
+    Work wk = work_begin(kSK, units);
+    int tile;
+    int64_t sb0, sb1;
+    while (ok && work_next(wk, n_tiles, nsb, tile, sb0, sb1)) {
       const int tt = tile % n_tt, ot = tile / n_tt;
       const int64_t t = static_cast<int64_t>(tt) * kTileM + row;  // < nt_pad: planes are padded
       const int64_t o0 = static_cast<int64_t>(ot) * kTileN + chalf * 64;
@@ -398,10 +450,11 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
       for (int i = 0; i < 32; ++i) y[i] = make_float2(0.f, 0.f);
       const float4 *darow = reinterpret_cast<const float4 *>(dap + t * nb32);
-      float4 nx0 = __ldg(darow), nx1 = __ldg(darow + 1);  // da' of the next super-block
-      for (int64_t sb = 0; sb < nsb && ok; ++sb) {
+      // da' of the next super-block
+      float4 nx0 = __ldg(darow + 2 * sb0), nx1 = __ldg(darow + 2 * sb0 + 1);
+      for (int64_t sb = sb0; sb < sb1 && ok; ++sb) {
         const float das[8] = {nx0.x, nx0.y, nx0.z, nx0.w, nx1.x, nx1.y, nx1.z, nx1.w};
-        if (sb + 1 < nsb) {
+        if (sb + 1 < sb1) {
           nx0 = __ldg(darow + 2 * sb + 2);
           nx1 = __ldg(darow + 2 * sb + 3);
         }
@@ -475,6 +528,58 @@ __global__ void __launch_bounds__(THREADS, 1)
         ++ns;
       }
       if (!ok) break;
+      if (kSK && (sb0 != 0 || sb1 != nsb)) {
+        // A tile cut between CTAs.  Its owner is the CTA holding its first
+        // super-block, where that CTA's range ends; the others hold the rest
+        // at the start of their ranges, so they publish their partial sums
+        // first thing and the owner, finishing its range, adds them.  Layout
+        // of a partial: 16 float4 per thread at
+        // ws[((cta * 8 + warp) * 16 + i) * 32 + lane].
+        if (sb0 != 0) {  // not the owner: publish (a CTA's first segment only)
+          float4 *dst = ws + static_cast<int64_t>(blockIdx.x * 8 + warp) * 16 * 32 + lane;
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            __stcg(dst + i * 32, make_float4(y[2 * i].x, y[2 * i].y, y[2 * i + 1].x, y[2 * i + 1].y));
+          epi_bar();
+          if (threadIdx.x == 0) {
+            __threadfence();
+            asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(flags + blockIdx.x), "r"(wctl.epoch)
+                         : "memory");
+          }
+          continue;
+        }
+        // owner: add the partials of the following CTAs that reach into this
+        // tile, in CTA order (deterministic results)
+        const int64_t tile_end = static_cast<int64_t>(tile + 1) * nsb;
+        for (int j = blockIdx.x + 1; j < static_cast<int>(gridDim.x) && sk_begin(units, j, gridDim.x) < tile_end && ok;
+             ++j) {
+          if (threadIdx.x == 0) {
+            const uint64_t t0 = globaltimer_ns();
+            unsigned v = 0;
+            for (uint32_t it = 0;; ++it) {
+              asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flags + j) : "memory");
+              if (v == wctl.epoch) break;
+              if ((it & 63u) == 63u &&
+                  (*reinterpret_cast<volatile unsigned *>(wctl.abort_epoch) == wctl.epoch ||
+                   globaltimer_ns() - t0 > wctl.limit_ns)) {
+                record_timeout(wctl);
+                break;
+              }
+              __nanosleep(64);
+            }
+          }
+          epi_bar();
+          ok = *reinterpret_cast<volatile unsigned *>(wctl.abort_epoch) != wctl.epoch;
+          const float4 *src = ws + static_cast<int64_t>(j * 8 + warp) * 16 * 32 + lane;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float4 v = __ldcg(src + i * 32);
+            y[2 * i] = __fadd2_rn(y[2 * i], make_float2(v.x, v.y));
+            y[2 * i + 1] = __fadd2_rn(y[2 * i + 1], make_float2(v.z, v.w));
+          }
+        }
+        if (!ok) break;
+      }
       if (t < nt) {
         const float inv = __ldg(invp + t);
         const float2 inv2 = make_float2(inv, inv);
@@ -519,8 +624,6 @@ __global__ void wait_selftest_kernel(WaitCtl wctl) {
   }
 }
 
-int g_num_sms[64];
-
 }  // namespace
 
 // Scratch for mmq_gemm_noalloc: a fixed device array in this module, so that
@@ -546,30 +649,78 @@ cudaError_t noalloc_scratch(int dev, void **out) {
   return cudaSuccess;
 }
 
-size_t gemm_scratch_bytes(int type, int64_t nt, int64_t id) {
-  const bool q4 = type == MMQ_Q4_K;
-  const int64_t n_tt = (nt + kTileM - 1) / kTileM, nt_pad = n_tt * kTileM;
-  const int64_t nsb = id / MMQ_QK, nb32 = id / 32;
-  const size_t a = static_cast<size_t>(n_tt * nsb) * a_pair_bytes(q4);
-  const size_t da = static_cast<size_t>(nt_pad * nb32) * 4;
-  const size_t inv = static_cast<size_t>(nt_pad) * 4;
-  return ((a + 255) / 256 + (da + 255) / 256 + (inv + 255) / 256) * 256;
+namespace {
+
+// SM count of a device, read once.
+int num_sms(int dev) {
+  static std::atomic<int> cached[64];
+  int v = cached[dev].load();
+  if (v == 0) {
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 1;
+    cached[dev].store(v);
+  }
+  return v;
+}
+
+// Launch shape and scratch layout of one GEMM call.
+struct GemmPlan {
+  bool q4, streamk;
+  int64_t n_tt, nt_pad, nsb, nb32;
+  int n_ot, n_tiles, grid;
+  size_t a_off, da_off, inv_off, ws_off, flag_off, bytes;
+};
+
+GemmPlan plan_gemm(const mmq_weights_s *h, int64_t nt, bool streamk_allowed) {
+  GemmPlan p{};
+  p.q4 = h->type == MMQ_Q4_K;
+  p.n_tt = (nt + kTileM - 1) / kTileM;
+  p.nt_pad = p.n_tt * kTileM;
+  p.nsb = h->nsb;
+  p.nb32 = h->nb32;
+  p.n_ot = static_cast<int>(h->od_pad / kTileN);
+  p.n_tiles = static_cast<int>(p.n_tt) * p.n_ot;
+  const int sms = num_sms(h->device);
+  // whole tiles per CTA, unless the last wave would leave more than a tenth
+  // of the SMs idle: then split the (tile, super-block) units evenly
+  const int64_t units = static_cast<int64_t>(p.n_tiles) * p.nsb;
+  const int64_t waves = (p.n_tiles + sms - 1) / sms;
+  const bool uneven = 10 * p.n_tiles < 9 * waves * sms;
+  p.streamk = streamk_allowed && uneven && units > p.n_tiles;
+  p.grid = p.streamk ? static_cast<int>(units < sms ? units : sms) : (p.n_tiles < sms ? p.n_tiles : sms);
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  p.a_off = 0;
+  p.da_off = up(static_cast<size_t>(p.n_tt * p.nsb) * a_pair_bytes(p.q4));
+  p.inv_off = p.da_off + up(static_cast<size_t>(p.nt_pad * p.nb32) * 4);
+  p.ws_off = p.inv_off + up(static_cast<size_t>(p.nt_pad) * 4);
+  p.flag_off = p.ws_off + (p.streamk ? static_cast<size_t>(p.grid) * kTileM * kTileN * 4 : 0);
+  p.bytes = p.flag_off + (p.streamk ? up(static_cast<size_t>(p.grid) * 4) : 0);
+  return p;
+}
+
+}  // namespace
+
+size_t gemm_scratch_bytes(const mmq_weights_s *h, int64_t nt, bool streamk_allowed) {
+  return plan_gemm(h, nt, streamk_allowed).bytes;
 }
 
 cudaError_t launch_gemm(const mmq_weights_s *h, const uint8_t *Q, int64_t nt, float *Y,
-                        void *scratch, DevStatus *st, unsigned epoch, uint64_t limit_ns,
-                        cudaStream_t s, cudaEvent_t ev0, cudaEvent_t ev1, unsigned ev_flags) {
-  const bool q4 = h->type == MMQ_Q4_K;
-  const int64_t n_tt = (nt + kTileM - 1) / kTileM, nt_pad = n_tt * kTileM;
-  const int64_t nsb = h->nsb, nb32 = h->nb32;
-  const size_t a_bytes = static_cast<size_t>(n_tt * nsb) * a_pair_bytes(q4);
-  uint8_t *aplane = static_cast<uint8_t *>(scratch);
-  float *dap = reinterpret_cast<float *>(aplane + (a_bytes + 255) / 256 * 256);
-  float *invp = dap + ((static_cast<size_t>(nt_pad * nb32) * 4 + 255) / 256 * 64);
+                        void *scratch, bool streamk_allowed, DevStatus *st, unsigned epoch,
+                        uint64_t limit_ns, cudaStream_t s, cudaEvent_t ev0, cudaEvent_t ev1,
+                        unsigned ev_flags) {
+  const GemmPlan p = plan_gemm(h, nt, streamk_allowed);
+  const bool q4 = p.q4;
+  const int64_t n_tt = p.n_tt, nt_pad = p.nt_pad, nsb = p.nsb, nb32 = p.nb32;
+  uint8_t *base8 = static_cast<uint8_t *>(scratch);
+  uint8_t *aplane = base8 + p.a_off;
+  float *dap = reinterpret_cast<float *>(base8 + p.da_off);
+  float *invp = reinterpret_cast<float *>(base8 + p.inv_off);
+  float4 *ws = p.streamk ? reinterpret_cast<float4 *>(base8 + p.ws_off) : nullptr;
+  unsigned *flags = p.streamk ? reinterpret_cast<unsigned *>(base8 + p.flag_off) : nullptr;
 
   // the last token tile's padding rows must read as zero
   cudaError_t e = cudaSuccess;
   if (nt_pad != nt) {
+    const size_t a_bytes = static_cast<size_t>(n_tt * nsb) * a_pair_bytes(q4);
     const uint64_t tail = static_cast<uint64_t>((n_tt - 1) * nsb) * a_pair_bytes(q4);
     e = cudaMemsetAsync(aplane + tail, 0, a_bytes - tail, s);
     if (e == cudaSuccess)
@@ -578,6 +729,9 @@ cudaError_t launch_gemm(const mmq_weights_s *h, const uint8_t *Q, int64_t nt, fl
       e = cudaMemsetAsync(invp + nt, 0, static_cast<size_t>(nt_pad - nt) * 4, s);
     if (e != cudaSuccess) return e;
   }
+  // stream-K hand-off flags: a partial is ready when its flag equals the epoch
+  if (p.streamk && (e = cudaMemsetAsync(flags, 0, static_cast<size_t>(p.grid) * 4, s)) != cudaSuccess)
+    return e;
   const unsigned pgrid = static_cast<unsigned>(nt);
   if (q4)
     gemm_prepass_kernel<true><<<pgrid, 128, 0, s>>>(Q, nt, nb32, aplane, dap, invp);
@@ -586,27 +740,25 @@ cudaError_t launch_gemm(const mmq_weights_s *h, const uint8_t *Q, int64_t nt, fl
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
-  auto kern = q4 ? mmq_gemm_kernel<true> : mmq_gemm_kernel<false>;
+  auto kern = q4 ? (p.streamk ? mmq_gemm_kernel<true, true> : mmq_gemm_kernel<true, false>)
+                 : (p.streamk ? mmq_gemm_kernel<false, true> : mmq_gemm_kernel<false, false>);
   const int smem = q4 ? Smem<true>::kBytes : Smem<false>::kBytes;
-  // the shared-memory opt-in and the SM count are read once per device,
-  // outside any stream capture the first call is not part of
-  static std::atomic<uint32_t> attr_done[64][2];
+  // the shared-memory opt-in is set once per device, outside any stream
+  // capture the first call is not part of
+  static std::atomic<uint32_t> attr_done[64][4];
   const int dev = h->device;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!attr_done[dev][q4].load()) {
+  const int variant = (q4 ? 2 : 0) + (p.streamk ? 1 : 0);
+  if (!attr_done[dev][variant].load()) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g_num_sms[dev], cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    attr_done[dev][q4].store(1);
+    attr_done[dev][variant].store(1);
   }
-  const int n_ot = static_cast<int>(h->od_pad / kTileN);
-  const int n_tiles = static_cast<int>(n_tt) * n_ot;
-  const int grid = n_tiles < g_num_sms[dev] ? n_tiles : g_num_sms[dev];
   WaitCtl w{&st->status, &st->abort_epoch, epoch, limit_ns};
   if (ev0 && (e = cudaEventRecordWithFlags(ev0, s, ev_flags)) != cudaSuccess) return e;
   const uint8_t *bp = static_cast<const uint8_t *>(h->bplane);
-  kern<<<grid, THREADS, smem, s>>>(aplane, bp, bp + b_scale_region(n_ot, nsb, q4), dap, invp, nt,
-                                   h->od, nb32, static_cast<int>(n_tt), n_ot, Y, w);
+  kern<<<p.grid, THREADS, smem, s>>>(aplane, bp, bp + b_scale_region(p.n_ot, nsb, q4), dap, invp, nt,
+                                     h->od, nb32, static_cast<int>(n_tt), p.n_ot, Y, w, ws, flags);
   e = cudaGetLastError();
   if (e == cudaSuccess && ev1) e = cudaEventRecordWithFlags(ev1, s, ev_flags);
   return e;

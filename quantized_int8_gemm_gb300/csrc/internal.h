@@ -47,12 +47,15 @@ cudaError_t launch_register(const mmq_weights_s *h, const uint8_t *W, int *bad_s
                             cudaStream_t s);
 
 // GEMM: scratch bytes for nt tokens, and the launch of the activation
-// prepass + GEMM kernel.  ev0/ev1 (optional) are recorded around the GEMM
-// kernel with cudaEventRecordWithFlags(ev, s, ev_flags).
-size_t gemm_scratch_bytes(int type, int64_t nt, int64_t id);
+// prepass + GEMM kernel.  With streamk_allowed the GEMM may split tiles
+// between CTAs (and then needs more scratch).  ev0/ev1 (optional) are
+// recorded around the GEMM kernel with cudaEventRecordWithFlags(ev, s,
+// ev_flags).
+size_t gemm_scratch_bytes(const mmq_weights_s *h, int64_t nt, bool streamk_allowed);
 cudaError_t launch_gemm(const mmq_weights_s *h, const uint8_t *Q, int64_t nt, float *Y,
-                        void *scratch, DevStatus *st, unsigned epoch, uint64_t limit_ns,
-                        cudaStream_t s, cudaEvent_t ev0, cudaEvent_t ev1, unsigned ev_flags);
+                        void *scratch, bool streamk_allowed, DevStatus *st, unsigned epoch,
+                        uint64_t limit_ns, cudaStream_t s, cudaEvent_t ev0, cudaEvent_t ev1,
+                        unsigned ev_flags);
 
 cudaError_t launch_wait_selftest(DevStatus *st, unsigned epoch, uint64_t limit_ns,
                                  cudaStream_t s);

@@ -97,6 +97,10 @@ SMALL = [
     ("q4_K", 384, 1024, 256, 5),   # second token tile starts at i0 = 128
     ("q6_K", 129, 2048, 127, 6),
     ("q4_K", 128, 768, 128, 7),
+    # few tiles, many super-blocks: the (tile, super-block) work is split over
+    # all SMs, each tile between several CTAs that hand partial sums over
+    ("q6_K", 1000, 4096, 300, 8),
+    ("q4_K", 700, 3072, 200, 9),
 ]
 
 
