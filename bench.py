@@ -269,9 +269,17 @@ def run_mine(args, cfg, rank, world):
     Ys = [torch.empty((nt, od), dtype=torch.float32, device=dev) for _ in range(n_sets)]
     del W_dev
 
+    fused = args.step == "fused"
+
     def step(i, ev=None):
         j = i % n_sets
-        mmq.mmq_quantize_act(Xs[j], Qs[j])
+        if fused:  # X -> operand plane -> Y: two kernels
+            if ev is None:
+                mmq.mmq_gemm_f32(ws[j], Xs[j], Ys[j])
+            else:
+                mmq.mmq_gemm_f32_profiled(ws[j], Xs[j], Ys[j], ev[0], ev[1])
+            return
+        mmq.mmq_quantize_act(Xs[j], Qs[j])  # X -> pad40 Q -> operand plane -> Y: three kernels
         if ev is None:
             mmq.mmq_gemm(ws[j], Qs[j], nt, Ys[j])
         else:
@@ -375,8 +383,11 @@ def run_mine(args, cfg, rank, world):
         def e2e_step(i):
             j = i % n_sets
             Xs[j].copy_(Xh[i % 2], non_blocking=True)
-            mmq.mmq_quantize_act(Xs[j], Qs[j])
-            mmq.mmq_gemm(ws[j], Qs[j], nt, Ys[j])
+            if fused:
+                mmq.mmq_gemm_f32(ws[j], Xs[j], Ys[j])
+            else:
+                mmq.mmq_quantize_act(Xs[j], Qs[j])
+                mmq.mmq_gemm(ws[j], Qs[j], nt, Ys[j])
             Yh.copy_(Ys[j], non_blocking=True)
 
         with torch.cuda.stream(stream):
@@ -398,7 +409,8 @@ def run_mine(args, cfg, rank, world):
         e2e = {"value": world * ops * E / (e_ms * 1e-3) / 1e12, "unit": UNIT,
                "h2d_bytes_per_step": nt * id_ * 4, "d2h_bytes_per_step": nt * od * 4,
                "steps": E, "ms_per_step": e_ms / E,
-               "path": "pinned host X -> device, mmq_quantize_act, mmq_gemm, Y -> pinned host"}
+               "path": ("pinned host X -> device, mmq_gemm_f32, Y -> pinned host" if fused else
+                        "pinned host X -> device, mmq_quantize_act, mmq_gemm, Y -> pinned host")}
 
     # ---- the oracle on the host cores (rank 0, N = 1 only)
     cpu = None
@@ -417,7 +429,8 @@ def run_mine(args, cfg, rank, world):
             "vs_baseline": (value / PAGES_TOPS[cfg.name]) if cfg.name in PAGES_TOPS else None,
             "dtype": "s8 x k-quant ints on f16 UMMA, f32 accumulate", "data": "synthetic",
             "config": {"workload": cfg.name, "qtype": cfg.qtype, "od": od, "id": id_, "nt": nt,
-                       "step": "mmq_quantize_act + mmq_gemm",
+                       "step": ("mmq_gemm_f32 (fused q8_0 quantization + GEMM)" if fused
+                                else "mmq_quantize_act + mmq_gemm"),
                        "cuda_graph": (f"{len(graphs)} graphs of <= {args.graph_chunk} steps"
                                       if use_graph else False),
                        "l2": f"inputs larger than L2: {n_sets} rotating sets x "
@@ -429,7 +442,7 @@ def run_mine(args, cfg, rank, world):
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": 3 * K,
+            "gpu_launches": (2 if fused else 3) * K,
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
@@ -452,6 +465,8 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--graph-chunk", type=int, default=500)
+    ap.add_argument("--step", choices=("fused", "two"), default="fused",
+                    help="fused: mmq_gemm_f32; two: mmq_quantize_act then mmq_gemm")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -10,6 +10,7 @@
  *   mmq_register_weights W (packed k-quant)  -> handle (internal planes,
  *                                               optional dense W_exp plane)
  *   mmq_gemm             handle, Q           -> Y (fp32)
+ * and mmq_gemm_f32 (handle, X -> Y) for the two steps fused.
  *
  * Conventions for every entry point:
  *   - Pointers named "device" are CUDA device pointers on the current device;
@@ -171,6 +172,21 @@ int mmq_gemm(mmq_weights_t h, const void *Q, int64_t nt, float *Y, mmq_stream_t 
              uint32_t flags, int *arm_used);
 
 /*
+ * mmq_gemm_f32 -- the GEMM straight from fp32 activations: each token is
+ * quantized to q8_0 exactly as mmq_quantize_act does and fed to the
+ * contraction without the pad40 plane being written: the producer emits the
+ * quantized operand plane directly, the step after the separate
+ * quantize-transpose prepass in "26 · r21 — Coalesced block-linear A
+ * staging", §5.  Y is bit-identical to mmq_quantize_act followed by
+ * mmq_gemm on the same X.
+ *   X     device, fp32, nt x id row-major, 16-byte aligned.
+ *   Other arguments, scratch, the out-of-contract inputs of mmq_quantize_act
+ *   and the errors as mmq_gemm.
+ */
+int mmq_gemm_f32(mmq_weights_t h, const float *X, int64_t nt, float *Y, mmq_stream_t stream,
+                 uint32_t flags, int *arm_used);
+
+/*
  * mmq_gemm_profiled -- mmq_gemm that also records two caller-created CUDA
  * events (cudaEvent_t, either may be NULL) on `stream` immediately before
  * and after the main GEMM kernel, so the caller can time that kernel alone.
@@ -178,6 +194,11 @@ int mmq_gemm(mmq_weights_t h, const void *Q, int64_t nt, float *Y, mmq_stream_t 
  */
 int mmq_gemm_profiled(mmq_weights_t h, const void *Q, int64_t nt, float *Y, mmq_stream_t stream,
                       uint32_t flags, int *arm_used, void *ev_start, void *ev_stop);
+
+/* mmq_gemm_f32 with the same two events around its main GEMM kernel. */
+int mmq_gemm_f32_profiled(mmq_weights_t h, const float *X, int64_t nt, float *Y,
+                          mmq_stream_t stream, uint32_t flags, int *arm_used, void *ev_start,
+                          void *ev_stop);
 
 /*
  * mmq_gemm_noalloc -- mmq_gemm for callers that cannot allocate device

@@ -14,6 +14,8 @@ from .mmq import (  # noqa: F401
     Weights,
     load,
     mmq_gemm,
+    mmq_gemm_f32,
+    mmq_gemm_f32_profiled,
     mmq_gemm_noalloc,
     mmq_gemm_profiled,
     mmq_last_device_error,

@@ -209,14 +209,17 @@ int mmq_weights_info(mmq_weights_t h, int *type, int64_t *od, int64_t *id,
   return MMQ_OK;
 }
 
-static int gemm_impl(mmq_weights_t h, const void *Q, int64_t nt, float *Y, mmq_stream_t stream,
-                     uint32_t flags, int *arm_used, cudaEvent_t ev0, cudaEvent_t ev1) {
+// Q (pad40 blocks) or X (fp32 activations, quantized on the fly) -> Y.
+static int gemm_impl(mmq_weights_t h, const void *Q, const float *X, int64_t nt, float *Y,
+                     mmq_stream_t stream, uint32_t flags, int *arm_used, cudaEvent_t ev0,
+                     cudaEvent_t ev1) {
   if (!h || nt < 0 || nt > kMaxTokens) return MMQ_ERR_ARG;
   if (flags != MMQ_ARM_AUTO && flags != MMQ_ARM_F16) return MMQ_ERR_UNSUPPORTED;
   if (arm_used) *arm_used = MMQ_ARM_F16;
   if (nt == 0) return MMQ_OK;
-  if (!Q || !Y) return MMQ_ERR_ARG;
-  if (!aligned16(Q) || !aligned16(Y)) return MMQ_ERR_ALIGN;
+  const void *A = X ? static_cast<const void *>(X) : Q;
+  if (!A || !Y) return MMQ_ERR_ARG;
+  if (!aligned16(A) || !aligned16(Y)) return MMQ_ERR_ALIGN;
   int dev;
   DeviceState *d;
   if (int rc = device_state(&dev, &d)) return rc;
@@ -236,7 +239,7 @@ static int gemm_impl(mmq_weights_t h, const void *Q, int64_t nt, float *Y, mmq_s
   if (e != cudaSuccess) return cuda_rc(e);
   // inside a capture the events must become real record nodes of the graph
   const unsigned ev_flags = capturing ? cudaEventRecordExternal : cudaEventRecordDefault;
-  e = mmq::launch_gemm(h, static_cast<const uint8_t *>(Q), nt, Y, scratch, true, d->words,
+  e = mmq::launch_gemm(h, static_cast<const uint8_t *>(Q), X, nt, Y, scratch, true, d->words,
                        next_epoch(), g_limit_ns.load(), s, ev0, ev1, ev_flags);
   cudaError_t ef = cudaFreeAsync(scratch, s);
   if (e == cudaSuccess) e = ef;
@@ -245,12 +248,26 @@ static int gemm_impl(mmq_weights_t h, const void *Q, int64_t nt, float *Y, mmq_s
 
 int mmq_gemm(mmq_weights_t h, const void *Q, int64_t nt, float *Y, mmq_stream_t stream,
              uint32_t flags, int *arm_used) {
-  return gemm_impl(h, Q, nt, Y, stream, flags, arm_used, nullptr, nullptr);
+  return gemm_impl(h, Q, nullptr, nt, Y, stream, flags, arm_used, nullptr, nullptr);
+}
+
+int mmq_gemm_f32(mmq_weights_t h, const float *X, int64_t nt, float *Y, mmq_stream_t stream,
+                 uint32_t flags, int *arm_used) {
+  if (!X && nt > 0) return MMQ_ERR_ARG;
+  return gemm_impl(h, nullptr, X, nt, Y, stream, flags, arm_used, nullptr, nullptr);
+}
+
+int mmq_gemm_f32_profiled(mmq_weights_t h, const float *X, int64_t nt, float *Y,
+                          mmq_stream_t stream, uint32_t flags, int *arm_used, void *ev_start,
+                          void *ev_stop) {
+  if (!X && nt > 0) return MMQ_ERR_ARG;
+  return gemm_impl(h, nullptr, X, nt, Y, stream, flags, arm_used,
+                   static_cast<cudaEvent_t>(ev_start), static_cast<cudaEvent_t>(ev_stop));
 }
 
 int mmq_gemm_profiled(mmq_weights_t h, const void *Q, int64_t nt, float *Y, mmq_stream_t stream,
                       uint32_t flags, int *arm_used, void *ev_start, void *ev_stop) {
-  return gemm_impl(h, Q, nt, Y, stream, flags, arm_used, static_cast<cudaEvent_t>(ev_start),
+  return gemm_impl(h, Q, nullptr, nt, Y, stream, flags, arm_used, static_cast<cudaEvent_t>(ev_start),
                    static_cast<cudaEvent_t>(ev_stop));
 }
 
@@ -278,7 +295,7 @@ int mmq_gemm_noalloc(mmq_weights_t h, const void *Q, int64_t nt, float *Y, mmq_s
   void *scratch = nullptr;
   cudaError_t e = mmq::noalloc_scratch(dev, &scratch);
   if (e == cudaSuccess)
-    e = mmq::launch_gemm(h, static_cast<const uint8_t *>(Q), nt, Y, scratch, false, d->words,
+    e = mmq::launch_gemm(h, static_cast<const uint8_t *>(Q), nullptr, nt, Y, scratch, false, d->words,
                          next_epoch(), g_limit_ns.load(), reinterpret_cast<cudaStream_t>(stream),
                          nullptr, nullptr, cudaEventRecordDefault);
   return cuda_rc(e);

@@ -180,6 +180,161 @@ __global__ void __launch_bounds__(128) gemm_prepass_kernel(const uint8_t *__rest
   }
 }
 
+// ---------------------------------------------------------------- fused quantization
+// The same per-token result as mmq_quantize_act followed by the prepass
+// above, straight from fp32 activations: one CTA of 128 threads per token,
+// eight lanes per 32-value block (one float4 each).  The quantization is the
+// q8_0 rule of quantize.cu (d = amax/127 by IEEE division, q = round half
+// away from zero of x/d, d16 = fp16_rn(d)), so the operand plane, da' and the
+// min slots are bit-identical to the two-kernel path.  For q4_K the token's
+// scale exponent s_t needs every block first: a first pass computes it, the
+// second (reading X again, from L2) writes the planes.
+__device__ __forceinline__ void quant_block8(float4 v, float &d, float &d16f, uint32_t &h01,
+                                             uint32_t &h23, int &ssum) {
+  float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+#pragma unroll
+  for (int m = 1; m < 8; m <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+  d = amax / 127.0f;
+  int q[4] = {0, 0, 0, 0};
+  if (amax != 0.0f) {
+    const float xs[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) q[i] = max(-127, min(127, static_cast<int>(roundf(xs[i] / d))));
+  }
+  ssum = q[0] + q[1] + q[2] + q[3];
+#pragma unroll
+  for (int m = 1; m < 8; m <<= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, m);
+  d16f = amax != 0.0f ? __half2float(__float2half_rn(d)) : 0.0f;
+  h01 = static_cast<uint32_t>(__half_as_ushort(__int2half_rn(q[0]))) |
+        (static_cast<uint32_t>(__half_as_ushort(__int2half_rn(q[1]))) << 16);
+  h23 = static_cast<uint32_t>(__half_as_ushort(__int2half_rn(q[2]))) |
+        (static_cast<uint32_t>(__half_as_ushort(__int2half_rn(q[3]))) << 16);
+}
+
+// One 32-value block's results in the token's operand row, da' plane and
+// (q4_K) min-term slots; lane `part` of the block's eight writes its 4 values.
+template <bool kQ4>
+__device__ __forceinline__ void emit_block(uint8_t *__restrict__ aplane, float *__restrict__ dap,
+                                           int64_t t, int64_t c, int64_t nb32, int part,
+                                           uint32_t h01, uint32_t h23, float d16f, int ssum,
+                                           float scale) {
+  const int64_t nsb = nb32 / 8;
+  const int r = static_cast<int>(t & (kTileM - 1));
+  const int64_t tile = t / kTileM, sb = c >> 3;
+  const int half = static_cast<int>((c >> 2) & 1);
+  uint8_t *blk = aplane + a_block(tile, sb, half, nsb, kQ4);
+  const int k0 = static_cast<int>(c & 3) * 32;
+  *reinterpret_cast<uint2 *>(blk + operand_off(r, k0 + 4 * part)) = make_uint2(h01, h23);
+  if (part == 0) {
+    dap[t * nb32 + c] = d16f * scale;
+    if (kQ4) {
+      const float g = d16f * static_cast<float>(ssum) * scale;  // exact
+      const __half hi = __float2half_rn(g);
+      const __half lo = __float2half_rn(g - __half2float(hi));
+      uint8_t *mblk = aplane + a_block(tile, sb, 1, nsb, true) + kAMin;
+      const uint32_t pair = static_cast<uint32_t>(__half_as_ushort(hi)) |
+                            (static_cast<uint32_t>(__half_as_ushort(lo)) << 16);
+      *reinterpret_cast<uint32_t *>(mblk + min_off(r, 2 * static_cast<int>(c & 7))) = pair;
+    }
+  }
+}
+
+// kStash (q4_K): the first pass keeps every block's results in shared memory
+// (72 B per block: 16 operand words, d16, ssum) for the second; otherwise the
+// second pass re-reads X and quantizes again.  Each warp takes 16 blocks per
+// step, four loads in flight per lane.
+constexpr int kStashBytesPerBlock = 72;
+constexpr int kStashMaxBytes = 48 * 1024;
+
+template <bool kQ4, bool kStash>
+__global__ void __launch_bounds__(128) quantize_prepass_kernel(const float *__restrict__ X,
+                                                               int64_t nt, int64_t nb32,
+                                                               uint8_t *__restrict__ aplane,
+                                                               float *__restrict__ dap,
+                                                               float *__restrict__ invp) {
+  extern __shared__ uint32_t stash[];  // [nb32][16] operand words, then [nb32] d16, [nb32] ssum
+  const int64_t t = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int part = lane & 7, grp = lane >> 3;
+  const float4 *xrow = reinterpret_cast<const float4 *>(X + t * nb32 * 32);
+  float *sd16 = reinterpret_cast<float *>(stash + nb32 * 16);
+  int *sssum = reinterpret_cast<int *>(sd16 + nb32);
+  float gmax = 0.f;
+  // pass 1 (the only one for q6_K, whose operands need no token scale)
+  for (int64_t base = warp * 16; base < nb32; base += 64) {
+    float4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t c = base + u * 4 + grp;
+      v[u] = c < nb32 ? __ldg(xrow + c * 8 + part) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t c = base + u * 4 + grp;
+      float d, d16f;
+      uint32_t h01, h23;
+      int ssum;
+      quant_block8(v[u], d, d16f, h01, h23, ssum);
+      if (c >= nb32) continue;
+      if (!kQ4) {
+        emit_block<false>(aplane, dap, t, c, nb32, part, h01, h23, d16f, ssum, 1.0f);
+      } else {
+        gmax = fmaxf(gmax, fabsf(d16f * static_cast<float>(ssum)));
+        if (kStash) {
+          reinterpret_cast<uint2 *>(stash + c * 16)[part] = make_uint2(h01, h23);
+          if (part == 0) {
+            sd16[c] = d16f;
+            sssum[c] = ssum;
+          }
+        }
+      }
+    }
+  }
+  if constexpr (!kQ4) {
+    if (tid == 0) invp[t] = 1.0f;
+  } else {
+  // s_t: the token's largest |d16 * ssum| lands in [2^14, 2^15)
+  __shared__ float wmax[4];
+#pragma unroll
+  for (int m = 16; m; m >>= 1) gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, m));
+  if (lane == 0) wmax[warp] = gmax;
+  __syncthreads();
+  gmax = fmaxf(fmaxf(wmax[0], wmax[1]), fmaxf(wmax[2], wmax[3]));
+  int s = 0;
+  if (gmax > 0.f) {
+    const int e = static_cast<int>((__float_as_uint(gmax) >> 23) & 0xFF) - 127;
+    s = min(30, max(-30, 14 - e));
+  }
+  const float scale = __uint_as_float(static_cast<uint32_t>(127 + s) << 23);
+  if (tid == 0) invp[t] = __uint_as_float(static_cast<uint32_t>(127 - s) << 23);
+  // pass 2
+  if (kStash) {
+    for (int64_t c = tid >> 3; c < nb32; c += 16) {
+      const uint2 hw = reinterpret_cast<const uint2 *>(stash + c * 16)[part];
+      emit_block<true>(aplane, dap, t, c, nb32, part, hw.x, hw.y, sd16[c], sssum[c], scale);
+    }
+  } else {
+    for (int64_t base = warp * 16; base < nb32; base += 64) {
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int64_t c = base + u * 4 + grp;
+        v[u] = c < nb32 ? __ldg(xrow + c * 8 + part) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int64_t c = base + u * 4 + grp;
+        float d, d16f;
+        uint32_t h01, h23;
+        int ssum;
+        quant_block8(v[u], d, d16f, h01, h23, ssum);
+        if (c < nb32) emit_block<true>(aplane, dap, t, c, nb32, part, h01, h23, d16f, ssum, scale);
+      }
+    }
+  }
+  }
+}
+
 // ---------------------------------------------------------------- the GEMM
 // acc[h*16 ..] = da * S (first chunk of a super-block) or += da * S, on one
 // 32-column half h of a chunk.
@@ -251,7 +406,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const uint8_t *__restrict__ bscale, const float *__restrict__ dap,
                     const float *__restrict__ invp, int64_t nt, int64_t od, int64_t nb32, int n_tt,
                     int n_ot, float *__restrict__ Y, WaitCtl wctl, float4 *__restrict__ ws,
-                    unsigned *__restrict__ flags) {
+                    uint64_t *__restrict__ flags) {
   using L = Smem<kQ4>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
@@ -529,6 +684,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       if (!ok) break;
       if (kSK && (sb0 != 0 || sb1 != nsb)) {
+        // hand-off tag of this launch: the scratch holding the flags is not
+        // cleared, so the tag pairs the epoch with its complement
+        const uint64_t tag = (static_cast<uint64_t>(wctl.epoch) << 32) | static_cast<uint32_t>(~wctl.epoch);
         // A tile cut between CTAs.  Its owner is the CTA holding its first
         // super-block, where that CTA's range ends; the others hold the rest
         // at the start of their ranges, so they publish their partial sums
@@ -543,7 +701,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           epi_bar();
           if (threadIdx.x == 0) {
             __threadfence();
-            asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(flags + blockIdx.x), "r"(wctl.epoch)
+            asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(flags + blockIdx.x), "l"(tag)
                          : "memory");
           }
           continue;
@@ -555,10 +713,10 @@ __global__ void __launch_bounds__(THREADS, 1)
              ++j) {
           if (threadIdx.x == 0) {
             const uint64_t t0 = globaltimer_ns();
-            unsigned v = 0;
+            uint64_t v = 0;
             for (uint32_t it = 0;; ++it) {
-              asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flags + j) : "memory");
-              if (v == wctl.epoch) break;
+              asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(flags + j) : "memory");
+              if (v == tag) break;
               if ((it & 63u) == 63u &&
                   (*reinterpret_cast<volatile unsigned *>(wctl.abort_epoch) == wctl.epoch ||
                    globaltimer_ns() - t0 > wctl.limit_ns)) {
@@ -693,7 +851,7 @@ GemmPlan plan_gemm(const mmq_weights_s *h, int64_t nt, bool streamk_allowed) {
   p.inv_off = p.da_off + up(static_cast<size_t>(p.nt_pad * p.nb32) * 4);
   p.ws_off = p.inv_off + up(static_cast<size_t>(p.nt_pad) * 4);
   p.flag_off = p.ws_off + (p.streamk ? static_cast<size_t>(p.grid) * kTileM * kTileN * 4 : 0);
-  p.bytes = p.flag_off + (p.streamk ? up(static_cast<size_t>(p.grid) * 4) : 0);
+  p.bytes = p.flag_off + (p.streamk ? up(static_cast<size_t>(p.grid) * 8) : 0);
   return p;
 }
 
@@ -703,10 +861,10 @@ size_t gemm_scratch_bytes(const mmq_weights_s *h, int64_t nt, bool streamk_allow
   return plan_gemm(h, nt, streamk_allowed).bytes;
 }
 
-cudaError_t launch_gemm(const mmq_weights_s *h, const uint8_t *Q, int64_t nt, float *Y,
-                        void *scratch, bool streamk_allowed, DevStatus *st, unsigned epoch,
-                        uint64_t limit_ns, cudaStream_t s, cudaEvent_t ev0, cudaEvent_t ev1,
-                        unsigned ev_flags) {
+cudaError_t launch_gemm(const mmq_weights_s *h, const uint8_t *Q, const float *X, int64_t nt,
+                        float *Y, void *scratch, bool streamk_allowed, DevStatus *st,
+                        unsigned epoch, uint64_t limit_ns, cudaStream_t s, cudaEvent_t ev0,
+                        cudaEvent_t ev1, unsigned ev_flags) {
   const GemmPlan p = plan_gemm(h, nt, streamk_allowed);
   const bool q4 = p.q4;
   const int64_t n_tt = p.n_tt, nt_pad = p.nt_pad, nsb = p.nsb, nb32 = p.nb32;
@@ -715,7 +873,7 @@ cudaError_t launch_gemm(const mmq_weights_s *h, const uint8_t *Q, int64_t nt, fl
   float *dap = reinterpret_cast<float *>(base8 + p.da_off);
   float *invp = reinterpret_cast<float *>(base8 + p.inv_off);
   float4 *ws = p.streamk ? reinterpret_cast<float4 *>(base8 + p.ws_off) : nullptr;
-  unsigned *flags = p.streamk ? reinterpret_cast<unsigned *>(base8 + p.flag_off) : nullptr;
+  uint64_t *flags = p.streamk ? reinterpret_cast<uint64_t *>(base8 + p.flag_off) : nullptr;
 
   // the last token tile's padding rows must read as zero
   cudaError_t e = cudaSuccess;
@@ -729,14 +887,21 @@ cudaError_t launch_gemm(const mmq_weights_s *h, const uint8_t *Q, int64_t nt, fl
       e = cudaMemsetAsync(invp + nt, 0, static_cast<size_t>(nt_pad - nt) * 4, s);
     if (e != cudaSuccess) return e;
   }
-  // stream-K hand-off flags: a partial is ready when its flag equals the epoch
-  if (p.streamk && (e = cudaMemsetAsync(flags, 0, static_cast<size_t>(p.grid) * 4, s)) != cudaSuccess)
-    return e;
+  // activation operand plane: from pad40 blocks, or quantized from fp32 X
   const unsigned pgrid = static_cast<unsigned>(nt);
-  if (q4)
+  if (X) {
+    const size_t stash = static_cast<size_t>(nb32) * kStashBytesPerBlock;
+    if (!q4)
+      quantize_prepass_kernel<false, false><<<pgrid, 128, 0, s>>>(X, nt, nb32, aplane, dap, invp);
+    else if (stash <= static_cast<size_t>(kStashMaxBytes))
+      quantize_prepass_kernel<true, true><<<pgrid, 128, stash, s>>>(X, nt, nb32, aplane, dap, invp);
+    else
+      quantize_prepass_kernel<true, false><<<pgrid, 128, 0, s>>>(X, nt, nb32, aplane, dap, invp);
+  } else if (q4) {
     gemm_prepass_kernel<true><<<pgrid, 128, 0, s>>>(Q, nt, nb32, aplane, dap, invp);
-  else
+  } else {
     gemm_prepass_kernel<false><<<pgrid, 128, 0, s>>>(Q, nt, nb32, aplane, dap, invp);
+  }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 

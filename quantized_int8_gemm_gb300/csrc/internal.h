@@ -52,10 +52,12 @@ cudaError_t launch_register(const mmq_weights_s *h, const uint8_t *W, int *bad_s
 // recorded around the GEMM kernel with cudaEventRecordWithFlags(ev, s,
 // ev_flags).
 size_t gemm_scratch_bytes(const mmq_weights_s *h, int64_t nt, bool streamk_allowed);
-cudaError_t launch_gemm(const mmq_weights_s *h, const uint8_t *Q, int64_t nt, float *Y,
-                        void *scratch, bool streamk_allowed, DevStatus *st, unsigned epoch,
-                        uint64_t limit_ns, cudaStream_t s, cudaEvent_t ev0, cudaEvent_t ev1,
-                        unsigned ev_flags);
+// The activations come either as pad40 blocks Q or, when X is non-null, as
+// fp32 rows quantized on the fly (Q is then ignored).
+cudaError_t launch_gemm(const mmq_weights_s *h, const uint8_t *Q, const float *X, int64_t nt,
+                        float *Y, void *scratch, bool streamk_allowed, DevStatus *st,
+                        unsigned epoch, uint64_t limit_ns, cudaStream_t s, cudaEvent_t ev0,
+                        cudaEvent_t ev1, unsigned ev_flags);
 
 cudaError_t launch_wait_selftest(DevStatus *st, unsigned epoch, uint64_t limit_ns,
                                  cudaStream_t s);

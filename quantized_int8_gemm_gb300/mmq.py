@@ -41,7 +41,8 @@ BLOCK_BYTES = {MMQ_Q4_K: 144, MMQ_Q6_K: 210}
 
 EXPORTS = [
     "mmq_quantize_act", "mmq_register_weights", "mmq_release_weights", "mmq_weights_wexp",
-    "mmq_weights_info", "mmq_gemm", "mmq_gemm_profiled", "mmq_gemm_noalloc",
+    "mmq_weights_info", "mmq_gemm", "mmq_gemm_f32", "mmq_gemm_profiled", "mmq_gemm_f32_profiled",
+    "mmq_gemm_noalloc",
     "mmq_last_device_error", "mmq_set_wait_timeout_ns",
     "mmq_selftest_wait_timeout", "mmq_strerror",
 ]
@@ -75,7 +76,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
                                        ctypes.POINTER(i64), ctypes.POINTER(i64),
                                        ctypes.POINTER(i64), ctypes.POINTER(i64)]
         L.mmq_gemm.argtypes = [vp, vp, i64, vp, vp, u32, ctypes.POINTER(i32)]
+        L.mmq_gemm_f32.argtypes = [vp, vp, i64, vp, vp, u32, ctypes.POINTER(i32)]
         L.mmq_gemm_profiled.argtypes = [vp, vp, i64, vp, vp, u32, ctypes.POINTER(i32), vp, vp]
+        L.mmq_gemm_f32_profiled.argtypes = [vp, vp, i64, vp, vp, u32, ctypes.POINTER(i32), vp, vp]
         L.mmq_gemm_noalloc.argtypes = [vp, vp, i64, vp, vp]
         L.mmq_last_device_error.argtypes = []
         L.mmq_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
@@ -198,6 +201,22 @@ def mmq_gemm(w: Weights, Q: torch.Tensor, nt: int, Y: torch.Tensor | None = None
     return (Y, arm.value) if return_arm else Y
 
 
+def mmq_gemm_f32(w: Weights, X: torch.Tensor, Y: torch.Tensor | None = None, stream=None,
+                 flags: int = MMQ_ARM_AUTO, return_arm: bool = False):
+    """Y (nt, od) fp32 from fp32 activations X (nt, id), quantized on the fly."""
+    if X.dtype != torch.float32 or X.dim() != 2 or X.shape[1] != w.id:
+        raise ValueError("X must be float32 (nt, id)")
+    nt = X.shape[0]
+    if Y is None:
+        Y = torch.empty((nt, w.od), dtype=torch.float32, device=X.device)
+    if Y.dtype != torch.float32 or Y.numel() != nt * w.od:
+        raise ValueError("Y must be float32 with nt*od elements")
+    arm = ctypes.c_int(0)
+    _check(load().mmq_gemm_f32(w.handle, _dev_ptr(X, "X"), nt, _dev_ptr(Y, "Y"), _stream(stream),
+                               flags, ctypes.byref(arm)), "mmq_gemm_f32")
+    return (Y, arm.value) if return_arm else Y
+
+
 def mmq_gemm_profiled(w: Weights, Q: torch.Tensor, nt: int, Y: torch.Tensor,
                       ev_start: torch.cuda.Event, ev_stop: torch.cuda.Event, stream=None,
                       flags: int = MMQ_ARM_AUTO) -> int:
@@ -208,6 +227,19 @@ def mmq_gemm_profiled(w: Weights, Q: torch.Tensor, nt: int, Y: torch.Tensor,
                                     _stream(stream), flags, ctypes.byref(arm),
                                     ctypes.c_void_p(ev_start.cuda_event),
                                     ctypes.c_void_p(ev_stop.cuda_event)), "mmq_gemm_profiled")
+    return arm.value
+
+
+def mmq_gemm_f32_profiled(w: Weights, X: torch.Tensor, Y: torch.Tensor,
+                          ev_start: torch.cuda.Event, ev_stop: torch.cuda.Event, stream=None,
+                          flags: int = MMQ_ARM_AUTO) -> int:
+    """mmq_gemm_f32 that records ev_start / ev_stop around the main GEMM kernel."""
+    arm = ctypes.c_int(0)
+    _check(load().mmq_gemm_f32_profiled(w.handle, _dev_ptr(X, "X"), X.shape[0], _dev_ptr(Y, "Y"),
+                                        _stream(stream), flags, ctypes.byref(arm),
+                                        ctypes.c_void_p(ev_start.cuda_event),
+                                        ctypes.c_void_p(ev_stop.cuda_event)),
+           "mmq_gemm_f32_profiled")
     return arm.value
 
 

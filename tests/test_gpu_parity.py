@@ -247,3 +247,29 @@ def test_repeat_calls_are_deterministic(mmq):
         Y2 = mmq.mmq_gemm(w, Q, nt, stream=s)
     s.synchronize()
     assert torch.equal(Y1, Y2)
+
+
+# --------------------------------------------------------------------------
+# fused quantization: fp32 activations straight into the operand plane
+@pytest.mark.parametrize("name,od,id_,nt,seed", [
+    ("q4_K", 260, 512, 129, 21),
+    ("q6_K", 300, 768, 200, 22),
+    ("q4_K", 3584, 3584, 512, 23),
+    ("q6_K", 1000, 4096, 300, 24),
+    ("q4_K", 130, 22016, 70, 25),   # too many blocks per token to stash: two passes over X
+])
+def test_gemm_f32_matches_quantize_then_gemm(mmq, name, od, id_, nt, seed):
+    W = gen.weights(name, od, id_, seed=300 + seed)
+    X = gen.activations(nt, id_, seed=400 + seed, outlier_p=0.01, outlier_scale=20.0)
+    w = mmq.mmq_register_weights(name, torch.from_numpy(W).cuda(), od, id_)
+    Xd = torch.from_numpy(X).cuda()
+    Y2 = mmq.mmq_gemm(w, mmq.mmq_quantize_act(Xd), nt)
+    Y1 = mmq.mmq_gemm_f32(w, Xd)
+    torch.cuda.synchronize()
+    assert mmq.mmq_last_device_error() == 0
+    # the same q8_0 operands reach the same kernel: bit-identical outputs
+    assert torch.equal(Y1, Y2)
+    if od * id_ * nt <= 1e8:
+        err, bound = _within_tol(Y1.cpu().numpy(), oracle.gemm(QT[name], W, od, id_, oracle.quantize_q8_0(X), nt))
+        assert err <= bound, (err, bound)
+    w.release()
