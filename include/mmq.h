@@ -85,10 +85,15 @@ typedef struct mmq_weights_s *mmq_weights_t;
 
 /* ---- registration flags ------------------------------------------------ */
 #define MMQ_REG_WEXP 0x1u  /* also build the dense centered-int8 W_exp plane (q6_K) */
+#define MMQ_REG_RAW 0x2u   /* also keep the packed bytes, regrouped, for MMQ_ARM_RAW */
 
 /* ---- GEMM arms (flags of mmq_gemm select one; arm_used reports it) ----- */
 #define MMQ_ARM_AUTO 0     /* library choice */
 #define MMQ_ARM_F16 1      /* operands from the registered fp16 operand plane (TMA copy) */
+#define MMQ_ARM_RAW 2      /* packed weight bytes streamed and unpacked to fp16 in shared
+                              memory inside the GEMM ("47 · r44 — W_exp stride mismatch
+                              root cause", §3.2: the in-kernel recombination); needs a
+                              handle registered with MMQ_REG_RAW; bit-identical to F16 */
 
 /*
  * mmq_quantize_act -- q8_0 quantization of activations.

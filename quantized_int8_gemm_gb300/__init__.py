@@ -7,8 +7,10 @@ from .mmq import (  # noqa: F401
     ARM_NAMES,
     MMQ_ARM_AUTO,
     MMQ_ARM_F16,
+    MMQ_ARM_RAW,
     MMQ_Q4_K,
     MMQ_Q6_K,
+    MMQ_REG_RAW,
     MMQ_REG_WEXP,
     MMQError,
     Weights,

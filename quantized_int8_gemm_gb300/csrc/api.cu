@@ -88,8 +88,10 @@ int cuda_rc(cudaError_t e) {
 void free_planes(mmq_weights_s *h) {
   if (h->bplane) cudaFree(h->bplane);
   if (h->wexp) cudaFree(h->wexp);
+  if (h->rawplane) cudaFree(h->rawplane);
   h->bplane = nullptr;
   h->wexp = nullptr;
+  h->rawplane = nullptr;
 }
 
 }  // namespace
@@ -134,7 +136,7 @@ int mmq_register_weights(int type, const void *W, int64_t od, int64_t id, uint32
   if (type != MMQ_Q4_K && type != MMQ_Q6_K) return MMQ_ERR_TYPE;
   if (!W || od <= 0 || id <= 0 || id % MMQ_QK != 0) return MMQ_ERR_ARG;
   if (od > 0x7fffffffLL || id / MMQ_QK > 65535) return MMQ_ERR_ARG;
-  if (flags & ~MMQ_REG_WEXP) return MMQ_ERR_ARG;
+  if (flags & ~(MMQ_REG_WEXP | MMQ_REG_RAW)) return MMQ_ERR_ARG;
   if ((flags & MMQ_REG_WEXP) && type != MMQ_Q6_K) return MMQ_ERR_UNSUPPORTED;
   int dev;
   DeviceState *d;
@@ -153,11 +155,14 @@ int mmq_register_weights(int type, const void *W, int64_t od, int64_t id, uint32
   h->nb32 = id / 32;
   h->bplane_bytes = mmq::bplane_bytes(type, od, id);
   h->wexp_bytes = (flags & MMQ_REG_WEXP) ? static_cast<size_t>(od) * id : 0;
+  h->rawplane_bytes = (flags & MMQ_REG_RAW) ? mmq::rawplane_bytes(type, od, id) : 0;
 
   int rc = MMQ_OK;
   int *bad = nullptr;
   cudaError_t e = cudaMalloc(&h->bplane, h->bplane_bytes);
   if (e == cudaSuccess && h->wexp_bytes) e = cudaMalloc(&h->wexp, h->wexp_bytes);
+  if (e == cudaSuccess && h->rawplane_bytes)
+    e = cudaMalloc(reinterpret_cast<void **>(&h->rawplane), h->rawplane_bytes);
   if (e == cudaSuccess) e = cudaMalloc(&bad, sizeof(int));
   if (e == cudaSuccess) e = cudaMemsetAsync(bad, 0, sizeof(int), s);
   if (e == cudaSuccess) e = mmq::launch_register(h, static_cast<const uint8_t *>(W), bad, s);
@@ -214,8 +219,10 @@ static int gemm_impl(mmq_weights_t h, const void *Q, const float *X, int64_t nt,
                      mmq_stream_t stream, uint32_t flags, int *arm_used, cudaEvent_t ev0,
                      cudaEvent_t ev1) {
   if (!h || nt < 0 || nt > kMaxTokens) return MMQ_ERR_ARG;
-  if (flags != MMQ_ARM_AUTO && flags != MMQ_ARM_F16) return MMQ_ERR_UNSUPPORTED;
-  if (arm_used) *arm_used = MMQ_ARM_F16;
+  if (flags != MMQ_ARM_AUTO && flags != MMQ_ARM_F16 && flags != MMQ_ARM_RAW) return MMQ_ERR_UNSUPPORTED;
+  if (flags == MMQ_ARM_RAW && !h->rawplane) return MMQ_ERR_UNSUPPORTED;
+  const bool raw = flags == MMQ_ARM_RAW;
+  if (arm_used) *arm_used = raw ? MMQ_ARM_RAW : MMQ_ARM_F16;
   if (nt == 0) return MMQ_OK;
   const void *A = X ? static_cast<const void *>(X) : Q;
   if (!A || !Y) return MMQ_ERR_ARG;
@@ -232,15 +239,15 @@ static int gemm_impl(mmq_weights_t h, const void *Q, const float *X, int64_t nt,
   cudaError_t e = cudaStreamIsCapturing(s, &cap);
   if (e != cudaSuccess) return cuda_rc(e);
   const bool capturing = cap == cudaStreamCaptureStatusActive;
-  const size_t bytes = mmq::gemm_scratch_bytes(h, nt, true);
+  const size_t bytes = mmq::gemm_scratch_bytes(h, nt, true, raw);
   void *scratch = nullptr;
   e = capturing ? cudaMallocAsync(&scratch, bytes, s)
                 : cudaMallocFromPoolAsync(&scratch, bytes, d->pool, s);
   if (e != cudaSuccess) return cuda_rc(e);
   // inside a capture the events must become real record nodes of the graph
   const unsigned ev_flags = capturing ? cudaEventRecordExternal : cudaEventRecordDefault;
-  e = mmq::launch_gemm(h, static_cast<const uint8_t *>(Q), X, nt, Y, scratch, true, d->words,
-                       next_epoch(), g_limit_ns.load(), s, ev0, ev1, ev_flags);
+  e = mmq::launch_gemm(h, static_cast<const uint8_t *>(Q), X, nt, Y, scratch, true, raw,
+                       d->words, next_epoch(), g_limit_ns.load(), s, ev0, ev1, ev_flags);
   cudaError_t ef = cudaFreeAsync(scratch, s);
   if (e == cudaSuccess) e = ef;
   return cuda_rc(e);
@@ -290,12 +297,12 @@ int mmq_gemm_noalloc(mmq_weights_t h, const void *Q, int64_t nt, float *Y, mmq_s
     if (g_dev[dev].usable) d = &g_dev[dev];
   }
   if (!d) return MMQ_ERR_ARG;
-  if (mmq::gemm_scratch_bytes(h, nt, false) > mmq::kNoallocScratchBytes)
+  if (mmq::gemm_scratch_bytes(h, nt, false, false) > mmq::kNoallocScratchBytes)
     return MMQ_ERR_SCRATCH_LIMIT;
   void *scratch = nullptr;
   cudaError_t e = mmq::noalloc_scratch(dev, &scratch);
   if (e == cudaSuccess)
-    e = mmq::launch_gemm(h, static_cast<const uint8_t *>(Q), nullptr, nt, Y, scratch, false, d->words,
+    e = mmq::launch_gemm(h, static_cast<const uint8_t *>(Q), nullptr, nt, Y, scratch, false, false, d->words,
                          next_epoch(), g_limit_ns.load(), reinterpret_cast<cudaStream_t>(stream),
                          nullptr, nullptr, cudaEventRecordDefault);
   return cuda_rc(e);

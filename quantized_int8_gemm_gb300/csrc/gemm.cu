@@ -55,36 +55,139 @@ namespace {
 
 using namespace tiling;
 
-constexpr int STAGES = 3;
 constexpr int SLOTS = 4;          // TMEM chunk slots of kTileN columns (512 columns)
 constexpr int SRING = 4;          // per-super-block scale ring entries
+constexpr int RRING = 4;          // raw arm: raw weight block ring entries
 constexpr int EPI_WARPS = 8;      // warpgroups 0 and 1
 constexpr int PRODUCER_WARP = 8;  // warpgroup 2: producer, two UMMA issuers, one idle warp
 constexpr int ISSUER_WARP = 9;    // issuers 9 and 10; issuer i owns TMEM slots 2i and 2i+1
 constexpr int ISSUERS = 2;
-constexpr int THREADS = 384;
-// Register split: launched at 168 per thread (384 x 168 = 64512); warpgroup 2
-// drops to 56 and the epilogue warpgroups rise to 224: 2*128*224 + 128*56 =
-// 64512.
-constexpr int REGS_EPI = 224;
-constexpr int REGS_CTL = 56;
+constexpr int CONVERTER_WARP = 12;  // raw arm: warpgroup 3 unpacks the weight blocks
+constexpr int CONVERTERS = 4;
 constexpr int TMEM_COLS = SLOTS * kTileN;  // 512
 
-template <bool kQ4>
+// Launch shape of the two arms.  Register split: the CTA is launched at
+// kRegsLaunch per thread; warpgroup 2 (and the raw arm's converter
+// warpgroup 3) drop to kRegsCtl and the two epilogue warpgroups rise to
+// kRegsEpi, using the whole register file the launch holds.
+template <bool kRaw>
+struct Shape {
+  static constexpr int kStages = kRaw ? 2 : 3;
+  static constexpr int kThreads = kRaw ? 512 : 384;
+  static constexpr int kRegsLaunch = kRaw ? 128 : 168;
+  static constexpr int kRegsEpi = kRaw ? 208 : 224;
+  static constexpr int kRegsCtl = kRaw ? 48 : 56;
+  static_assert(kThreads * kRegsLaunch <= 65536, "register file");
+  static_assert(256 * kRegsEpi + (kThreads - 256) * kRegsCtl == kThreads * kRegsLaunch,
+                "the register split must add up to what the launch holds");
+};
+
+template <bool kQ4, bool kRaw>
 struct Smem {
+  using S = Shape<kRaw>;
   static constexpr int kA = a_odd_bytes(kQ4);                          // A region per stage
   static constexpr int kB = ((b_odd_bytes(kQ4) + 1023) / 1024) * 1024;  // B region per stage
   static constexpr int kStage = kA + kB;
+  static constexpr int kRaw_ = ((raw_block_bytes(kQ4) + 127) / 128) * 128;  // one raw ring entry
+  static constexpr int kRawRing = S::kStages * kStage;
   static constexpr int kScale = scale_block_bytes(kQ4);                // one scale ring entry
-  static constexpr int kScaleRing = STAGES * kStage;
+  static constexpr int kScaleRing = kRawRing + (kRaw ? RRING * kRaw_ : 0);
   static constexpr int kBar = kScaleRing + SRING * kScale;
-  static constexpr int kNumBars = 2 * STAGES + 2 * SLOTS + 2 * SRING + 1;
+  // full, empty, conv per stage; rfull, rempty per slot; sfull, sempty per
+  // scale entry; rawfull, rawempty per raw entry; done
+  static constexpr int kNumBars = 3 * S::kStages + 2 * SLOTS + 2 * SRING + 2 * RRING + 1;
   static constexpr int kSlot = kBar + kNumBars * 8;
   static constexpr int kUsed = kSlot + 16;
   static constexpr int kBytes = kUsed + 1024;  // slack for 1024-byte alignment
   static_assert(kA % 1024 == 0 && kStage % 1024 == 0, "stage buffers must keep 1 KB alignment");
   static_assert(kBytes <= 227 * 1024, "shared memory budget");
 };
+
+// ---------------------------------------------------------------- raw unpack
+// 4 values of 4-bit or 6-bit codes (one per byte of x) -> 2 x half2 of
+// 1024 + code (the 0x64 exponent byte above each code byte).
+__device__ __forceinline__ uint32_t bytes01_to_h2(uint32_t x) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(d) : "r"(x), "r"(0x64646464u));
+  return d;
+}
+__device__ __forceinline__ uint32_t bytes23_to_h2(uint32_t x) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, 0x7362;" : "=r"(d) : "r"(x), "r"(0x64646464u));
+  return d;
+}
+__device__ __forceinline__ uint32_t h2_fma(uint32_t a, __half2 b, __half2 c) {
+  const __half2 r = __hfma2(*reinterpret_cast<const __half2 *>(&a), b, c);
+  return *reinterpret_cast<const uint32_t *>(&r);
+}
+__device__ __forceinline__ uint32_t h2_sub(uint32_t a, __half2 b) {
+  const __half2 r = __hsub2(*reinterpret_cast<const __half2 *>(&a), b);
+  return *reinterpret_cast<const uint32_t *>(&r);
+}
+
+// One stage (half super-block, 128 rows x 128 K) of raw weight bytes ->
+// the fp16 operand image, byte-identical to the registered operand plane:
+// q4_K sc*q (as (1024+q)*sc - 1024*sc, one exact fp16 FMA), q6_K sc*(q-32)
+// (as ((1024+q) - 1056) * sc + 0, exact, +0 for zero).  Thread t of the
+// converter warpgroup handles row t.
+template <bool kQ4>
+__device__ __forceinline__ void unpack_stage(const uint8_t *__restrict__ raw, uint8_t *__restrict__ bop,
+                                             int r) {
+  if constexpr (kQ4) {
+    const uint2 *qs = reinterpret_cast<const uint2 *>(raw + kRawQ4Qs);
+    const __half *sc = reinterpret_cast<const __half *>(raw + kRawQ4Sc);
+    __half2 s2[4], n2[4];
+#pragma unroll
+    for (int sub = 0; sub < 4; ++sub) {
+      s2[sub] = __half2half2(sc[sub * 128 + r]);
+      n2[sub] = __hmul2(s2[sub], __float2half2_rn(-1024.0f));  // exact: 1024 * sc <= 64512
+    }
+#pragma unroll
+    for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint2 w = qs[(kb * 4 + j) * 128 + r];
+        const uint32_t l0 = w.x & 0x0F0F0F0Fu, l1 = w.y & 0x0F0F0F0Fu;
+        const uint32_t h0 = (w.x >> 4) & 0x0F0F0F0Fu, h1 = (w.y >> 4) & 0x0F0F0F0Fu;
+        const int sl = 2 * kb, sh = 2 * kb + 1;
+        const uint4 lo = make_uint4(h2_fma(bytes01_to_h2(l0), s2[sl], n2[sl]),
+                                    h2_fma(bytes23_to_h2(l0), s2[sl], n2[sl]),
+                                    h2_fma(bytes01_to_h2(l1), s2[sl], n2[sl]),
+                                    h2_fma(bytes23_to_h2(l1), s2[sl], n2[sl]));
+        const uint4 hi = make_uint4(h2_fma(bytes01_to_h2(h0), s2[sh], n2[sh]),
+                                    h2_fma(bytes23_to_h2(h0), s2[sh], n2[sh]),
+                                    h2_fma(bytes01_to_h2(h1), s2[sh], n2[sh]),
+                                    h2_fma(bytes23_to_h2(h1), s2[sh], n2[sh]));
+        *reinterpret_cast<uint4 *>(bop + operand_off(r, 64 * kb + 8 * j)) = lo;
+        *reinterpret_cast<uint4 *>(bop + operand_off(r, 64 * kb + 8 * (j + 4))) = hi;
+      }
+  } else {
+    const uint2 *ql = reinterpret_cast<const uint2 *>(raw + kRawQ6Ql);
+    const uint2 *qh = reinterpret_cast<const uint2 *>(raw + kRawQ6Qh);
+    const __half *sc = reinterpret_cast<const __half *>(raw + kRawQ6Sc);
+    const __half2 off2 = __float2half2_rn(1056.0f), zero2 = __float2half2_rn(0.0f);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint2 a = ql[j * 128 + r], b = ql[(j + 4) * 128 + r], h = qh[j * 128 + r];
+      // chunk (kb, jj): low bits from ql nibble kb, high bits from qh pair 2*kb + (jj >= 4)
+      auto chunk = [&](uint2 q, int nib, int pair, int kb, int jj) {
+        const uint32_t lo0 = (q.x >> (4 * nib)) & 0x0F0F0F0Fu, lo1 = (q.y >> (4 * nib)) & 0x0F0F0F0Fu;
+        const uint32_t v0 = lo0 | (((h.x >> (2 * pair)) & 0x03030303u) << 4);
+        const uint32_t v1 = lo1 | (((h.y >> (2 * pair)) & 0x03030303u) << 4);
+        const __half2 s2 = __half2half2(sc[(4 * kb + (jj >> 1)) * 128 + r]);
+        const uint4 o = make_uint4(h2_fma(h2_sub(bytes01_to_h2(v0), off2), s2, zero2),
+                                   h2_fma(h2_sub(bytes23_to_h2(v0), off2), s2, zero2),
+                                   h2_fma(h2_sub(bytes01_to_h2(v1), off2), s2, zero2),
+                                   h2_fma(h2_sub(bytes23_to_h2(v1), off2), s2, zero2));
+        *reinterpret_cast<uint4 *>(bop + operand_off(r, 64 * kb + 8 * jj)) = o;
+      };
+      chunk(a, 0, 0, 0, j);
+      chunk(b, 0, 1, 0, j + 4);
+      chunk(a, 1, 2, 1, j);
+      chunk(b, 1, 3, 1, j + 4);
+    }
+  }
+}
 
 // ---------------------------------------------------------------- small helpers
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
@@ -400,14 +503,17 @@ __device__ __forceinline__ bool work_next(Work &w, int n_tiles, int64_t nsb, int
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
-template <bool kQ4, bool kSK>
-__global__ void __launch_bounds__(THREADS, 1)
+template <bool kQ4, bool kSK, bool kRaw>
+__global__ void __launch_bounds__(Shape<kRaw>::kThreads, 1)
     mmq_gemm_kernel(const uint8_t *__restrict__ aplane, const uint8_t *__restrict__ bplane,
+                    const uint8_t *__restrict__ rawplane,
                     const uint8_t *__restrict__ bscale, const float *__restrict__ dap,
                     const float *__restrict__ invp, int64_t nt, int64_t od, int64_t nb32, int n_tt,
                     int n_ot, float *__restrict__ Y, WaitCtl wctl, float4 *__restrict__ ws,
                     uint64_t *__restrict__ flags) {
-  using L = Smem<kQ4>;
+  using L = Smem<kQ4, kRaw>;
+  using S = Shape<kRaw>;
+  constexpr int STAGES = S::kStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -424,10 +530,14 @@ __global__ void __launch_bounds__(THREADS, 1)
   auto rempty = [&](uint32_t i) { return bar + 8u * (2 * STAGES + SLOTS + i); };
   auto sfull = [&](int e) { return bar + 8u * (2 * STAGES + 2 * SLOTS + e); };
   auto sempty = [&](int e) { return bar + 8u * (2 * STAGES + 2 * SLOTS + SRING + e); };
-  const uint32_t done = bar + 8u * (2 * STAGES + 2 * SLOTS + 2 * SRING);
+  auto conv = [&](int s) { return bar + 8u * (2 * STAGES + 2 * SLOTS + 2 * SRING + s); };
+  auto rawfull = [&](int e) { return bar + 8u * (3 * STAGES + 2 * SLOTS + 2 * SRING + e); };
+  auto rawempty = [&](int e) { return bar + 8u * (3 * STAGES + 2 * SLOTS + 2 * SRING + RRING + e); };
+  const uint32_t done = bar + 8u * (3 * STAGES + 2 * SLOTS + 2 * SRING + 2 * RRING);
   auto a_smem = [&](int s) { return base + s * L::kStage; };
   auto b_smem = [&](int s) { return base + s * L::kStage + L::kA; };
   auto s_smem = [&](int e) { return base + L::kScaleRing + e * L::kScale; };
+  auto raw_smem = [&](int e) { return base + L::kRawRing + e * L::kRaw_; };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -442,6 +552,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(sfull(e), 1);
       mbar_init(sempty(e), EPI_WARPS);
     }
+    if (kRaw) {
+      for (int s = 0; s < STAGES; ++s) mbar_init(conv(s), CONVERTERS);
+      for (int e = 0; e < RRING; ++e) {
+        mbar_init(rawfull(e), 1);
+        mbar_init(rawempty(e), CONVERTERS);
+      }
+    }
     mbar_init(done, ISSUERS);
     fence_mbar_init();
   }
@@ -454,13 +571,13 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_after();
   const uint32_t tbase = *reinterpret_cast<volatile uint32_t *>(smem + L::kSlot);
   if (warp >= PRODUCER_WARP) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_CTL));
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(S::kRegsCtl));
   if (warp == PRODUCER_WARP) {
     // ------------------------------------------------------------ producer
     // The whole warp runs the loop (warp-uniform control flow); lane 0 copies
     // the activation block, lane 1 the weight block, lane 2 the super-block's
     // scale block into the scale ring.
-    uint32_t ks = 0, ns = 0, issued = 0, s_issued = 0;
+    uint32_t ks = 0, ns = 0, issued = 0, s_issued = 0, r_issued = 0;
     bool ok = true;
     Work wk = work_begin(kSK, static_cast<int64_t>(n_tiles) * nsb);
     int tile;
@@ -478,16 +595,32 @@ __global__ void __launch_bounds__(THREADS, 1)
         __syncwarp();
         s_issued = ns + 1;
         for (int half = 0; half < 2; ++half, ++ks) {
+          if (kRaw) {  // the raw weight block first: its ring runs ahead of the stages
+            const int re = static_cast<int>(ks % RRING);
+            ok = __all_sync(0xffffffffu, mbar_wait(rawempty(re), ((ks / RRING) & 1) ^ 1, wctl));
+            if (!ok) break;
+            if (lane == 3) {
+              mbar_arrive_expect_tx(rawfull(re), raw_block_bytes(kQ4));
+              bulk_load(raw_smem(re), rawplane + raw_block(ot, sb, half, nsb, kQ4), raw_block_bytes(kQ4),
+                        rawfull(re));
+            }
+            __syncwarp();
+            r_issued = ks + 1;
+          }
           const int s = static_cast<int>(ks % STAGES);
           ok = __all_sync(0xffffffffu, mbar_wait(empty(s), ((ks / STAGES) & 1) ^ 1, wctl));
           if (!ok) break;
           const uint32_t ab = half ? a_odd_bytes(kQ4) : a_even_bytes();
-          const uint32_t bb = half ? b_odd_bytes(kQ4) : b_even_bytes();
+          // raw arm: only the q4_K min image of the weight block is copied
+          const uint32_t bb = kRaw ? ((kQ4 && half) ? kMinBytes : 0) : (half ? b_odd_bytes(kQ4) : b_even_bytes());
           if (lane == 0) {
             mbar_arrive_expect_tx(full(s), ab + bb);
             bulk_load(a_smem(s), aplane + a_block(tt, sb, half, nsb, kQ4), ab, full(s));
-          } else if (lane == 1) {
-            bulk_load(b_smem(s), bplane + b_block(ot, sb, half, nsb, kQ4), bb, full(s));
+          } else if (lane == 1 && bb) {
+            if (kRaw)
+              bulk_load(b_smem(s) + kBMin, bplane + b_block(ot, sb, half, nsb, kQ4) + kBMin, bb, full(s));
+            else
+              bulk_load(b_smem(s), bplane + b_block(ot, sb, half, nsb, kQ4), bb, full(s));
           }
           __syncwarp();
           issued = ks + 1;
@@ -499,6 +632,37 @@ __global__ void __launch_bounds__(THREADS, 1)
         mbar_wait(full(k % STAGES), (k / STAGES) & 1, wctl, false);
       for (uint32_t k = s_issued > SRING ? s_issued - SRING : 0; k < s_issued; ++k)
         mbar_wait(sfull(k % SRING), (k / SRING) & 1, wctl, false);
+      for (uint32_t k = r_issued > RRING ? r_issued - RRING : 0; k < r_issued; ++k)
+        mbar_wait(rawfull(k % RRING), (k / RRING) & 1, wctl, false);
+    }
+  } else if (kRaw && warp >= CONVERTER_WARP) {
+    // ------------------------------------------------------------ converters
+    // Raw arm: per stage, unpack the raw weight block into the stage's fp16
+    // operand image once both the block has landed and the stage is free.
+    const int r = threadIdx.x - CONVERTER_WARP * 32;  // row of the weight tile
+    uint32_t ks = 0;
+    bool ok = true;
+    Work wk = work_begin(kSK, static_cast<int64_t>(n_tiles) * nsb);
+    int tile;
+    int64_t sb0, sb1;
+    while (ok && work_next(wk, n_tiles, nsb, tile, sb0, sb1)) {
+      for (int64_t sb = sb0; sb < sb1 && ok; ++sb) {
+        for (int half = 0; half < 2 && ok; ++half, ++ks) {
+          const int re = static_cast<int>(ks % RRING), s = static_cast<int>(ks % STAGES);
+          ok = __all_sync(0xffffffffu, mbar_wait(rawfull(re), (ks / RRING) & 1, wctl));
+          if (ok) ok = __all_sync(0xffffffffu, mbar_wait(empty(s), ((ks / STAGES) & 1) ^ 1, wctl));
+          if (!ok) break;
+          unpack_stage<kQ4>(smem + (raw_smem(re) - base), smem + (b_smem(s) - base), r);
+          // generic-proxy writes of the operand image, read next by the
+          // tensor core (async proxy); the raw block was read the same way
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(conv(s));
+            mbar_arrive(rawempty(re));
+          }
+        }
+      }
     }
   } else if (warp < ISSUER_WARP + ISSUERS) {
     // ------------------------------------------------------------ UMMA issuers
@@ -543,6 +707,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int half = 0; half < 2 && ok; ++half, ++ks) {
           const int s = static_cast<int>(ks % STAGES);
           ok = __all_sync(0xffffffffu, mbar_wait(full(s), (ks / STAGES) & 1, wctl));
+          if (ok && kRaw) ok = __all_sync(0xffffffffu, mbar_wait(conv(s), (ks / STAGES) & 1, wctl));
           if (!ok) break;
           tc_fence_after();
           const uint64_t as = a0 + s * kStageDesc, bs = b0 + s * kStageDesc;
@@ -565,7 +730,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_wait(done, 0, wctl, false);
   }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS_EPI));
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(S::kRegsEpi));
     // ------------------------------------------------------------ epilogue
     // Software-pipelined over 32-column halves: while the packed FMAs of one
     // half run, the TMEM load of the next half and the barrier test of the
@@ -857,14 +1022,46 @@ GemmPlan plan_gemm(const mmq_weights_s *h, int64_t nt, bool streamk_allowed) {
 
 }  // namespace
 
-size_t gemm_scratch_bytes(const mmq_weights_s *h, int64_t nt, bool streamk_allowed) {
+size_t gemm_scratch_bytes(const mmq_weights_s *h, int64_t nt, bool streamk_allowed, bool raw) {
+  (void)raw;  // both arms use the same scratch
   return plan_gemm(h, nt, streamk_allowed).bytes;
 }
 
+namespace {
+
+// One GEMM kernel variant: its function, launch shape and a one-time check,
+// per device, of the shared-memory opt-in and of the register count the
+// register split was planned for (a mismatch would stall setmaxnreg).
+template <bool kQ4, bool kSK, bool kRaw>
+cudaError_t launch_variant(int dev, int grid, cudaStream_t s, const uint8_t *aplane, const uint8_t *bplane,
+                           const uint8_t *rawplane, const uint8_t *bscale, const float *dap,
+                           const float *invp, int64_t nt, int64_t od, int64_t nb32, int n_tt, int n_ot,
+                           float *Y, WaitCtl w, float4 *ws, uint64_t *flags) {
+  auto kern = mmq_gemm_kernel<kQ4, kSK, kRaw>;
+  constexpr int smem = Smem<kQ4, kRaw>::kBytes;
+  static std::atomic<int> ready[64];  // 0 unknown, 1 ready, 2 unusable
+  int st = ready[dev].load();
+  if (st == 0) {
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    st = fa.numRegs == Shape<kRaw>::kRegsLaunch ? 1 : 2;
+    ready[dev].store(st);
+  }
+  if (st != 1) return cudaErrorInvalidKernelImage;
+  kern<<<grid, Shape<kRaw>::kThreads, smem, s>>>(aplane, bplane, rawplane, bscale, dap, invp, nt, od, nb32,
+                                                 n_tt, n_ot, Y, w, ws, flags);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
 cudaError_t launch_gemm(const mmq_weights_s *h, const uint8_t *Q, const float *X, int64_t nt,
-                        float *Y, void *scratch, bool streamk_allowed, DevStatus *st,
+                        float *Y, void *scratch, bool streamk_allowed, bool raw, DevStatus *st,
                         unsigned epoch, uint64_t limit_ns, cudaStream_t s, cudaEvent_t ev0,
                         cudaEvent_t ev1, unsigned ev_flags) {
+  if (raw && !h->rawplane) return cudaErrorInvalidValue;
   const GemmPlan p = plan_gemm(h, nt, streamk_allowed);
   const bool q4 = p.q4;
   const int64_t n_tt = p.n_tt, nt_pad = p.nt_pad, nsb = p.nsb, nb32 = p.nb32;
@@ -905,25 +1102,25 @@ cudaError_t launch_gemm(const mmq_weights_s *h, const uint8_t *Q, const float *X
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
-  auto kern = q4 ? (p.streamk ? mmq_gemm_kernel<true, true> : mmq_gemm_kernel<true, false>)
-                 : (p.streamk ? mmq_gemm_kernel<false, true> : mmq_gemm_kernel<false, false>);
-  const int smem = q4 ? Smem<true>::kBytes : Smem<false>::kBytes;
-  // the shared-memory opt-in is set once per device, outside any stream
-  // capture the first call is not part of
-  static std::atomic<uint32_t> attr_done[64][4];
   const int dev = h->device;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  const int variant = (q4 ? 2 : 0) + (p.streamk ? 1 : 0);
-  if (!attr_done[dev][variant].load()) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr_done[dev][variant].store(1);
-  }
   WaitCtl w{&st->status, &st->abort_epoch, epoch, limit_ns};
   if (ev0 && (e = cudaEventRecordWithFlags(ev0, s, ev_flags)) != cudaSuccess) return e;
   const uint8_t *bp = static_cast<const uint8_t *>(h->bplane);
-  kern<<<p.grid, THREADS, smem, s>>>(aplane, bp, bp + b_scale_region(p.n_ot, nsb, q4), dap, invp, nt,
-                                     h->od, nb32, static_cast<int>(n_tt), p.n_ot, Y, w, ws, flags);
+  const uint8_t *bs = bp + b_scale_region(p.n_ot, nsb, q4);
+  const uint8_t *rp = h->rawplane;
+  const int nti = static_cast<int>(n_tt);
+#define MMQ_LAUNCH(Q4, SK, RAW)                                                                 \
+  launch_variant<Q4, SK, RAW>(dev, p.grid, s, aplane, bp, rp, bs, dap, invp, nt, h->od, nb32, nti, \
+                              p.n_ot, Y, w, ws, flags)
+  if (q4)
+    e = p.streamk ? (raw ? MMQ_LAUNCH(true, true, true) : MMQ_LAUNCH(true, true, false))
+                  : (raw ? MMQ_LAUNCH(true, false, true) : MMQ_LAUNCH(true, false, false));
+  else
+    e = p.streamk ? (raw ? MMQ_LAUNCH(false, true, true) : MMQ_LAUNCH(false, true, false))
+                  : (raw ? MMQ_LAUNCH(false, false, true) : MMQ_LAUNCH(false, false, false));
+#undef MMQ_LAUNCH
+  if (e != cudaSuccess) return e;
   e = cudaGetLastError();
   if (e == cudaSuccess && ev1) e = cudaEventRecordWithFlags(ev1, s, ev_flags);
   return e;

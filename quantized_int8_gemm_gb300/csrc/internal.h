@@ -14,6 +14,8 @@
 //           scale region (d and, for q4_K, dmin rows).  Rows od..od_pad-1
 //           are zero.
 //   wexp    optional dense centered q6_K plane, int8 [od][id], q - 32
+//   rawplane  optional packed bytes of W regrouped per tile (tiling.h), read
+//           by the GEMM's raw arm
 struct mmq_weights_s {
   int type = 0;
   int device = 0;
@@ -21,7 +23,8 @@ struct mmq_weights_s {
   int64_t od = 0, id = 0, od_pad = 0, nsb = 0, nb32 = 0;
   void *bplane = nullptr;
   int8_t *wexp = nullptr;
-  size_t bplane_bytes = 0, wexp_bytes = 0;
+  uint8_t *rawplane = nullptr;  // MMQ_REG_RAW: packed bytes regrouped for the raw arm
+  size_t bplane_bytes = 0, wexp_bytes = 0, rawplane_bytes = 0;
 };
 
 namespace mmq {
@@ -43,6 +46,7 @@ cudaError_t launch_quantize_q8_0(const float *X, int64_t nt, int64_t id, uint8_t
 // *bad_scale (device int) becomes nonzero if a q6_K sub-block scale |sc| > 64.
 size_t bplane_bytes(int type, int64_t od, int64_t id);
 size_t bplane_operand_bytes(int type, int64_t od, int64_t id);  // without the scale region
+size_t rawplane_bytes(int type, int64_t od, int64_t id);
 cudaError_t launch_register(const mmq_weights_s *h, const uint8_t *W, int *bad_scale,
                             cudaStream_t s);
 
@@ -51,11 +55,10 @@ cudaError_t launch_register(const mmq_weights_s *h, const uint8_t *W, int *bad_s
 // between CTAs (and then needs more scratch).  ev0/ev1 (optional) are
 // recorded around the GEMM kernel with cudaEventRecordWithFlags(ev, s,
 // ev_flags).
-size_t gemm_scratch_bytes(const mmq_weights_s *h, int64_t nt, bool streamk_allowed);
-// The activations come either as pad40 blocks Q or, when X is non-null, as
-// fp32 rows quantized on the fly (Q is then ignored).
+// raw: stream the handle's raw plane and unpack it in the kernel.
+size_t gemm_scratch_bytes(const mmq_weights_s *h, int64_t nt, bool streamk_allowed, bool raw);
 cudaError_t launch_gemm(const mmq_weights_s *h, const uint8_t *Q, const float *X, int64_t nt,
-                        float *Y, void *scratch, bool streamk_allowed, DevStatus *st,
+                        float *Y, void *scratch, bool streamk_allowed, bool raw, DevStatus *st,
                         unsigned epoch, uint64_t limit_ns, cudaStream_t s, cudaEvent_t ev0,
                         cudaEvent_t ev1, unsigned ev_flags);
 

@@ -110,7 +110,66 @@ __global__ void __launch_bounds__(256) register_kernel(const uint8_t *__restrict
   if (e == 0) scl[r] = d;
 }
 
+// Raw plane (tiling.h): the packed bytes of row o, super-block sb regrouped
+// for the GEMM's in-kernel unpack; scales as fp16.  One CTA per block.
+template <bool kQ4>
+__global__ void __launch_bounds__(64) register_raw_kernel(const uint8_t *__restrict__ W, int64_t id,
+                                                          uint8_t *__restrict__ raw) {
+  constexpr int kBytes = kQ4 ? MMQ_Q4K_BLOCK_BYTES : MMQ_Q6K_BLOCK_BYTES;
+  __shared__ __align__(8) uint8_t blk[kBytes + 6];
+  const int64_t nsb = id / MMQ_QK;
+  const int64_t o = blockIdx.x, sb = blockIdx.y;
+  const int tid = threadIdx.x;
+  for (int i = tid; i < kBytes; i += 64) blk[i] = W[(o * nsb + sb) * kBytes + i];
+  __syncthreads();
+  const int64_t ot = o / kTileN;
+  const int r = static_cast<int>(o % kTileN);
+  auto word8 = [&](int off) {  // 8 bytes at byte offset off of the packed block
+    uint64_t v = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v |= static_cast<uint64_t>(blk[off + i]) << (8 * i);
+    return v;
+  };
+  if constexpr (kQ4) {
+    // per half: 8 qs words and 4 scales
+    if (tid < 16) {
+      const int half = tid >> 3, g = tid & 7, kb = g >> 2, j = g & 3;
+      uint8_t *dst = raw + raw_block(ot, sb, half, nsb, true);
+      reinterpret_cast<uint64_t *>(dst + kRawQ4Qs)[g * 128 + r] =
+          word8(MMQ_Q4K_QS_OFF + 64 * half + 32 * kb + 8 * j);
+    } else if (tid < 24) {
+      const int half = (tid - 16) >> 2, sub = (tid - 16) & 3;
+      int sc, m;
+      q4k_scale_min(blk + MMQ_Q4K_SC_OFF, 4 * half + sub, sc, m);
+      uint8_t *dst = raw + raw_block(ot, sb, half, nsb, true);
+      reinterpret_cast<__half *>(dst + kRawQ4Sc)[sub * 128 + r] = __int2half_rn(sc);
+    }
+  } else {
+    // per half: 8 ql words, 4 qh words and 8 scales
+    if (tid < 16) {
+      const int half = tid >> 3, j = tid & 7;
+      uint8_t *dst = raw + raw_block(ot, sb, half, nsb, false);
+      reinterpret_cast<uint64_t *>(dst + kRawQ6Ql)[j * 128 + r] = word8(MMQ_Q6K_QL_OFF + 64 * half + 8 * j);
+    } else if (tid < 24) {
+      const int half = (tid - 16) >> 2, j = (tid - 16) & 3;
+      uint8_t *dst = raw + raw_block(ot, sb, half, nsb, false);
+      reinterpret_cast<uint64_t *>(dst + kRawQ6Qh)[j * 128 + r] = word8(MMQ_Q6K_QH_OFF + 32 * half + 8 * j);
+    } else if (tid < 40) {
+      const int half = (tid - 24) >> 3, sub = (tid - 24) & 7;
+      const int sc = static_cast<int8_t>(blk[MMQ_Q6K_SC_OFF + 8 * half + sub]);
+      uint8_t *dst = raw + raw_block(ot, sb, half, nsb, false);
+      reinterpret_cast<__half *>(dst + kRawQ6Sc)[sub * 128 + r] = __int2half_rn(sc);
+    }
+  }
+}
+
 }  // namespace
+
+size_t rawplane_bytes(int type, int64_t od, int64_t id) {
+  const bool q4 = type == MMQ_Q4_K;
+  const int64_t n_ot = (od + kTileN - 1) / kTileN;
+  return static_cast<size_t>(n_ot * (id / MMQ_QK) * 2) * raw_block_bytes(q4);
+}
 
 size_t bplane_bytes(int type, int64_t od, int64_t id) {
   const bool q4 = type == MMQ_Q4_K;
@@ -132,6 +191,14 @@ cudaError_t launch_register(const mmq_weights_s *h, const uint8_t *W, int *bad_s
   uint8_t *bp = static_cast<uint8_t *>(h->bplane);
   const bool q4 = h->type == MMQ_Q4_K;
   const uint64_t sr = b_scale_region(h->od_pad / kTileN, h->nsb, q4);
+  if (h->rawplane) {
+    e = cudaMemsetAsync(h->rawplane, 0, h->rawplane_bytes, s);
+    if (e != cudaSuccess) return e;
+    if (q4)
+      register_raw_kernel<true><<<grid, 64, 0, s>>>(W, h->id, h->rawplane);
+    else
+      register_raw_kernel<false><<<grid, 64, 0, s>>>(W, h->id, h->rawplane);
+  }
   if (q4) {
     register_kernel<true, false><<<grid, 256, 0, s>>>(W, nullptr, h->id, bp, sr, bad_scale);
   } else if (h->wexp) {

@@ -84,5 +84,29 @@ __host__ __device__ constexpr uint64_t b_scale_block(int64_t tile, int64_t sb, i
   return static_cast<uint64_t>((tile * nsb + sb) * scale_block_bytes(q4));
 }
 
+// ---------------------------------------------------------------- raw plane
+// The raw arm streams the packed weight bytes and unpacks them in the GEMM.
+// Per (weight tile, super-block, half) one raw block holds the bytes of that
+// half of the 128 rows' k-quant blocks, regrouped so that a converter thread
+// (one row) and its neighbours (the next rows) read consecutive 8-byte words:
+//   q4_K: qs   [g = kb*4 + j][row] 8 B: qs bytes 32*kb + 8*j .. +7 of the half
+//                (low nibbles: k = 64*kb + 8*j .., high nibbles: k + 32 ..)
+//         sc   [sub 0..3][row] fp16: the 6-bit scale of sub-block 4*half+sub
+//   q6_K: ql   [j 0..7][row] 8 B: ql bytes 8*j .. +7 of the half
+//                (low nibbles: k = 8*j .., high nibbles: k = 64 + 8*j ..)
+//         qh   [j 0..3][row] 8 B: qh bytes 8*j .. +7 of the half
+//                (bit pair 2*p is k = 32*p + 8*j ..)
+//         sc   [sub 0..7][row] fp16: the int8 scale of 16-element sub-block
+//                8*half + sub
+// where the half's bytes are q4_K qs[64*half ..], q6_K ql[64*half ..] and
+// qh[32*half ..].  The scale region (d, dmin) and, for q4_K, the B min
+// images are read from the operand plane, which the raw arm otherwise skips.
+constexpr int kRawQ4Qs = 0, kRawQ4Sc = 8192, kRawQ4Bytes = 8192 + 1024;
+constexpr int kRawQ6Ql = 0, kRawQ6Qh = 8192, kRawQ6Sc = 8192 + 4096, kRawQ6Bytes = 8192 + 4096 + 2048;
+__host__ __device__ constexpr int raw_block_bytes(bool q4) { return q4 ? kRawQ4Bytes : kRawQ6Bytes; }
+__host__ __device__ constexpr uint64_t raw_block(int64_t tile, int64_t sb, int half, int64_t nsb, bool q4) {
+  return static_cast<uint64_t>(((tile * nsb + sb) * 2 + half) * raw_block_bytes(q4));
+}
+
 }  // namespace tiling
 }  // namespace mmq

@@ -32,9 +32,11 @@ MMQ_Q6_K = 14
 QTYPES = {"q4_K": MMQ_Q4_K, "q6_K": MMQ_Q6_K}
 
 MMQ_REG_WEXP = 0x1
+MMQ_REG_RAW = 0x2
 MMQ_ARM_AUTO = 0
 MMQ_ARM_F16 = 1
-ARM_NAMES = {MMQ_ARM_F16: "f16_plane"}
+MMQ_ARM_RAW = 2
+ARM_NAMES = {MMQ_ARM_F16: "f16_plane", MMQ_ARM_RAW: "raw_unpack"}
 
 Q8_BLOCK_BYTES = 40
 BLOCK_BYTES = {MMQ_Q4_K: 144, MMQ_Q6_K: 210}

@@ -273,3 +273,49 @@ def test_gemm_f32_matches_quantize_then_gemm(mmq, name, od, id_, nt, seed):
         err, bound = _within_tol(Y1.cpu().numpy(), oracle.gemm(QT[name], W, od, id_, oracle.quantize_q8_0(X), nt))
         assert err <= bound, (err, bound)
     w.release()
+
+
+# --------------------------------------------------------------------------
+# raw arm: packed weight bytes unpacked inside the GEMM
+RAW_SHAPES = [
+    ("q6_K", 256, 512, 16, 31),
+    ("q4_K", 260, 512, 129, 32),
+    ("q6_K", 300, 768, 200, 33),
+    ("q4_K", 131, 256, 1, 34),
+    ("q6_K", 1000, 4096, 300, 35),   # stream-K split tiles
+    ("q4_K", 3584, 3584, 512, 36),   # the q-proj workload
+    ("q6_K", 3584, 18944, 300, 37),  # many super-blocks, whole tiles
+]
+
+
+@pytest.mark.parametrize("name,od,id_,nt,seed", RAW_SHAPES)
+def test_raw_arm_bit_identical_to_operand_plane(mmq, name, od, id_, nt, seed):
+    W = gen.weights(name, od, id_, seed=500 + seed)
+    X = gen.activations(nt, id_, seed=600 + seed, outlier_p=0.01, outlier_scale=20.0)
+    w = mmq.mmq_register_weights(name, torch.from_numpy(W).cuda(), od, id_, mmq.MMQ_REG_RAW)
+    Q = mmq.mmq_quantize_act(torch.from_numpy(X).cuda())
+    Y16, a16 = mmq.mmq_gemm(w, Q, nt, flags=mmq.MMQ_ARM_F16, return_arm=True)
+    Yraw, araw = mmq.mmq_gemm(w, Q, nt, flags=mmq.MMQ_ARM_RAW, return_arm=True)
+    torch.cuda.synchronize()
+    assert mmq.mmq_last_device_error() == 0
+    assert (a16, araw) == (mmq.MMQ_ARM_F16, mmq.MMQ_ARM_RAW)
+    # the unpacked operand images equal the registered ones: same results
+    assert torch.equal(Y16, Yraw)
+    if od * id_ * nt <= 1e8:
+        err, bound = _within_tol(Yraw.cpu().numpy(),
+                                 oracle.gemm(QT[name], W, od, id_, oracle.quantize_q8_0(X), nt))
+        assert err <= bound, (err, bound)
+    w.release()
+
+
+def test_raw_arm_argument_errors(mmq):
+    W = gen.weights("q6_K", 128, 256, seed=7)
+    w = mmq.mmq_register_weights("q6_K", torch.from_numpy(W).cuda(), 128, 256)
+    Q = mmq.mmq_quantize_act(torch.randn(4, 256, device="cuda"))
+    with pytest.raises(mmq.MMQError) as ei:
+        mmq.mmq_gemm(w, Q, 4, flags=mmq.MMQ_ARM_RAW)  # handle has no raw plane
+    assert ei.value.code == -7
+    with pytest.raises(mmq.MMQError) as ei:
+        mmq.mmq_gemm(w, Q, 4, flags=7)  # no such arm
+    assert ei.value.code == -7
+    w.release()
