@@ -84,7 +84,7 @@ typedef struct mmq_weights_s *mmq_weights_t;
 #define MMQ_QK 256
 
 /* ---- registration flags ------------------------------------------------ */
-#define MMQ_REG_WEXP 0x1u  /* also build the dense centered-int8 W_exp plane (q6_K) */
+#define MMQ_REG_WEXP 0x1u  /* also build the dense int8 W_exp code plane */
 #define MMQ_REG_RAW 0x2u   /* also keep the packed bytes, regrouped, for MMQ_ARM_RAW */
 
 /* ---- GEMM arms (flags of mmq_gemm select one; arm_used reports it) ----- */
@@ -121,8 +121,12 @@ int mmq_quantize_act(const float *X, int64_t nt, int64_t id, void *Q, mmq_stream
  *         row pitch (id/256)*block bytes, no alignment requirement.  Read
  *         only during this call; the caller keeps ownership.
  *   od    output rows (> 0).   id  K, a positive multiple of 256.
- *   flags MMQ_REG_WEXP: also keep the dense centered-int8 W_exp plane
- *         (od*id bytes, q6_K only).
+ *   flags MMQ_REG_WEXP: also keep the dense int8 W_exp code plane (od*id
+ *         bytes): q6_K the centered code q - 32, q4_K the code q (the same
+ *         plane carried to q4_K); the operand plane is then built by reading
+ *         W_exp back with its dense strides.
+ *         MMQ_REG_RAW: also keep the packed bytes regrouped for MMQ_ARM_RAW
+ *         (od_pad*id*0.56 B q4_K, *0.88 B q6_K).
  *   out   receives a handle owning the internal planes (fp16 operand plane
  *         with sub-block scales folded in, fp32 scale planes, optional
  *         W_exp) until mmq_release_weights.
@@ -140,13 +144,33 @@ int mmq_register_weights(int type, const void *W, int64_t od, int64_t id, uint32
 int mmq_release_weights(mmq_weights_t h);
 
 /*
- * mmq_weights_wexp -- the dense centered-int8 W_exp plane of a q6_K handle
- * registered with MMQ_REG_WEXP ("46 · r43 — PC-sampling attribution", §3.2):
+ * mmq_weights_wexp -- the dense int8 W_exp plane of a handle registered with
+ * MMQ_REG_WEXP ("46 · r43 — PC-sampling attribution", §3.2; q6_K q - 32, q4_K q):
  * element (o, k) at plane[o*row_pitch + k], row_pitch == id, super-block
  * pitch 256.  The pointer is device memory owned by the handle.
  * Errors: MMQ_ERR_ARG (null argument), MMQ_ERR_UNSUPPORTED (no plane).
  */
 int mmq_weights_wexp(mmq_weights_t h, const int8_t **plane, int64_t *row_pitch);
+
+/*
+ * mmq_dequantize_weights -- the dequantization fallback: packed k-quant rows
+ * to a dense od x id plane of real weights, for consumers that do not run
+ * the MMQ contraction ("47 · r44 — W_exp stride mismatch root cause", §2.2:
+ * the dequant/embedding paths read the raw blocks).  Each weight
+ * (q6_K d*sc*(q-32), q4_K d*sc*q - dmin*m) is formed exactly in fp64 and
+ * rounded once, to nearest even, to the output type.
+ *   type   MMQ_Q6_K or MMQ_Q4_K.   W  device, packed rows as for
+ *          mmq_register_weights.   od, id  as there.
+ *   out    device, od*id elements of out_type, row-major (row pitch id),
+ *          16-byte aligned.
+ *   out_type MMQ_OUT_F16 or MMQ_OUT_F32.
+ * Errors: MMQ_ERR_ARG, MMQ_ERR_ALIGN, MMQ_ERR_TYPE, MMQ_ERR_NO_DEVICE,
+ * MMQ_ERR_CUDA.
+ */
+#define MMQ_OUT_F16 1
+#define MMQ_OUT_F32 2
+int mmq_dequantize_weights(int type, const void *W, int64_t od, int64_t id, void *out,
+                           int out_type, mmq_stream_t stream);
 
 /* Sizes of a handle's device planes, in bytes (the VRAM side of the
  * registration trade-off, "47 · r44 — W_exp stride mismatch root cause",

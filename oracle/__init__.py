@@ -14,6 +14,7 @@ from .oracle import (  # noqa: F401
     build,
     dequant_act,
     dequant_weights,
+    expand_q4k_dense,
     expand_q6k_dense,
     f16_to_f64,
     f32_to_f16,

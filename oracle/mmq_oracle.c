@@ -228,6 +228,21 @@ int mmq_oracle_q4k_quant(const uint8_t *blk, int e) {
     return (j % 2 == 0) ? (b & 0xF) : (b >> 4);
 }
 
+/* Dense q4_K code plane (the W_exp idea carried to q4_K): element (j, k) of
+ * the od x id plane is the 4-bit code q of weight (j, k), row pitch id,
+ * super-block pitch 256, as for the q6_K plane. */
+int mmq_oracle_expand_q4k_dense(const uint8_t *W, int64_t od, int64_t id, int8_t *out) {
+    if (od < 0 || id <= 0 || id % 256 != 0) return -1;
+    int64_t nsb = id / 256;
+    for (int64_t j = 0; j < od; ++j)
+        for (int64_t sb = 0; sb < nsb; ++sb) {
+            const uint8_t *blk = W + (j * nsb + sb) * OR_Q4_BYTES;
+            for (int e = 0; e < 256; ++e)
+                out[j * id + sb * 256 + e] = (int8_t)mmq_oracle_q4k_quant(blk, e);
+        }
+    return 0;
+}
+
 static double q4k_weight(const uint8_t *blk, int e) {
     int sc, m;
     mmq_oracle_q4k_scale_min(blk, e / 32, &sc, &m);

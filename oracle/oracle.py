@@ -66,6 +66,8 @@ def lib() -> ctypes.CDLL:
             L.mmq_oracle_dequant_weights.restype = ctypes.c_int
             L.mmq_oracle_expand_q6k_dense.argtypes = [_ptr, _i64, _i64, _ptr]
             L.mmq_oracle_expand_q6k_dense.restype = ctypes.c_int
+            L.mmq_oracle_expand_q4k_dense.argtypes = [_ptr, _i64, _i64, _ptr]
+            L.mmq_oracle_expand_q4k_dense.restype = ctypes.c_int
             for fn in (L.mmq_oracle_gemm_entries, L.mmq_oracle_gemm_entries_int):
                 fn.argtypes = [ctypes.c_int, _ptr, _i64, _i64, _ptr, _i64, _ptr, _ptr,
                                _i64, _ptr]
@@ -163,6 +165,16 @@ def expand_q6k_dense(W: np.ndarray, od: int, id_: int) -> np.ndarray:
     rc = lib().mmq_oracle_expand_q6k_dense(_p(W), od, id_, _p(out))
     if rc != 0:
         raise ValueError(f"oracle expand_q6k_dense failed rc={rc}")
+    return out
+
+
+def expand_q4k_dense(W: np.ndarray, od: int, id_: int) -> np.ndarray:
+    W = np.ascontiguousarray(W, dtype=np.uint8)
+    assert W.size == od * (id_ // 256) * 144
+    out = np.empty((od, id_), dtype=np.int8)
+    rc = lib().mmq_oracle_expand_q4k_dense(_p(W), od, id_, _p(out))
+    if rc != 0:
+        raise ValueError(f"oracle expand_q4k_dense failed rc={rc}")
     return out
 
 

@@ -8,6 +8,8 @@ from .mmq import (  # noqa: F401
     MMQ_ARM_AUTO,
     MMQ_ARM_F16,
     MMQ_ARM_RAW,
+    MMQ_OUT_F16,
+    MMQ_OUT_F32,
     MMQ_Q4_K,
     MMQ_Q6_K,
     MMQ_REG_RAW,
@@ -15,6 +17,7 @@ from .mmq import (  # noqa: F401
     MMQError,
     Weights,
     load,
+    mmq_dequantize_weights,
     mmq_gemm,
     mmq_gemm_f32,
     mmq_gemm_f32_profiled,

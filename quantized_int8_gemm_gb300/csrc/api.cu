@@ -137,7 +137,6 @@ int mmq_register_weights(int type, const void *W, int64_t od, int64_t id, uint32
   if (!W || od <= 0 || id <= 0 || id % MMQ_QK != 0) return MMQ_ERR_ARG;
   if (od > 0x7fffffffLL || id / MMQ_QK > 65535) return MMQ_ERR_ARG;
   if (flags & ~(MMQ_REG_WEXP | MMQ_REG_RAW)) return MMQ_ERR_ARG;
-  if ((flags & MMQ_REG_WEXP) && type != MMQ_Q6_K) return MMQ_ERR_UNSUPPORTED;
   int dev;
   DeviceState *d;
   if (int rc = device_state(&dev, &d)) return rc;
@@ -179,6 +178,20 @@ int mmq_register_weights(int type, const void *W, int64_t od, int64_t id, uint32
   }
   *out = h;
   return MMQ_OK;
+}
+
+int mmq_dequantize_weights(int type, const void *W, int64_t od, int64_t id, void *out,
+                           int out_type, mmq_stream_t stream) {
+  if (type != MMQ_Q4_K && type != MMQ_Q6_K) return MMQ_ERR_TYPE;
+  if (!W || !out || od <= 0 || id <= 0 || id % MMQ_QK != 0) return MMQ_ERR_ARG;
+  if (od > 0x7fffffffLL || id / MMQ_QK > 65535) return MMQ_ERR_ARG;
+  if (out_type != MMQ_OUT_F16 && out_type != MMQ_OUT_F32) return MMQ_ERR_ARG;
+  if (!aligned16(out)) return MMQ_ERR_ALIGN;
+  int dev;
+  DeviceState *d;
+  if (int rc = device_state(&dev, &d)) return rc;
+  return cuda_rc(mmq::launch_dequant(type, static_cast<const uint8_t *>(W), od, id, out, out_type,
+                                     reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int mmq_release_weights(mmq_weights_t h) {

@@ -47,6 +47,8 @@ cudaError_t launch_quantize_q8_0(const float *X, int64_t nt, int64_t id, uint8_t
 size_t bplane_bytes(int type, int64_t od, int64_t id);
 size_t bplane_operand_bytes(int type, int64_t od, int64_t id);  // without the scale region
 size_t rawplane_bytes(int type, int64_t od, int64_t id);
+cudaError_t launch_dequant(int type, const uint8_t *W, int64_t od, int64_t id, void *out,
+                           int out_type, cudaStream_t s);
 cudaError_t launch_register(const mmq_weights_s *h, const uint8_t *W, int *bad_scale,
                             cudaStream_t s);
 

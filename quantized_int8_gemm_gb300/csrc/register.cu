@@ -51,16 +51,26 @@ __device__ __forceinline__ float f16_at(const uint8_t *p) {
   return __half2float(__ushort_as_half(static_cast<unsigned short>(p[0] | (p[1] << 8))));
 }
 
-// dense W_exp plane, element (o, sb*256 + e) at o*id + sb*256 + e
+// q4_K element e: nibble (e/32)%2 of qs[32*(e/64) + e%32].
+__device__ __forceinline__ int q4k_code(const uint8_t *blk, int e) {
+  const int j = e >> 5;
+  const int byte = blk[MMQ_Q4K_QS_OFF + 32 * (j >> 1) + (e & 31)];
+  return (j & 1) ? (byte >> 4) : (byte & 0xF);
+}
+
+// dense W_exp plane, element (o, sb*256 + e) at o*id + sb*256 + e: q6_K the
+// centered code q - 32, q4_K the code q
+template <bool kQ4>
 __global__ void __launch_bounds__(256) expand_wexp_kernel(const uint8_t *__restrict__ W,
                                                           int64_t id, int8_t *__restrict__ wexp) {
-  __shared__ uint8_t blk[MMQ_Q6K_BLOCK_BYTES + 2];
+  constexpr int kBytes = kQ4 ? MMQ_Q4K_BLOCK_BYTES : MMQ_Q6K_BLOCK_BYTES;
+  __shared__ uint8_t blk[kBytes + 2];
   const int64_t nsb = id / MMQ_QK;
   const int64_t o = blockIdx.x, sb = blockIdx.y;
   const int e = threadIdx.x;
-  if (e < MMQ_Q6K_BLOCK_BYTES) blk[e] = W[(o * nsb + sb) * MMQ_Q6K_BLOCK_BYTES + e];
+  if (e < kBytes) blk[e] = W[(o * nsb + sb) * kBytes + e];
   __syncthreads();
-  wexp[o * id + sb * MMQ_QK + e] = static_cast<int8_t>(q6k_centered(blk, e));
+  wexp[o * id + sb * MMQ_QK + e] = static_cast<int8_t>(kQ4 ? q4k_code(blk, e) : q6k_centered(blk, e));
 }
 
 template <bool kQ4, bool kFromWexp>
@@ -86,8 +96,9 @@ __global__ void __launch_bounds__(256) register_kernel(const uint8_t *__restrict
   float d;
   if constexpr (kQ4) {
     const int j = e >> 5;
-    const int byte = blk[MMQ_Q4K_QS_OFF + 32 * (j >> 1) + (e & 31)];
-    const int q = (j & 1) ? (byte >> 4) : (byte & 0xF);
+    int q;
+    if constexpr (kFromWexp) q = wexp[o * id + sb * MMQ_QK + e];  // the dense plane's strides
+    else q = q4k_code(blk, e);
     int sc, m;
     q4k_scale_min(blk + MMQ_Q4K_SC_OFF, j, sc, m);
     val = sc * q;
@@ -163,7 +174,52 @@ __global__ void __launch_bounds__(64) register_raw_kernel(const uint8_t *__restr
   }
 }
 
+// Dequantization fallback: weight (o, sb*256 + e), exact in fp64, rounded
+// once to the output type.  One CTA of 256 threads per block.
+template <bool kQ4, typename T>
+__global__ void __launch_bounds__(256) dequant_kernel(const uint8_t *__restrict__ W, int64_t id,
+                                                      T *__restrict__ out) {
+  constexpr int kBytes = kQ4 ? MMQ_Q4K_BLOCK_BYTES : MMQ_Q6K_BLOCK_BYTES;
+  __shared__ uint8_t blk[kBytes + 2];
+  const int64_t nsb = id / MMQ_QK;
+  const int64_t o = blockIdx.x, sb = blockIdx.y;
+  const int e = threadIdx.x;
+  if (e < kBytes) blk[e] = W[(o * nsb + sb) * kBytes + e];
+  __syncthreads();
+  double w;
+  if constexpr (kQ4) {
+    int sc, m;
+    q4k_scale_min(blk + MMQ_Q4K_SC_OFF, e >> 5, sc, m);
+    const double d = static_cast<double>(f16_at(blk + MMQ_Q4K_D_OFF));
+    const double dmin = static_cast<double>(f16_at(blk + MMQ_Q4K_DMIN_OFF));
+    w = d * sc * q4k_code(blk, e) - dmin * m;  // both products exact in fp64
+  } else {
+    const int sc = static_cast<int8_t>(blk[MMQ_Q6K_SC_OFF + (e >> 4)]);
+    w = static_cast<double>(f16_at(blk + MMQ_Q6K_D_OFF)) * sc * q6k_centered(blk, e);
+  }
+  T v;
+  if constexpr (sizeof(T) == 2) v = __double2half(w);
+  else v = __double2float_rn(w);
+  out[o * id + sb * MMQ_QK + e] = v;
+}
+
 }  // namespace
+
+cudaError_t launch_dequant(int type, const uint8_t *W, int64_t od, int64_t id, void *out,
+                           int out_type, cudaStream_t s) {
+  const dim3 grid(static_cast<unsigned>(od), static_cast<unsigned>(id / MMQ_QK));
+  const bool q4 = type == MMQ_Q4_K;
+  if (out_type == MMQ_OUT_F16) {
+    __half *o = static_cast<__half *>(out);
+    if (q4) dequant_kernel<true, __half><<<grid, 256, 0, s>>>(W, id, o);
+    else dequant_kernel<false, __half><<<grid, 256, 0, s>>>(W, id, o);
+  } else {
+    float *o = static_cast<float *>(out);
+    if (q4) dequant_kernel<true, float><<<grid, 256, 0, s>>>(W, id, o);
+    else dequant_kernel<false, float><<<grid, 256, 0, s>>>(W, id, o);
+  }
+  return cudaGetLastError();
+}
 
 size_t rawplane_bytes(int type, int64_t od, int64_t id) {
   const bool q4 = type == MMQ_Q4_K;
@@ -199,10 +255,13 @@ cudaError_t launch_register(const mmq_weights_s *h, const uint8_t *W, int *bad_s
     else
       register_raw_kernel<false><<<grid, 64, 0, s>>>(W, h->id, h->rawplane);
   }
-  if (q4) {
+  if (q4 && h->wexp) {
+    expand_wexp_kernel<true><<<grid, 256, 0, s>>>(W, h->id, h->wexp);
+    register_kernel<true, true><<<grid, 256, 0, s>>>(W, h->wexp, h->id, bp, sr, bad_scale);
+  } else if (q4) {
     register_kernel<true, false><<<grid, 256, 0, s>>>(W, nullptr, h->id, bp, sr, bad_scale);
   } else if (h->wexp) {
-    expand_wexp_kernel<<<grid, 256, 0, s>>>(W, h->id, h->wexp);
+    expand_wexp_kernel<false><<<grid, 256, 0, s>>>(W, h->id, h->wexp);
     register_kernel<false, true><<<grid, 256, 0, s>>>(W, h->wexp, h->id, bp, sr, bad_scale);
   } else {
     register_kernel<false, false><<<grid, 256, 0, s>>>(W, nullptr, h->id, bp, sr, bad_scale);

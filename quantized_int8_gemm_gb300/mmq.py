@@ -36,6 +36,8 @@ MMQ_REG_RAW = 0x2
 MMQ_ARM_AUTO = 0
 MMQ_ARM_F16 = 1
 MMQ_ARM_RAW = 2
+MMQ_OUT_F16 = 1
+MMQ_OUT_F32 = 2
 ARM_NAMES = {MMQ_ARM_F16: "f16_plane", MMQ_ARM_RAW: "raw_unpack"}
 
 Q8_BLOCK_BYTES = 40
@@ -44,7 +46,7 @@ BLOCK_BYTES = {MMQ_Q4_K: 144, MMQ_Q6_K: 210}
 EXPORTS = [
     "mmq_quantize_act", "mmq_register_weights", "mmq_release_weights", "mmq_weights_wexp",
     "mmq_weights_info", "mmq_gemm", "mmq_gemm_f32", "mmq_gemm_profiled", "mmq_gemm_f32_profiled",
-    "mmq_gemm_noalloc",
+    "mmq_gemm_noalloc", "mmq_dequantize_weights",
     "mmq_last_device_error", "mmq_set_wait_timeout_ns",
     "mmq_selftest_wait_timeout", "mmq_strerror",
 ]
@@ -82,6 +84,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         L.mmq_gemm_profiled.argtypes = [vp, vp, i64, vp, vp, u32, ctypes.POINTER(i32), vp, vp]
         L.mmq_gemm_f32_profiled.argtypes = [vp, vp, i64, vp, vp, u32, ctypes.POINTER(i32), vp, vp]
         L.mmq_gemm_noalloc.argtypes = [vp, vp, i64, vp, vp]
+        L.mmq_dequantize_weights.argtypes = [i32, vp, i64, i64, vp, i32, vp]
         L.mmq_last_device_error.argtypes = []
         L.mmq_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
         L.mmq_set_wait_timeout_ns.restype = None
@@ -164,6 +167,17 @@ def mmq_register_weights(qtype, W: torch.Tensor, od: int, id_: int, flags: int =
     _check(load().mmq_register_weights(int(qt), _dev_ptr(W, "W"), od, id_, flags, _stream(stream),
                                        ctypes.byref(h)), "mmq_register_weights")
     return Weights(h.value, int(qt), od, id_, flags)
+
+
+def mmq_dequantize_weights(qtype, W: torch.Tensor, od: int, id_: int, dtype=torch.float16,
+                           stream=None) -> torch.Tensor:
+    """Packed k-quant rows -> dense (od, id) fp16 or fp32 weights (the fallback plane)."""
+    qt = QTYPES.get(qtype, qtype)
+    out_type = {torch.float16: MMQ_OUT_F16, torch.float32: MMQ_OUT_F32}[dtype]
+    out = torch.empty((od, id_), dtype=dtype, device=W.device)
+    _check(load().mmq_dequantize_weights(int(qt), _dev_ptr(W, "W"), od, id_, _dev_ptr(out, "out"),
+                                         out_type, _stream(stream)), "mmq_dequantize_weights")
+    return out
 
 
 def mmq_weights_wexp(w: Weights) -> torch.Tensor:

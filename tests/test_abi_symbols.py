@@ -52,7 +52,7 @@ def test_strerror_and_argument_checks_without_gpu(lib):
     h = vp()
     assert lib.mmq_register_weights(7, vp(16), 4, 256, 0, None, ctypes.byref(h)) == -3
     assert lib.mmq_register_weights(14, vp(16), 4, 300, 0, None, ctypes.byref(h)) == -1
-    assert lib.mmq_register_weights(12, vp(16), 4, 256, 1, None, ctypes.byref(h)) == -7
+    assert lib.mmq_register_weights(12, vp(16), 4, 256, 0x80, None, ctypes.byref(h)) == -1  # unknown flag
     lib.mmq_gemm.argtypes = [vp, vp, i64, vp, vp, ctypes.c_uint32, ctypes.POINTER(ctypes.c_int)]
     assert lib.mmq_gemm(None, None, 4, None, None, 0, None) == -1
 

@@ -170,8 +170,8 @@ def test_error_codes(mmq):
         mmq.mmq_register_weights(7, W, 8, 256)
     assert e.value.code == -3
     with pytest.raises(mmq.MMQError) as e:
-        mmq.mmq_register_weights("q4_K", W, 8, 256, mmq.MMQ_REG_WEXP)
-    assert e.value.code == -7
+        mmq.mmq_register_weights("q4_K", W, 8, 256, 0x80)  # no such flag
+    assert e.value.code == -1
     # q6_K sub-block scale beyond +-64: sc*(q-32) would not be exact in fp16
     Wb = gen.weights("q6_K", 8, 256, seed=2).reshape(8, 210)
     Wb[3, 192 + 5] = np.uint8(np.int8(-100).view(np.uint8))
@@ -319,3 +319,29 @@ def test_raw_arm_argument_errors(mmq):
         mmq.mmq_gemm(w, Q, 4, flags=7)  # no such arm
     assert ei.value.code == -7
     w.release()
+
+
+# --------------------------------------------------------------------------
+# the W_exp code plane carried to q4_K, and the dequantization fallback
+@pytest.mark.parametrize("od,id_,nt", [(300, 768, 70), (131, 2048, 129)])
+def test_q4k_wexp_plane_and_consumer(mmq, od, id_, nt):
+    W = gen.weights("q4_K", od, id_, seed=41)
+    X = gen.activations(nt, id_, seed=42)
+    w, Q, Y, _ = _run(mmq, "q4_K", W, od, id_, X, mmq.MMQ_REG_WEXP)
+    # producer gate: the plane's bytes; consumer gate: the GEMM built from it
+    assert np.array_equal(mmq.mmq_weights_wexp(w).cpu().numpy(), oracle.expand_q4k_dense(W, od, id_))
+    err, bound = _within_tol(Y, oracle.gemm(oracle.Q4_K, W, od, id_, oracle.quantize_q8_0(X), nt))
+    assert err <= bound, (err, bound)
+    w.release()
+
+
+@pytest.mark.parametrize("name,od,id_", [("q6_K", 300, 768), ("q4_K", 131, 2048), ("q6_K", 5, 256)])
+def test_dequantize_weights_bit_exact(mmq, name, od, id_):
+    W = gen.weights(name, od, id_, seed=43)
+    Wd = torch.from_numpy(W).cuda()
+    ref = oracle.dequant_weights(QT[name], W, od, id_)
+    for dt, npt in ((torch.float16, np.float16), (torch.float32, np.float32)):
+        got = mmq.mmq_dequantize_weights(name, Wd, od, id_, dt).cpu().numpy()
+        want = ref.astype(npt)  # one rounding, to nearest even, from the exact fp64 weight
+        assert np.array_equal(got.view(np.uint16 if npt is np.float16 else np.uint32),
+                              want.view(np.uint16 if npt is np.float16 else np.uint32))

@@ -472,3 +472,22 @@ def test_gemm_is_not_transposed():
     assert not Y[[0, 1, 3, 4]].any()
     deq = oracle.dequant_weights(oracle.Q4_K, W, od, id_)
     np.testing.assert_allclose(Y[2], deq @ oracle.dequant_act(Q, nt, id_)[2], rtol=1e-12)
+
+
+def test_q4k_dense_plane_codes():
+    """The dense q4_K code plane against the per-element code reading, and
+    a hand-built block: qs byte i = i, so element e reads byte
+    32*(e//64) + e%32 and takes its low nibble when (e//32) is even."""
+    W = gen.weights("q4_K", 3, 512, seed=9)
+    P = oracle.expand_q4k_dense(W, 3, 512)
+    B = W.reshape(3, 2, 144)
+    for j in range(3):
+        for sb in range(2):
+            assert [int(P[j, sb * 256 + e]) for e in range(256)] == \
+                [oracle.q4k_quant(B[j, sb], e) for e in range(256)]
+    blk = np.zeros(144, dtype=np.uint8)
+    blk[16:144] = np.arange(128, dtype=np.uint8)
+    P1 = oracle.expand_q4k_dense(blk, 1, 256)[0]
+    # e=0: byte 0 low = 0; e=33: byte 1 high = 0; e=65: byte 33 low = 1;
+    # e=100: byte 36 high (36 = 0x24) = 2; e=255: byte 127 high (0x7f) = 7
+    assert (P1[0], P1[33], P1[65], P1[100], P1[255]) == (0, 0, 1, 2, 7)
