@@ -66,21 +66,43 @@ def _peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def _sha1(path):
-    with open(path, "rb") as f:
-        return hashlib.sha1(f.read()).hexdigest()
+def _code_sha1(path):
+    """sha1 of a C/CUDA source with comments removed and whitespace runs
+    collapsed, so that a comment edit does not orphan its profile."""
+    src = open(path).read()
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    code = " ".join("".join(out).split())
+    return hashlib.sha1(code.encode()).hexdigest()
 
 
 def _profiled_traffic(workload):
     """DRAM bytes per GEMM launch from the committed ncu summary of this
     workload, if it was taken on the current kernel source; else None."""
     src = os.path.join(ROOT, "quantized_int8_gemm_gb300", "csrc", "gemm.cu")
-    sha = _sha1(src)
+    sha = _code_sha1(src)
     for p in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
         text = open(p).read()
         if workload not in text:
             continue
-        m_sha = re.search(r"gemm_cu_sha1:\s*([0-9a-f]{40})", text)
+        m_sha = re.search(r"gemm_cu_code_sha1:\s*([0-9a-f]{40})", text)
         m_b = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
         if m_sha and m_b and m_sha.group(1) == sha:
             return int(m_b.group(1))

@@ -14,8 +14,10 @@
 //   Y'[t][o] += d[o][sb] * acc[t][o]  -  dmin[o][sb] * MIN[t][o][sb]   (per super-block)
 //   Y[t][o]   = Y'[t][o] * 2^-s_t                                (per tile)
 // The q4_K min term  sum_c da*ssum * dmin*m  runs on the tensor core: per
-// super-block one K=16 UMMA of  g' = da*ssum*2^s_t  split exactly into fp16
-// hi + lo  against the integer mins m  (MIN above); s_t is a per-token power
+// super-block one K=16 UMMA of  g' = da*ssum*2^s_t  split into fp16 hi + lo
+// against the integer mins m  (MIN above).  g' carries up to 23 significant
+// bits and hi + lo 22, so the split is exact for most chunks and otherwise
+// off by one unit of about 2^-22 of the token's largest g'; s_t is a per-token power
 // of two that keeps g' in fp16 range, and da' = da*2^s_t carries the same
 // factor so the final scaling by 2^-s_t is exact.
 //
