@@ -715,7 +715,7 @@ __global__ void __launch_bounds__(Shape<kRaw>::kThreads, 1)
           const uint64_t as = a0 + s * kStageDesc, bs = b0 + s * kStageDesc;
 #pragma unroll
           for (int q = 0; q < 2 && ok; ++q) {
-            const int lc = iw + 2 * q;  // chunk in the stage: K = 32*lc .. 32*lc+31
+            const int lc = 2 * iw + q;  // chunk in the stage: K = 32*lc .. 32*lc+31
             const uint64_t off = (lc >> 1) * (16384 >> 4) + (lc & 1) * (64 >> 4);
             ok = item(as + off, bs + off, true);
           }
@@ -781,29 +781,41 @@ __global__ void __launch_bounds__(Shape<kRaw>::kThreads, 1)
           nx1 = __ldg(darow + 2 * sb + 3);
         }
         uint32_t r0[32], r1[32];
-        uint32_t slot, par;
+        // Chunks come in pairs (2p, 2p+1), both from issuer p & 1 and
+        // committed in issue order, so the barrier of a pair's second chunk
+        // covers the pair: one wait per two chunks.
+        uint32_t slot, slot_b, par, par_b;
         next_item(0, slot, par);
-        if (!(ok = wait_item(slot, par, false))) break;
+        next_item(0, slot_b, par_b);
+        if (!(ok = wait_item(slot_b, par_b, false))) break;
         tmem_ld_32x32b_x32(taddr + slot * kTileN, r0);
         tmem_wait_ld(r0);
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-          // second half of chunk c, and an early test of chunk c+1
+          // second half of chunk c; in a pair's second chunk, an early test
+          // of the next pair
           tmem_ld_32x32b_x32(taddr + slot * kTileN + 32, r1);
-          uint32_t nslot = 0, npar = 0;
+          uint32_t na = 0, nb = 0, npb = 0;
           bool ready = true;
-          if (c < 7) {
-            next_item((c + 1) & 1, nslot, npar);
-            ready = mbar_try_wait(rfull(nslot), npar);
+          if ((c & 1) && c < 7) {
+            const int niw = ((c + 1) >> 1) & 1;
+            next_item(niw, na, par);
+            next_item(niw, nb, npb);
+            ready = mbar_test_wait(rfull(nb), npb);
           }
           reg_fence(r0);
           fold_half(acc, 0, r0, das[c], c == 0);
           tmem_wait_ld(r1);
           give(slot);
           if (c < 7) {
-            if (!(ok = wait_item(nslot, npar, ready))) break;
-            tmem_ld_32x32b_x32(taddr + nslot * kTileN, r0);
-            slot = nslot;
+            if (c & 1) {
+              if (!(ok = wait_item(nb, npb, ready))) break;
+              slot = na;
+              slot_b = nb;
+            } else {
+              slot = slot_b;
+            }
+            tmem_ld_32x32b_x32(taddr + slot * kTileN, r0);
           }
           fold_half(acc, 1, r1, das[c], c == 0);
           if (c < 7) tmem_wait_ld(r0);
