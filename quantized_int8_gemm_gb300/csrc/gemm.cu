@@ -351,8 +351,10 @@ __device__ __forceinline__ void emit_block(uint8_t *__restrict__ aplane, float *
 constexpr int kStashBytesPerBlock = 72;
 constexpr int kStashMaxBytes = 48 * 1024;
 
+constexpr int kQuantWarps = 8;  // one step of 16 blocks per warp covers id <= 4096
+
 template <bool kQ4, bool kStash>
-__global__ void __launch_bounds__(128) quantize_prepass_kernel(const float *__restrict__ X,
+__global__ void __launch_bounds__(32 * kQuantWarps) quantize_prepass_kernel(const float *__restrict__ X,
                                                                int64_t nt, int64_t nb32,
                                                                uint8_t *__restrict__ aplane,
                                                                float *__restrict__ dap,
@@ -366,7 +368,7 @@ __global__ void __launch_bounds__(128) quantize_prepass_kernel(const float *__re
   int *sssum = reinterpret_cast<int *>(sd16 + nb32);
   float gmax = 0.f;
   // pass 1 (the only one for q6_K, whose operands need no token scale)
-  for (int64_t base = warp * 16; base < nb32; base += 64) {
+  for (int64_t base = warp * 16; base < nb32; base += 16 * kQuantWarps) {
     float4 v[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
@@ -399,12 +401,13 @@ __global__ void __launch_bounds__(128) quantize_prepass_kernel(const float *__re
     if (tid == 0) invp[t] = 1.0f;
   } else {
   // s_t: the token's largest |d16 * ssum| lands in [2^14, 2^15)
-  __shared__ float wmax[4];
+  __shared__ float wmax[kQuantWarps];
 #pragma unroll
   for (int m = 16; m; m >>= 1) gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, m));
   if (lane == 0) wmax[warp] = gmax;
   __syncthreads();
-  gmax = fmaxf(fmaxf(wmax[0], wmax[1]), fmaxf(wmax[2], wmax[3]));
+#pragma unroll
+  for (int w = 0; w < kQuantWarps; ++w) gmax = fmaxf(gmax, wmax[w]);
   int s = 0;
   if (gmax > 0.f) {
     const int e = static_cast<int>((__float_as_uint(gmax) >> 23) & 0xFF) - 127;
@@ -414,12 +417,12 @@ __global__ void __launch_bounds__(128) quantize_prepass_kernel(const float *__re
   if (tid == 0) invp[t] = __uint_as_float(static_cast<uint32_t>(127 - s) << 23);
   // pass 2
   if (kStash) {
-    for (int64_t c = tid >> 3; c < nb32; c += 16) {
+    for (int64_t c = tid >> 3; c < nb32; c += 4 * kQuantWarps) {
       const uint2 hw = reinterpret_cast<const uint2 *>(stash + c * 16)[part];
       emit_block<true>(aplane, dap, t, c, nb32, part, hw.x, hw.y, sd16[c], sssum[c], scale);
     }
   } else {
-    for (int64_t base = warp * 16; base < nb32; base += 64) {
+    for (int64_t base = warp * 16; base < nb32; base += 16 * kQuantWarps) {
       float4 v[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
@@ -501,6 +504,12 @@ __device__ __forceinline__ bool work_next(Work &w, int n_tiles, int64_t nsb, int
   sb1 = nsb;
   w.tile += gridDim.x;
   return true;
+}
+
+__device__ __forceinline__ void st_global_v8(float *p, float2 a, float2 b, float2 c, float2 d) {
+  asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "f"(a.x), "f"(a.y),
+               "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y), "f"(d.x), "f"(d.y)
+               : "memory");
 }
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
@@ -921,7 +930,17 @@ __global__ void __launch_bounds__(Shape<kRaw>::kThreads, 1)
         const float inv = __ldg(invp + t);
         const float2 inv2 = make_float2(inv, inv);
         float *yrow = Y + t * od + o0;
-        if ((od & 3) == 0) {
+        if ((od & 7) == 0 && (reinterpret_cast<uintptr_t>(Y) & 31) == 0) {
+          // 32-byte stores: each row segment of a warp's store is a whole sector
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            if (o0 + 2 * i < od) {
+              const float2 a = __fmul2_rn(y[i], inv2), b = __fmul2_rn(y[i + 1], inv2);
+              const float2 c = __fmul2_rn(y[i + 2], inv2), d = __fmul2_rn(y[i + 3], inv2);
+              st_global_v8(yrow + 2 * i, a, b, c, d);
+            }
+          }
+        } else if ((od & 3) == 0) {
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {
             if (o0 + 2 * i < od) {
@@ -1103,11 +1122,11 @@ cudaError_t launch_gemm(const mmq_weights_s *h, const uint8_t *Q, const float *X
   if (X) {
     const size_t stash = static_cast<size_t>(nb32) * kStashBytesPerBlock;
     if (!q4)
-      quantize_prepass_kernel<false, false><<<pgrid, 128, 0, s>>>(X, nt, nb32, aplane, dap, invp);
+      quantize_prepass_kernel<false, false><<<pgrid, 32 * kQuantWarps, 0, s>>>(X, nt, nb32, aplane, dap, invp);
     else if (stash <= static_cast<size_t>(kStashMaxBytes))
-      quantize_prepass_kernel<true, true><<<pgrid, 128, stash, s>>>(X, nt, nb32, aplane, dap, invp);
+      quantize_prepass_kernel<true, true><<<pgrid, 32 * kQuantWarps, stash, s>>>(X, nt, nb32, aplane, dap, invp);
     else
-      quantize_prepass_kernel<true, false><<<pgrid, 128, 0, s>>>(X, nt, nb32, aplane, dap, invp);
+      quantize_prepass_kernel<true, false><<<pgrid, 32 * kQuantWarps, 0, s>>>(X, nt, nb32, aplane, dap, invp);
   } else if (q4) {
     gemm_prepass_kernel<true><<<pgrid, 128, 0, s>>>(Q, nt, nb32, aplane, dap, invp);
   } else {
