@@ -223,6 +223,7 @@ __global__ void __launch_bounds__(128) gemm_prepass_kernel(const uint8_t *__rest
                                                            uint8_t *__restrict__ aplane,
                                                            float *__restrict__ dap,
                                                            float *__restrict__ invp) {
+  griddep_launch_dependents();
   const int64_t t = blockIdx.x;
   const int tid = threadIdx.x;
   const uint8_t *qrow = Q + t * nb32 * MMQ_Q8_BLOCK_BYTES;
@@ -360,6 +361,7 @@ __global__ void __launch_bounds__(32 * kQuantWarps) quantize_prepass_kernel(cons
                                                                float *__restrict__ dap,
                                                                float *__restrict__ invp) {
   extern __shared__ uint32_t stash[];  // [nb32][16] operand words, then [nb32] d16, [nb32] ssum
+  griddep_launch_dependents();
   const int64_t t = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int part = lane & 7, grp = lane >> 3;
@@ -581,6 +583,27 @@ __global__ void __launch_bounds__(Shape<kRaw>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *reinterpret_cast<volatile uint32_t *>(smem + L::kSlot);
+  // The activation plane, da' and 2^-s are written by the kernel before this
+  // one, which may still be running (programmatic launch); the weight side is
+  // not, so its first blocks are pulled into L2 meanwhile.
+  if (warp == PRODUCER_WARP && lane == 0) {
+    Work wk = work_begin(kSK, static_cast<int64_t>(n_tiles) * nsb);
+    int tile;
+    int64_t sb0, sb1;
+    if (work_next(wk, n_tiles, nsb, tile, sb0, sb1)) {
+      const int ot = tile / n_tt;
+      for (int64_t sb = sb0; sb < sb1 && sb < sb0 + 2; ++sb) {
+        bulk_prefetch_l2(bscale + b_scale_block(ot, sb, nsb, kQ4), L::kScale);
+        for (int half = 0; half < 2; ++half) {
+          if (kRaw)
+            bulk_prefetch_l2(rawplane + raw_block(ot, sb, half, nsb, kQ4), raw_block_bytes(kQ4));
+          else
+            bulk_prefetch_l2(bplane + b_block(ot, sb, half, nsb, kQ4), half ? b_odd_bytes(kQ4) : b_even_bytes());
+        }
+      }
+    }
+  }
+  griddep_wait();
   if (warp >= PRODUCER_WARP) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(S::kRegsCtl));
   if (warp == PRODUCER_WARP) {
@@ -1069,7 +1092,7 @@ template <bool kQ4, bool kSK, bool kRaw>
 cudaError_t launch_variant(int dev, int grid, cudaStream_t s, const uint8_t *aplane, const uint8_t *bplane,
                            const uint8_t *rawplane, const uint8_t *bscale, const float *dap,
                            const float *invp, int64_t nt, int64_t od, int64_t nb32, int n_tt, int n_ot,
-                           float *Y, WaitCtl w, float4 *ws, uint64_t *flags) {
+                           float *Y, WaitCtl w, float4 *ws, uint64_t *flags, bool pdl) {
   auto kern = mmq_gemm_kernel<kQ4, kSK, kRaw>;
   constexpr int smem = Smem<kQ4, kRaw>::kBytes;
   static std::atomic<int> ready[64];  // 0 unknown, 1 ready, 2 unusable
@@ -1083,9 +1106,18 @@ cudaError_t launch_variant(int dev, int grid, cudaStream_t s, const uint8_t *apl
     ready[dev].store(st);
   }
   if (st != 1) return cudaErrorInvalidKernelImage;
-  kern<<<grid, Shape<kRaw>::kThreads, smem, s>>>(aplane, bplane, rawplane, bscale, dap, invp, nt, od, nb32,
-                                                 n_tt, n_ot, Y, w, ws, flags);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(Shape<kRaw>::kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, aplane, bplane, rawplane, bscale, dap, invp, nt, od, nb32, n_tt,
+                            n_ot, Y, w, ws, flags);
 }
 
 }  // namespace
@@ -1145,7 +1177,7 @@ cudaError_t launch_gemm(const mmq_weights_s *h, const uint8_t *Q, const float *X
   const int nti = static_cast<int>(n_tt);
 #define MMQ_LAUNCH(Q4, SK, RAW)                                                                 \
   launch_variant<Q4, SK, RAW>(dev, p.grid, s, aplane, bp, rp, bs, dap, invp, nt, h->od, nb32, nti, \
-                              p.n_ot, Y, w, ws, flags)
+                              p.n_ot, Y, w, ws, flags, ev0 == nullptr)
   if (q4)
     e = p.streamk ? (raw ? MMQ_LAUNCH(true, true, true) : MMQ_LAUNCH(true, true, false))
                   : (raw ? MMQ_LAUNCH(true, false, true) : MMQ_LAUNCH(true, false, false));
