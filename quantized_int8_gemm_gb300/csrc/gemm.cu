@@ -584,26 +584,9 @@ __global__ void __launch_bounds__(Shape<kRaw>::kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *reinterpret_cast<volatile uint32_t *>(smem + L::kSlot);
   // The activation plane, da' and 2^-s are written by the kernel before this
-  // one, which may still be running (programmatic launch); the weight side is
-  // not, so its first blocks are pulled into L2 meanwhile.
-  if (warp == PRODUCER_WARP && lane == 0) {
-    Work wk = work_begin(kSK, static_cast<int64_t>(n_tiles) * nsb);
-    int tile;
-    int64_t sb0, sb1;
-    if (work_next(wk, n_tiles, nsb, tile, sb0, sb1)) {
-      const int ot = tile / n_tt;
-      for (int64_t sb = sb0; sb < sb1 && sb < sb0 + 2; ++sb) {
-        bulk_prefetch_l2(bscale + b_scale_block(ot, sb, nsb, kQ4), L::kScale);
-        for (int half = 0; half < 2; ++half) {
-          if (kRaw)
-            bulk_prefetch_l2(rawplane + raw_block(ot, sb, half, nsb, kQ4), raw_block_bytes(kQ4));
-          else
-            bulk_prefetch_l2(bplane + b_block(ot, sb, half, nsb, kQ4), half ? b_odd_bytes(kQ4) : b_even_bytes());
-        }
-      }
-    }
-  }
-  griddep_wait();
+  // one, which may still be running (programmatic launch): the producer and
+  // the epilogue wait for it before their first read of them; the weight side
+  // does not depend on it.
   if (warp >= PRODUCER_WARP) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(S::kRegsCtl));
   if (warp == PRODUCER_WARP) {
@@ -611,6 +594,7 @@ __global__ void __launch_bounds__(Shape<kRaw>::kThreads, 1)
     // The whole warp runs the loop (warp-uniform control flow); lane 0 copies
     // the activation block, lane 1 the weight block, lane 2 the super-block's
     // scale block into the scale ring.
+    griddep_wait();
     uint32_t ks = 0, ns = 0, issued = 0, s_issued = 0, r_issued = 0;
     bool ok = true;
     Work wk = work_begin(kSK, static_cast<int64_t>(n_tiles) * nsb);
@@ -762,6 +746,25 @@ __global__ void __launch_bounds__(Shape<kRaw>::kThreads, 1)
     if (elected) umma_commit(done);  // all UMMAs of both issuers have finished once `done` flips
     __syncwarp();
     mbar_wait(done, 0, wctl, false);
+  } else if (warp == PRODUCER_WARP + 3 && lane == 0) {
+    // ------------------------------------------------------------ L2 prefetch
+    // The first two super-blocks of this CTA's weight (and scale) blocks,
+    // pulled into L2 off the producer's path.
+    Work wk = work_begin(kSK, static_cast<int64_t>(n_tiles) * nsb);
+    int tile;
+    int64_t sb0, sb1;
+    if (work_next(wk, n_tiles, nsb, tile, sb0, sb1)) {
+      const int ot = tile / n_tt;
+      for (int64_t sb = sb0; sb < sb1 && sb < sb0 + 2; ++sb) {
+        bulk_prefetch_l2(bscale + b_scale_block(ot, sb, nsb, kQ4), L::kScale);
+        for (int half = 0; half < 2; ++half) {
+          if (kRaw)
+            bulk_prefetch_l2(rawplane + raw_block(ot, sb, half, nsb, kQ4), raw_block_bytes(kQ4));
+          else
+            bulk_prefetch_l2(bplane + b_block(ot, sb, half, nsb, kQ4), half ? b_odd_bytes(kQ4) : b_even_bytes());
+        }
+      }
+    }
   }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(S::kRegsEpi));
@@ -796,6 +799,7 @@ __global__ void __launch_bounds__(Shape<kRaw>::kThreads, 1)
     Work wk = work_begin(kSK, units);
     int tile;
     int64_t sb0, sb1;
+    griddep_wait();  // da' and 2^-s come from the kernel before this one
     while (ok && work_next(wk, n_tiles, nsb, tile, sb0, sb1)) {
       const int tt = tile % n_tt, ot = tile / n_tt;
       const int64_t t = static_cast<int64_t>(tt) * kTileM + row;  // < nt_pad: planes are padded
