@@ -820,6 +820,8 @@ __global__ void __launch_bounds__(Shape<kRaw>::kThreads, 1)
         // Chunks come in pairs (2p, 2p+1), both from issuer p & 1 and
         // committed in issue order, so the barrier of a pair's second chunk
         // covers the pair: one wait per two chunks.
+        const int e = static_cast<int>(ns % SRING);
+        const bool s_ready = mbar_test_wait(sfull(e), (ns / SRING) & 1);  // early probe of the scales
         uint32_t slot, slot_b, par, par_b;
         next_item(0, slot, par);
         next_item(0, slot_b, par_b);
@@ -858,8 +860,7 @@ __global__ void __launch_bounds__(Shape<kRaw>::kThreads, 1)
         }
         if (!ok) break;
         // super-block end: y += d * acc  (- dmin * MIN for q4_K)
-        const int e = static_cast<int>(ns % SRING);
-        ok = __all_sync(0xffffffffu, mbar_wait(sfull(e), (ns / SRING) & 1, wctl));
+        ok = __all_sync(0xffffffffu, s_ready || mbar_wait(sfull(e), (ns / SRING) & 1, wctl));
         if (!ok) break;
         const uint8_t *sblk = smem + (s_smem(e) - base);
         const float4 *d4 = reinterpret_cast<const float4 *>(sblk) + chalf * 16;
@@ -870,6 +871,8 @@ __global__ void __launch_bounds__(Shape<kRaw>::kThreads, 1)
           y[2 * i + 1] = __ffma2_rn(make_float2(d.z, d.w), acc[2 * i + 1], y[2 * i + 1]);
         }
         if (kQ4) {
+          // the min-term item needs a wait of its own: its slot is the one
+          // chunk 4 held, so it cannot be issued before chunk 4 is loaded
           next_item(0, slot, par);
           if (!(ok = wait_item(slot, par, false))) break;
           tmem_ld_32x32b_x32(taddr + slot * kTileN, r0);
