@@ -469,32 +469,39 @@ __device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
                  "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
 }
 
-// The work of one CTA as segments (tile, super-blocks [sb0, sb1)).
+// The work of one CTA as segments (tile, super-blocks [sb0, sb1)); tile =
+// token tile + n_tt * weight tile.
 // Tile mode: whole tiles blockIdx.x, blockIdx.x + gridDim.x, ...
-// Stream-K mode: the (tile, super-block) units are split into gridDim.x
-// contiguous ranges of nearly equal length; a tile cut between CTAs is
-// finished by the CTA that holds its first super-block (its owner).
+// Stream-K mode: the grid is gridDim.x / n_tt groups of n_tt CTAs.  Member m
+// of a group takes token tile m, and each group an equal contiguous share of
+// the (weight tile, super-block) units, so the CTAs of a group read the same
+// weight blocks at the same time.  A tile cut between groups is finished by
+// the CTA that holds its first super-block (its owner).
 struct Work {
-  int64_t u, u_end;  // stream-K: current and end unit
+  int64_t u, u_end;  // stream-K: current and end unit of the group
   int tile;          // tile mode: next tile
+  int member;        // stream-K: token tile
   bool sk;
 };
-__device__ __forceinline__ int64_t sk_begin(int64_t units, int cta, int ctas) {
-  return units * cta / ctas;
+__device__ __forceinline__ int64_t sk_begin(int64_t gunits, int group, int groups) {
+  return gunits * group / groups;
 }
-__device__ __forceinline__ Work work_begin(bool sk, int64_t units) {
+__device__ __forceinline__ Work work_begin(bool sk, int n_tt, int n_ot, int64_t nsb) {
   Work w;
   w.sk = sk;
-  w.u = sk_begin(units, blockIdx.x, gridDim.x);
-  w.u_end = sk_begin(units, blockIdx.x + 1, gridDim.x);
+  const int groups = static_cast<int>(gridDim.x) / n_tt, g = static_cast<int>(blockIdx.x) / n_tt;
+  const int64_t gunits = static_cast<int64_t>(n_ot) * nsb;
+  w.u = sk_begin(gunits, g, groups);
+  w.u_end = sk_begin(gunits, g + 1, groups);
+  w.member = static_cast<int>(blockIdx.x) % n_tt;
   w.tile = blockIdx.x;
   return w;
 }
-__device__ __forceinline__ bool work_next(Work &w, int n_tiles, int64_t nsb, int &tile, int64_t &sb0,
+__device__ __forceinline__ bool work_next(Work &w, int n_tiles, int n_tt, int64_t nsb, int &tile, int64_t &sb0,
                                           int64_t &sb1) {
   if (w.sk) {
     if (w.u >= w.u_end) return false;
-    tile = static_cast<int>(w.u / nsb);
+    tile = w.member + n_tt * static_cast<int>(w.u / nsb);
     sb0 = w.u % nsb;
     sb1 = min(nsb, sb0 + (w.u_end - w.u));
     w.u += sb1 - sb0;
@@ -597,10 +604,10 @@ __global__ void __launch_bounds__(Shape<kRaw>::kThreads, 1)
     griddep_wait();
     uint32_t ks = 0, ns = 0, issued = 0, s_issued = 0, r_issued = 0;
     bool ok = true;
-    Work wk = work_begin(kSK, static_cast<int64_t>(n_tiles) * nsb);
+    Work wk = work_begin(kSK, n_tt, n_ot, nsb);
     int tile;
     int64_t sb0, sb1;
-    while (ok && work_next(wk, n_tiles, nsb, tile, sb0, sb1)) {
+    while (ok && work_next(wk, n_tiles, n_tt, nsb, tile, sb0, sb1)) {
       const int tt = tile % n_tt, ot = tile / n_tt;
       for (int64_t sb = sb0; sb < sb1 && ok; ++sb, ++ns) {
         const int e = static_cast<int>(ns % SRING);
@@ -660,10 +667,10 @@ __global__ void __launch_bounds__(Shape<kRaw>::kThreads, 1)
     const int r = threadIdx.x - CONVERTER_WARP * 32;  // row of the weight tile
     uint32_t ks = 0;
     bool ok = true;
-    Work wk = work_begin(kSK, static_cast<int64_t>(n_tiles) * nsb);
+    Work wk = work_begin(kSK, n_tt, n_ot, nsb);
     int tile;
     int64_t sb0, sb1;
-    while (ok && work_next(wk, n_tiles, nsb, tile, sb0, sb1)) {
+    while (ok && work_next(wk, n_tiles, n_tt, nsb, tile, sb0, sb1)) {
       for (int64_t sb = sb0; sb < sb1 && ok; ++sb) {
         for (int half = 0; half < 2 && ok; ++half, ++ks) {
           const int re = static_cast<int>(ks % RRING), s = static_cast<int>(ks % STAGES);
@@ -717,10 +724,10 @@ __global__ void __launch_bounds__(Shape<kRaw>::kThreads, 1)
       }
       return got;
     };
-    Work wk = work_begin(kSK, static_cast<int64_t>(n_tiles) * nsb);
+    Work wk = work_begin(kSK, n_tt, n_ot, nsb);
     int tile;
     int64_t sb0, sb1;
-    while (ok && work_next(wk, n_tiles, nsb, tile, sb0, sb1)) {
+    while (ok && work_next(wk, n_tiles, n_tt, nsb, tile, sb0, sb1)) {
       for (int64_t sb = sb0; sb < sb1 && ok; ++sb) {
         for (int half = 0; half < 2 && ok; ++half, ++ks) {
           const int s = static_cast<int>(ks % STAGES);
@@ -750,10 +757,10 @@ __global__ void __launch_bounds__(Shape<kRaw>::kThreads, 1)
     // ------------------------------------------------------------ L2 prefetch
     // The first two super-blocks of this CTA's weight (and scale) blocks,
     // pulled into L2 off the producer's path.
-    Work wk = work_begin(kSK, static_cast<int64_t>(n_tiles) * nsb);
+    Work wk = work_begin(kSK, n_tt, n_ot, nsb);
     int tile;
     int64_t sb0, sb1;
-    if (work_next(wk, n_tiles, nsb, tile, sb0, sb1)) {
+    if (work_next(wk, n_tiles, n_tt, nsb, tile, sb0, sb1)) {
       const int ot = tile / n_tt;
       for (int64_t sb = sb0; sb < sb1 && sb < sb0 + 2; ++sb) {
         bulk_prefetch_l2(bscale + b_scale_block(ot, sb, nsb, kQ4), L::kScale);
@@ -795,12 +802,11 @@ __global__ void __launch_bounds__(Shape<kRaw>::kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(rempty(slot));
     };
-    const int64_t units = static_cast<int64_t>(n_tiles) * nsb;
-    Work wk = work_begin(kSK, units);
+    Work wk = work_begin(kSK, n_tt, n_ot, nsb);
     int tile;
     int64_t sb0, sb1;
     griddep_wait();  // da' and 2^-s come from the kernel before this one
-    while (ok && work_next(wk, n_tiles, nsb, tile, sb0, sb1)) {
+    while (ok && work_next(wk, n_tiles, n_tt, nsb, tile, sb0, sb1)) {
       const int tt = tile % n_tt, ot = tile / n_tt;
       const int64_t t = static_cast<int64_t>(tt) * kTileM + row;  // < nt_pad: planes are padded
       const int64_t o0 = static_cast<int64_t>(ot) * kTileN + chalf * 64;
@@ -924,11 +930,14 @@ __global__ void __launch_bounds__(Shape<kRaw>::kThreads, 1)
           }
           continue;
         }
-        // owner: add the partials of the following CTAs that reach into this
-        // tile, in CTA order (deterministic results)
-        const int64_t tile_end = static_cast<int64_t>(tile + 1) * nsb;
-        for (int j = blockIdx.x + 1; j < static_cast<int>(gridDim.x) && sk_begin(units, j, gridDim.x) < tile_end && ok;
-             ++j) {
+        // owner: add the partials of the same member of the following groups
+        // that reach into this tile, in group order (deterministic results)
+        const int groups = static_cast<int>(gridDim.x) / n_tt;
+        const int64_t gunits = static_cast<int64_t>(n_ot) * nsb;
+        const int64_t tile_end = static_cast<int64_t>(ot + 1) * nsb;
+        for (int gg = static_cast<int>(blockIdx.x) / n_tt + 1;
+             gg < groups && sk_begin(gunits, gg, groups) < tile_end && ok; ++gg) {
+          const int j = gg * n_tt + wk.member;
           if (threadIdx.x == 0) {
             const uint64_t t0 = globaltimer_ns();
             uint64_t v = 0;
@@ -1066,13 +1075,19 @@ GemmPlan plan_gemm(const mmq_weights_s *h, int64_t nt, bool streamk_allowed) {
   p.n_ot = static_cast<int>(h->od_pad / kTileN);
   p.n_tiles = static_cast<int>(p.n_tt) * p.n_ot;
   const int sms = num_sms(h->device);
-  // whole tiles per CTA, unless the last wave would leave more than a tenth
-  // of the SMs idle: then split the (tile, super-block) units evenly
-  const int64_t units = static_cast<int64_t>(p.n_tiles) * p.nsb;
+  // Whole tiles per CTA, unless groups of n_tt CTAs sharing the (weight
+  // tile, super-block) units evenly cut the longest CTA's work by more than a
+  // tenth and by more than three super-blocks: publishing and collecting a
+  // split tile's partial sums costs about three super-blocks of work
+  // (measured on the 3584 x 3584 q-proj shapes, where whole tiles win).
   const int64_t waves = (p.n_tiles + sms - 1) / sms;
-  const bool uneven = 10 * p.n_tiles < 9 * waves * sms;
-  p.streamk = streamk_allowed && uneven && units > p.n_tiles;
-  p.grid = p.streamk ? static_cast<int>(units < sms ? units : sms) : (p.n_tiles < sms ? p.n_tiles : sms);
+  const int64_t gunits = static_cast<int64_t>(p.n_ot) * p.nsb;
+  int64_t groups = p.n_tt <= sms ? sms / p.n_tt : 0;
+  if (groups > gunits) groups = gunits;
+  const int64_t sk_max = groups > 0 ? (gunits + groups - 1) / groups : 0;
+  const int64_t tile_max = waves * p.nsb;
+  p.streamk = streamk_allowed && groups >= 2 && 10 * sk_max < 9 * tile_max && tile_max - sk_max > 3;
+  p.grid = p.streamk ? static_cast<int>(groups * p.n_tt) : (p.n_tiles < sms ? p.n_tiles : sms);
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
   p.a_off = 0;
   p.da_off = up(static_cast<size_t>(p.n_tt * p.nsb) * a_pair_bytes(p.q4));
