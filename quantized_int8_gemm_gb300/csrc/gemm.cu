@@ -317,39 +317,43 @@ __device__ __forceinline__ void quant_block8(float4 v, float &d, float &d16f, ui
         (static_cast<uint32_t>(__half_as_ushort(__int2half_rn(q[3]))) << 16);
 }
 
-// One 32-value block's results in the token's operand row, da' plane and
-// (q4_K) min-term slots; lane `part` of the block's eight writes its 4 values.
+// One 32-value block's fp16 operand words in the token's operand row; lane
+// `part` of the block's eight writes its 4 values.
 template <bool kQ4>
-__device__ __forceinline__ void emit_block(uint8_t *__restrict__ aplane, float *__restrict__ dap,
-                                           int64_t t, int64_t c, int64_t nb32, int part,
-                                           uint32_t h01, uint32_t h23, float d16f, int ssum,
-                                           float scale) {
+__device__ __forceinline__ void emit_operand(uint8_t *__restrict__ aplane, int64_t t, int64_t c,
+                                             int64_t nb32, int part, uint32_t h01, uint32_t h23) {
   const int64_t nsb = nb32 / 8;
   const int r = static_cast<int>(t & (kTileM - 1));
-  const int64_t tile = t / kTileM, sb = c >> 3;
-  const int half = static_cast<int>((c >> 2) & 1);
-  uint8_t *blk = aplane + a_block(tile, sb, half, nsb, kQ4);
+  uint8_t *blk = aplane + a_block(t / kTileM, c >> 3, static_cast<int>((c >> 2) & 1), nsb, kQ4);
   const int k0 = static_cast<int>(c & 3) * 32;
   *reinterpret_cast<uint2 *>(blk + operand_off(r, k0 + 4 * part)) = make_uint2(h01, h23);
-  if (part == 0) {
-    dap[t * nb32 + c] = d16f * scale;
-    if (kQ4) {
-      const float g = d16f * static_cast<float>(ssum) * scale;  // exact
-      const __half hi = __float2half_rn(g);
-      const __half lo = __float2half_rn(g - __half2float(hi));
-      uint8_t *mblk = aplane + a_block(tile, sb, 1, nsb, true) + kAMin;
-      const uint32_t pair = static_cast<uint32_t>(__half_as_ushort(hi)) |
-                            (static_cast<uint32_t>(__half_as_ushort(lo)) << 16);
-      *reinterpret_cast<uint32_t *>(mblk + min_off(r, 2 * static_cast<int>(c & 7))) = pair;
-    }
+}
+
+// One block's da' and (q4_K) min-term slots, written by one thread.
+template <bool kQ4>
+__device__ __forceinline__ void emit_scales(uint8_t *__restrict__ aplane, float *__restrict__ dap,
+                                            int64_t t, int64_t c, int64_t nb32, float d16f, int ssum,
+                                            float scale) {
+  dap[t * nb32 + c] = d16f * scale;
+  if (kQ4) {
+    const int64_t nsb = nb32 / 8;
+    const int r = static_cast<int>(t & (kTileM - 1));
+    const float g = d16f * static_cast<float>(ssum) * scale;  // exact
+    const __half hi = __float2half_rn(g);
+    const __half lo = __float2half_rn(g - __half2float(hi));
+    uint8_t *mblk = aplane + a_block(t / kTileM, c >> 3, 1, nsb, true) + kAMin;
+    const uint32_t pair = static_cast<uint32_t>(__half_as_ushort(hi)) |
+                          (static_cast<uint32_t>(__half_as_ushort(lo)) << 16);
+    *reinterpret_cast<uint32_t *>(mblk + min_off(r, 2 * static_cast<int>(c & 7))) = pair;
   }
 }
 
-// kStash (q4_K): the first pass keeps every block's results in shared memory
-// (72 B per block: 16 operand words, d16, ssum) for the second; otherwise the
-// second pass re-reads X and quantizes again.  Each warp takes 16 blocks per
-// step, four loads in flight per lane.
-constexpr int kStashBytesPerBlock = 72;
+// The operand words do not depend on the token scale s_t, so the first pass
+// writes them; q4_K's da' and min-term slots wait for s_t.  kStash (q4_K):
+// the first pass keeps every block's d16 and ssum in shared memory (8 B per
+// block) for the second; otherwise the second pass re-reads X and quantizes
+// again.  Each warp takes 16 blocks per step, four loads in flight per lane.
+constexpr int kStashBytesPerBlock = 8;
 constexpr int kStashMaxBytes = 48 * 1024;
 
 constexpr int kQuantWarps = 8;  // one step of 16 blocks per warp covers id <= 4096
@@ -360,16 +364,16 @@ __global__ void __launch_bounds__(32 * kQuantWarps) quantize_prepass_kernel(cons
                                                                uint8_t *__restrict__ aplane,
                                                                float *__restrict__ dap,
                                                                float *__restrict__ invp) {
-  extern __shared__ uint32_t stash[];  // [nb32][16] operand words, then [nb32] d16, [nb32] ssum
+  extern __shared__ float stash[];  // [nb32] d16, then [nb32] ssum
   griddep_launch_dependents();
   const int64_t t = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int part = lane & 7, grp = lane >> 3;
   const float4 *xrow = reinterpret_cast<const float4 *>(X + t * nb32 * 32);
-  float *sd16 = reinterpret_cast<float *>(stash + nb32 * 16);
-  int *sssum = reinterpret_cast<int *>(sd16 + nb32);
+  float *sd16 = stash;
+  int *sssum = reinterpret_cast<int *>(stash + nb32);
   float gmax = 0.f;
-  // pass 1 (the only one for q6_K, whose operands need no token scale)
+  // pass 1: operand words (and, for q6_K, whose operands need no token scale, everything)
   for (int64_t base = warp * 16; base < nb32; base += 16 * kQuantWarps) {
     float4 v[4];
 #pragma unroll
@@ -385,16 +389,14 @@ __global__ void __launch_bounds__(32 * kQuantWarps) quantize_prepass_kernel(cons
       int ssum;
       quant_block8(v[u], d, d16f, h01, h23, ssum);
       if (c >= nb32) continue;
+      emit_operand<kQ4>(aplane, t, c, nb32, part, h01, h23);
       if (!kQ4) {
-        emit_block<false>(aplane, dap, t, c, nb32, part, h01, h23, d16f, ssum, 1.0f);
+        if (part == 0) emit_scales<false>(aplane, dap, t, c, nb32, d16f, ssum, 1.0f);
       } else {
         gmax = fmaxf(gmax, fabsf(d16f * static_cast<float>(ssum)));
-        if (kStash) {
-          reinterpret_cast<uint2 *>(stash + c * 16)[part] = make_uint2(h01, h23);
-          if (part == 0) {
-            sd16[c] = d16f;
-            sssum[c] = ssum;
-          }
+        if (kStash && part == 0) {
+          sd16[c] = d16f;
+          sssum[c] = ssum;
         }
       }
     }
@@ -417,12 +419,10 @@ __global__ void __launch_bounds__(32 * kQuantWarps) quantize_prepass_kernel(cons
   }
   const float scale = __uint_as_float(static_cast<uint32_t>(127 + s) << 23);
   if (tid == 0) invp[t] = __uint_as_float(static_cast<uint32_t>(127 - s) << 23);
-  // pass 2
+  // pass 2: da' and the min-term slots
   if (kStash) {
-    for (int64_t c = tid >> 3; c < nb32; c += 4 * kQuantWarps) {
-      const uint2 hw = reinterpret_cast<const uint2 *>(stash + c * 16)[part];
-      emit_block<true>(aplane, dap, t, c, nb32, part, hw.x, hw.y, sd16[c], sssum[c], scale);
-    }
+    for (int64_t c = tid; c < nb32; c += 32 * kQuantWarps)
+      emit_scales<true>(aplane, dap, t, c, nb32, sd16[c], sssum[c], scale);
   } else {
     for (int64_t base = warp * 16; base < nb32; base += 16 * kQuantWarps) {
       float4 v[4];
@@ -438,7 +438,7 @@ __global__ void __launch_bounds__(32 * kQuantWarps) quantize_prepass_kernel(cons
         uint32_t h01, h23;
         int ssum;
         quant_block8(v[u], d, d16f, h01, h23, ssum);
-        if (c < nb32) emit_block<true>(aplane, dap, t, c, nb32, part, h01, h23, d16f, ssum, scale);
+        if (c < nb32 && part == 0) emit_scales<true>(aplane, dap, t, c, nb32, d16f, ssum, scale);
       }
     }
   }

@@ -256,7 +256,8 @@ def test_repeat_calls_are_deterministic(mmq):
     ("q6_K", 300, 768, 200, 22),
     ("q4_K", 3584, 3584, 512, 23),
     ("q6_K", 1000, 4096, 300, 24),
-    ("q4_K", 130, 22016, 70, 25),   # too many blocks per token to stash: two passes over X
+    ("q4_K", 130, 22016, 70, 25),   # 688 blocks per token, stashed
+    ("q4_K", 64, 196864, 5, 26),    # 6152 blocks per token, past the stash: two passes over X
 ])
 def test_gemm_f32_matches_quantize_then_gemm(mmq, name, od, id_, nt, seed):
     W = gen.weights(name, od, id_, seed=300 + seed)
