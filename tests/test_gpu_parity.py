@@ -207,6 +207,69 @@ def test_zero_and_constant_activations(mmq):
     assert err <= bound
 
 
+def _fp16_bits(v):
+    return np.frombuffer(np.float16(v).tobytes(), dtype=np.uint8)
+
+
+def test_extreme_weight_blocks(mmq):
+    """The exactness boundary of the fp16 operands and extreme block scales:
+    q6_K sub-block scales of exactly +-64 with codes 0 and 63 give |sc*(q-32)|
+    up to 2048; q4_K scales and mins of 63 with codes 15; d and dmin at the
+    fp16 maximum, at a subnormal and at zero."""
+    od, id_, nt = 160, 768, 130
+    X = gen.activations(nt, id_, seed=61, outlier_p=0.02, outlier_scale=30.0)
+    Q_ref = oracle.quantize_q8_0(X)
+    rng = np.random.default_rng(62)
+    # q6_K: 210-byte blocks, ql @0, qh @128, sc @192 (int8), d @208
+    W6 = gen.weights("q6_K", od, id_, seed=63).reshape(-1, 210).copy()
+    n = W6.shape[0]
+    W6[:, 192:208] = np.where(rng.random((n, 16)) < 0.5, 64, np.uint8(np.int8(-64).view(np.uint8)))
+    W6[0::3, 0:192] = 0xFF       # q = 63
+    W6[1::3, 0:192] = 0x00       # q = 0: q - 32 = -32, |sc (q - 32)| = 2048
+    # d: the fp16 maximum (on blocks with small codes, so |Y| stays finite), a
+    # subnormal, zero, and the generator's values elsewhere
+    W6[0::20, 208:210] = _fp16_bits(65504.0)
+    W6[0::20, 0:192] = 0x22
+    W6[5::20, 208:210] = _fp16_bits(6e-8)
+    W6[10::20, 208:210] = _fp16_bits(0.0)
+    W6 = W6.reshape(-1)
+    # q4_K: 144-byte blocks, d @0, dmin @2, packed scales/mins @4, qs @16
+    W4 = gen.weights("q4_K", od, id_, seed=64).reshape(-1, 144).copy()
+    W4[0::2, 4:16] = 0xFF        # every 6-bit scale and min = 63
+    W4[0::4, 16:144] = 0xFF      # codes 15
+    W4[1::4, 16:144] = 0x00      # codes 0: only the min term
+    for i, (dv, mv) in enumerate([(65504.0, 0.0), (0.0, 2.0), (6e-8, 6e-8), (1e-3, 65504.0)]):
+        W4[i::20, 0:2] = _fp16_bits(dv)
+        W4[i::20, 2:4] = _fp16_bits(mv)
+    big4 = (W4[:, 0:2].view(np.uint16)[:, 0] == 0x7BFF) | (W4[:, 2:4].view(np.uint16)[:, 0] == 0x7BFF)
+    W4[big4, 4:16] = 0x41        # small scales and mins there
+    W4 = W4.reshape(-1)
+    for name, W in (("q6_K", W6), ("q4_K", W4)):
+        _, Q, Y, _ = _run(mmq, name, W, od, id_, X)
+        assert np.array_equal(Q, Q_ref)
+        Y_ref = oracle.gemm(QT[name], W, od, id_, Q_ref, nt)
+        assert np.isfinite(Y_ref).all()
+        # the task's bound, applied per weight row (stricter than over all of Y,
+        # whose maximum the fp16-maximum blocks dominate)
+        err = np.abs(Y.astype(np.float64) - Y_ref).max(axis=0)
+        bound = RTOL_MAX * np.abs(Y_ref).max(axis=0) + ATOL
+        assert (err <= bound).all(), (name, int(np.argmax(err - bound)))
+
+
+def test_many_token_tiles(mmq):
+    """nt = 16384: 128 token tiles, persistent CTAs over many tiles, sampled."""
+    od, id_, nt = 256, 512, 16384
+    W = gen.weights("q4_K", od, id_, seed=71)
+    X = gen.activations(nt, id_, seed=72)
+    _, Q, Y, _ = _run(mmq, "q4_K", W, od, id_, X)
+    Q_ref = oracle.quantize_q8_0(X)
+    assert np.array_equal(Q, Q_ref)
+    ts, os_ = _sample_entries(nt, od, 4000, 73)
+    y_ref = oracle.gemm_entries(oracle.Q4_K, W, od, id_, Q_ref, nt, ts, os_)
+    err, bound = _within_tol(Y[ts, os_], y_ref)
+    assert err <= bound, (err, bound)
+
+
 def test_bounded_wait_reports_and_context_survives(mmq):
     rc = mmq.mmq_selftest_wait_timeout(50_000_000)  # 50 ms, nothing ever arrives
     assert rc == mmq.mmq.MMQ_ERR_DEVICE_TIMEOUT
