@@ -425,29 +425,53 @@ def run_mine(args, cfg, rank, world):
         Xh = [torch.from_numpy(gen.activations(nt, id_, seed + 7 * i, cfg.sigma, cfg.outlier_p,
                                                cfg.outlier_scale)).pin_memory()
               for i in range(2)]
-        Yh = torch.empty((nt, od), dtype=torch.float32).pin_memory()
+        Yh = [torch.empty((nt, od), dtype=torch.float32).pin_memory() for _ in range(2)]
+        # Three streams, pipelined across steps: step i's host->device copy
+        # runs while step i-1 computes and step i-2's result goes back.  Every
+        # step still copies its own input in and its own result out.
+        s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+        done_c = [torch.cuda.Event() for _ in range(n_sets)]  # compute of the last step on set j
+        done_o = [torch.cuda.Event() for _ in range(n_sets)]  # read-back of the last step on set j
+        started = [False] * n_sets
 
         def e2e_step(i):
             j = i % n_sets
-            Xs[j].copy_(Xh[i % 2], non_blocking=True)
-            if fused:
-                mmq.mmq_gemm_f32(ws[j], Xs[j], Ys[j])
-            else:
-                mmq.mmq_quantize_act(Xs[j], Qs[j])
-                mmq.mmq_gemm(ws[j], Qs[j], nt, Ys[j])
-            Yh.copy_(Ys[j], non_blocking=True)
+            ev_in = torch.cuda.Event()
+            with torch.cuda.stream(s_in):
+                if started[j]:
+                    s_in.wait_event(done_c[j])  # set j's X is free once its last step computed
+                Xs[j].copy_(Xh[i % 2], non_blocking=True)
+                ev_in.record()
+            with torch.cuda.stream(stream):
+                stream.wait_event(ev_in)
+                if started[j]:
+                    stream.wait_event(done_o[j])  # set j's Y is free once read back
+                if fused:
+                    mmq.mmq_gemm_f32(ws[j], Xs[j], Ys[j])
+                else:
+                    mmq.mmq_quantize_act(Xs[j], Qs[j])
+                    mmq.mmq_gemm(ws[j], Qs[j], nt, Ys[j])
+                done_c[j].record()
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(done_c[j])
+                Yh[i % 2].copy_(Ys[j], non_blocking=True)
+                done_o[j].record()
+            started[j] = True
 
-        with torch.cuda.stream(stream):
-            for i in range(3):
-                e2e_step(i)
-        stream.synchronize()
+        for i in range(3):
+            e2e_step(i)
+        torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
             e0.record()
-            for i in range(E):
-                e2e_step(i)
+        for st in (s_in, s_out):
+            st.wait_event(e0)
+        for i in range(E):
+            e2e_step(i)
+        with torch.cuda.stream(stream):
+            stream.wait_stream(s_out)
             e1.record()
-        stream.synchronize()
+        torch.cuda.synchronize()
         e_ms = e0.elapsed_time(e1)
         if world > 1:
             t = torch.tensor([e_ms], device=dev, dtype=torch.float64)
@@ -457,7 +481,8 @@ def run_mine(args, cfg, rank, world):
                "h2d_bytes_per_step": nt * id_ * 4, "d2h_bytes_per_step": nt * od * 4,
                "steps": E, "ms_per_step": e_ms / E,
                "path": ("pinned host X -> device, mmq_gemm_f32, Y -> pinned host" if fused else
-                        "pinned host X -> device, mmq_quantize_act, mmq_gemm, Y -> pinned host")}
+                        "pinned host X -> device, mmq_quantize_act, mmq_gemm, Y -> pinned host"),
+               "overlap": "copies in, compute and copies out on three streams, pipelined across steps"}
 
     # ---- the oracle on the host cores (rank 0, N = 1 only)
     cpu = None
