@@ -27,20 +27,28 @@
 // super-block of the weight scales (d, dmin) into a 4-entry scale ring that
 // the epilogue releases.
 //
-// Kernel shape: persistent, one CTA of 384 threads per SM, 128 x 128 tiles,
-// token tiles fastest so concurrently running CTAs share weight tiles in L2.
+// Kernel shape: persistent, one CTA of 384 threads per SM (512 for the raw
+// arm), 128 x 128 tiles, token tiles fastest so concurrently running CTAs
+// share weight tiles in L2; whole tiles per CTA, or (few tiles, many
+// super-blocks) the stream-K split below.
 //   warps 0..7  epilogue: warp w reads TMEM lanes 32*(w%4).. and columns
-//               64*(w/4)..: TMEM -> registers (one 64-column load per chunk)
-//               -> packed fp32x2 FMAs
+//               64*(w/4)..: TMEM -> registers in 32-column halves,
+//               software-pipelined with packed fp32x2 FMAs; one barrier wait
+//               per pair of chunks
 //   warp 8      producer: lane 0 the activation block, lane 1 the weight
 //               block, lane 2 the scale block
-//   warp 9      TMEM owner + UMMA issuer (one elected lane of a warp-uniform
-//               loop): per 32-K chunk two 128x128x16 UMMAs into one of four
-//               TMEM chunk slots, committed per chunk; the slots go in two
-//               groups of two, and a group is refilled as soon as the
-//               epilogue has loaded both of its chunks into registers
-//               (+ the min-term UMMA per q4_K super-block, in a group alone)
-//   warps 10-11 idle (complete the register-donating warpgroup)
+//   warps 9-10  UMMA issuers (one elected lane of a warp-uniform loop each);
+//               warp 9 also owns TMEM.  The eight 32-K chunks of a super-block
+//               go in pairs, (0,1) and (4,5) to issuer 0, (2,3) and (6,7) to
+//               issuer 1; each issuer has two of the four 128-column TMEM chunk
+//               slots and commits every chunk on its slot's barrier (a commit
+//               covers all earlier UMMAs of its thread, so a pair's second
+//               barrier covers the pair); issuer 0 also issues the q4_K
+//               min-term UMMA per super-block
+//   warp 11     pulls the first weight blocks into L2 at launch
+//   warps 12-15 (raw arm) converters: packed weight bytes -> fp16 operand
+// The launch is programmatic: the producer and the epilogue wait for the
+// prepass kernel just before their first read of its output.
 // Every wait is bounded (ptx.cuh); a CTA that gives up drains its own copies
 // and UMMAs, frees TMEM and returns.
 #include <cuda_fp16.h>
