@@ -167,6 +167,24 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(use), "samples_in_timed_region": len(inwin)}
 
 
+def _max_over_ranks(x: float, world: int, device) -> float:
+    """The largest x over the ranks of the process group (x itself at world 1):
+    the job's time is its slowest rank's."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _job_tops(world: int, ops_per_step: float, steps: int, ms: float) -> float:
+    """Whole-job throughput: every rank runs `steps` steps of `ops_per_step`
+    (weak scaling) in `ms`, the slowest rank's time."""
+    return world * ops_per_step * steps / (ms * 1e-3) / 1e12
+
+
 def _gpu_uuid(dev):
     import torch
     try:
@@ -394,13 +412,10 @@ def run_mine(args, cfg, rank, world):
     elapsed_ms = ev_all0.elapsed_time(ev_all1)
     gemm_ms = [a.elapsed_time(b) for a, b in evs]
     gemm_avg_ms = sum(gemm_ms) / len(gemm_ms)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = _max_over_ranks(elapsed_ms, world, dev)
 
     ops = cfg.ops
-    value = world * ops * K / (elapsed_ms * 1e-3) / 1e12
+    value = _job_tops(world, ops, K, elapsed_ms)
     tokens_per_s = world * nt * K / (elapsed_ms * 1e-3)
 
     # ---- roofline of the GEMM kernel (tensor-bound: fp16 UMMA carrying exact integers)
@@ -473,11 +488,8 @@ def run_mine(args, cfg, rank, world):
             e1.record()
         torch.cuda.synchronize()
         e_ms = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([e_ms], device=dev, dtype=torch.float64)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": world * ops * E / (e_ms * 1e-3) / 1e12, "unit": UNIT,
+        e_ms = _max_over_ranks(e_ms, world, dev)
+        e2e = {"value": _job_tops(world, ops, E, e_ms), "unit": UNIT,
                "h2d_bytes_per_step": nt * id_ * 4, "d2h_bytes_per_step": nt * od * 4,
                "steps": E, "ms_per_step": e_ms / E,
                "path": ("pinned host X -> device, mmq_gemm_f32, Y -> pinned host" if fused else
