@@ -94,6 +94,12 @@ typedef struct mmq_weights_s *mmq_weights_t;
                               memory inside the GEMM ("47 · r44 — W_exp stride mismatch
                               root cause", §3.2: the in-kernel recombination); needs a
                               handle registered with MMQ_REG_RAW; bit-identical to F16 */
+#define MMQ_ARM_SPLIT 3    /* the activation scale folded into the A operand as an exact
+                              fp16 pair (hi = rn(da'*qs), lo = rn(da'*qs - hi)), so the
+                              tensor core sums a whole 256-K super-block and the scales
+                              apply once per super-block: every product exact, fp32
+                              summation (results within the GEMM tolerance, not
+                              bit-identical to F16); whole tiles per CTA */
 
 /*
  * mmq_quantize_act -- q8_0 quantization of activations.

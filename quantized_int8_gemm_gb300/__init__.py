@@ -8,6 +8,7 @@ from .mmq import (  # noqa: F401
     MMQ_ARM_AUTO,
     MMQ_ARM_F16,
     MMQ_ARM_RAW,
+    MMQ_ARM_SPLIT,
     MMQ_OUT_F16,
     MMQ_OUT_F32,
     MMQ_Q4_K,

@@ -232,10 +232,11 @@ static int gemm_impl(mmq_weights_t h, const void *Q, const float *X, int64_t nt,
                      mmq_stream_t stream, uint32_t flags, int *arm_used, cudaEvent_t ev0,
                      cudaEvent_t ev1) {
   if (!h || nt < 0 || nt > kMaxTokens) return MMQ_ERR_ARG;
-  if (flags != MMQ_ARM_AUTO && flags != MMQ_ARM_F16 && flags != MMQ_ARM_RAW) return MMQ_ERR_UNSUPPORTED;
+  if (flags != MMQ_ARM_AUTO && flags != MMQ_ARM_F16 && flags != MMQ_ARM_RAW && flags != MMQ_ARM_SPLIT)
+    return MMQ_ERR_UNSUPPORTED;
   if (flags == MMQ_ARM_RAW && !h->rawplane) return MMQ_ERR_UNSUPPORTED;
-  const bool raw = flags == MMQ_ARM_RAW;
-  if (arm_used) *arm_used = raw ? MMQ_ARM_RAW : MMQ_ARM_F16;
+  const bool raw = flags == MMQ_ARM_RAW, split = flags == MMQ_ARM_SPLIT;
+  if (arm_used) *arm_used = raw ? MMQ_ARM_RAW : split ? MMQ_ARM_SPLIT : MMQ_ARM_F16;
   if (nt == 0) return MMQ_OK;
   const void *A = X ? static_cast<const void *>(X) : Q;
   if (!A || !Y) return MMQ_ERR_ARG;
@@ -252,15 +253,19 @@ static int gemm_impl(mmq_weights_t h, const void *Q, const float *X, int64_t nt,
   cudaError_t e = cudaStreamIsCapturing(s, &cap);
   if (e != cudaSuccess) return cuda_rc(e);
   const bool capturing = cap == cudaStreamCaptureStatusActive;
-  const size_t bytes = mmq::gemm_scratch_bytes(h, nt, true, raw);
+  const size_t bytes = split ? mmq::gemm_split_scratch_bytes(h, nt) : mmq::gemm_scratch_bytes(h, nt, true, raw);
   void *scratch = nullptr;
   e = capturing ? cudaMallocAsync(&scratch, bytes, s)
                 : cudaMallocFromPoolAsync(&scratch, bytes, d->pool, s);
   if (e != cudaSuccess) return cuda_rc(e);
   // inside a capture the events must become real record nodes of the graph
   const unsigned ev_flags = capturing ? cudaEventRecordExternal : cudaEventRecordDefault;
-  e = mmq::launch_gemm(h, static_cast<const uint8_t *>(Q), X, nt, Y, scratch, true, raw,
-                       d->words, next_epoch(), g_limit_ns.load(), s, ev0, ev1, ev_flags);
+  if (split)
+    e = mmq::launch_gemm_split(h, static_cast<const uint8_t *>(Q), X, nt, Y, scratch, d->words, next_epoch(),
+                               g_limit_ns.load(), s, ev0, ev1, ev_flags);
+  else
+    e = mmq::launch_gemm(h, static_cast<const uint8_t *>(Q), X, nt, Y, scratch, true, raw,
+                         d->words, next_epoch(), g_limit_ns.load(), s, ev0, ev1, ev_flags);
   cudaError_t ef = cudaFreeAsync(scratch, s);
   if (e == cudaSuccess) e = ef;
   return cuda_rc(e);

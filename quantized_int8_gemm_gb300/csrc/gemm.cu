@@ -453,6 +453,184 @@ __global__ void __launch_bounds__(32 * kQuantWarps) quantize_prepass_kernel(cons
   }
 }
 
+// ---------------------------------------------------------------- split-arm prepass
+// The split arm's activation blocks (tiling.h): a = d16 * 2^s_t * q, exact in
+// fp32 (11 x 7 significant bits), travels as fp16 hi = rn(a), lo = rn(a - hi).
+// The pair is exact while |a| >= 2^-7 (lo keeps its bits above the fp16
+// subnormal step), i.e. for every block within 2^22 of the token's largest.
+// s_t puts the token's largest |d16 * 127| and (q4_K) |d16 * ssum| in
+// [2^14, 2^15), so hi, lo and the min-term g' stay in fp16 range; inv = 2^-s_t.
+__device__ __forceinline__ int split_scale_exp(float m) {
+  if (!(m > 0.f)) return 0;
+  const int e = static_cast<int>((__float_as_uint(m) >> 23) & 0xFF) - 127;
+  return min(30, max(-30, 14 - e));
+}
+
+// two fp16 integers (one word) times da_s -> hi word and lo word
+__device__ __forceinline__ void split_word(uint32_t hq, float da_s, uint32_t &hi, uint32_t &lo) {
+  const __half2 q2 = *reinterpret_cast<const __half2 *>(&hq);
+  const float a0 = da_s * __low2float(q2), a1 = da_s * __high2float(q2);  // exact
+  const __half h0 = __float2half_rn(a0), h1 = __float2half_rn(a1);
+  const __half l0 = __float2half_rn(a0 - __half2float(h0)), l1 = __float2half_rn(a1 - __half2float(h1));
+  hi = static_cast<uint32_t>(__half_as_ushort(h0)) | (static_cast<uint32_t>(__half_as_ushort(h1)) << 16);
+  lo = static_cast<uint32_t>(__half_as_ushort(l0)) | (static_cast<uint32_t>(__half_as_ushort(l1)) << 16);
+}
+
+// Lane `part` of block c's eight: its 4 values into the hi and lo images, and
+// (part 0, q4_K) the block's min-term slots.
+template <bool kQ4>
+__device__ __forceinline__ void emit_split(uint8_t *__restrict__ aplane, int64_t t, int64_t c, int64_t nb32,
+                                           int part, uint32_t h01, uint32_t h23, float d16f, int ssum,
+                                           float scale) {
+  const int64_t nsb = nb32 / 8;
+  const int r = static_cast<int>(t & (kTileM - 1));
+  uint8_t *blk = aplane + as_block(t / kTileM, c >> 3, static_cast<int>((c >> 2) & 1), nsb, kQ4);
+  const uint32_t off = split_off(r, static_cast<int>(c & 3) * 32 + 4 * part);
+  const float da_s = d16f * scale;
+  uint32_t hi0, lo0, hi1, lo1;
+  split_word(h01, da_s, hi0, lo0);
+  split_word(h23, da_s, hi1, lo1);
+  *reinterpret_cast<uint2 *>(blk + off) = make_uint2(hi0, hi1);
+  *reinterpret_cast<uint2 *>(blk + kSplitLo + off) = make_uint2(lo0, lo1);
+  if (kQ4 && part == 0) {
+    const float g = d16f * static_cast<float>(ssum) * scale;  // exact to fp32
+    const __half hi = __float2half_rn(g);
+    const __half lo = __float2half_rn(g - __half2float(hi));
+    uint8_t *mblk = aplane + as_block(t / kTileM, c >> 3, 1, nsb, true) + kSplitMin;
+    *reinterpret_cast<uint32_t *>(mblk + min_off(r, 2 * static_cast<int>(c & 7))) =
+        static_cast<uint32_t>(__half_as_ushort(hi)) | (static_cast<uint32_t>(__half_as_ushort(lo)) << 16);
+  }
+}
+
+// the largest value the token's scale has to keep in range, for one block
+template <bool kQ4>
+__device__ __forceinline__ float split_range(float d16f, int ssum) {
+  const float m = d16f * 127.0f;
+  return kQ4 ? fmaxf(m, fabsf(d16f * static_cast<float>(ssum))) : m;
+}
+
+constexpr int kSplitStashBytesPerBlock = 72;  // 16 words of fp16 q, d16, ssum
+
+// From fp32 X: one CTA of eight warps per token, eight lanes per block; the
+// first pass quantizes (q8_0, as quantize.cu) and keeps each block in shared
+// memory (kStash) for the second, or the second quantizes again.
+template <bool kQ4, bool kStash>
+__global__ void __launch_bounds__(32 * kQuantWarps) split_prepass_f32_kernel(const float *__restrict__ X,
+                                                                   int64_t nt, int64_t nb32,
+                                                                   uint8_t *__restrict__ aplane,
+                                                                   float *__restrict__ invp) {
+  extern __shared__ uint32_t sstash[];  // [nb32][16] fp16 q words, then [nb32] d16, [nb32] ssum
+  griddep_launch_dependents();
+  const int64_t t = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int part = lane & 7, grp = lane >> 3;
+  const float4 *xrow = reinterpret_cast<const float4 *>(X + t * nb32 * 32);
+  float *sd16 = reinterpret_cast<float *>(sstash + nb32 * 16);
+  int *sssum = reinterpret_cast<int *>(sd16 + nb32);
+  float gmax = 0.f;
+  for (int64_t base = warp * 16; base < nb32; base += 16 * kQuantWarps) {
+    float4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t c = base + u * 4 + grp;
+      v[u] = c < nb32 ? __ldg(xrow + c * 8 + part) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t c = base + u * 4 + grp;
+      float d, d16f;
+      uint32_t h01, h23;
+      int ssum;
+      quant_block8(v[u], d, d16f, h01, h23, ssum);
+      if (c >= nb32) continue;
+      gmax = fmaxf(gmax, split_range<kQ4>(d16f, ssum));
+      if (kStash) {
+        reinterpret_cast<uint2 *>(sstash + c * 16)[part] = make_uint2(h01, h23);
+        if (part == 0) {
+          sd16[c] = d16f;
+          sssum[c] = ssum;
+        }
+      }
+    }
+  }
+  __shared__ float wmax[kQuantWarps];
+#pragma unroll
+  for (int m = 16; m; m >>= 1) gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, m));
+  if (lane == 0) wmax[warp] = gmax;
+  __syncthreads();
+#pragma unroll
+  for (int w = 0; w < kQuantWarps; ++w) gmax = fmaxf(gmax, wmax[w]);
+  const int s = split_scale_exp(gmax);
+  const float scale = __uint_as_float(static_cast<uint32_t>(127 + s) << 23);
+  if (tid == 0) invp[t] = __uint_as_float(static_cast<uint32_t>(127 - s) << 23);
+  if (kStash) {
+    for (int64_t c = tid >> 3; c < nb32; c += 4 * kQuantWarps) {
+      const uint2 hw = reinterpret_cast<const uint2 *>(sstash + c * 16)[part];
+      emit_split<kQ4>(aplane, t, c, nb32, part, hw.x, hw.y, sd16[c], sssum[c], scale);
+    }
+  } else {
+    for (int64_t base = warp * 16; base < nb32; base += 16 * kQuantWarps) {
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int64_t c = base + u * 4 + grp;
+        v[u] = c < nb32 ? __ldg(xrow + c * 8 + part) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int64_t c = base + u * 4 + grp;
+        float d, d16f;
+        uint32_t h01, h23;
+        int ssum;
+        quant_block8(v[u], d, d16f, h01, h23, ssum);
+        if (c < nb32) emit_split<kQ4>(aplane, t, c, nb32, part, h01, h23, d16f, ssum, scale);
+      }
+    }
+  }
+}
+
+// From pad40 q8_0 blocks: one CTA of 128 threads per token.
+template <bool kQ4>
+__global__ void __launch_bounds__(128) split_prepass_q_kernel(const uint8_t *__restrict__ Q, int64_t nt,
+                                                              int64_t nb32, uint8_t *__restrict__ aplane,
+                                                              float *__restrict__ invp) {
+  griddep_launch_dependents();
+  const int64_t t = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint8_t *qrow = Q + t * nb32 * 40;
+  float gmax = 0.f;
+  for (int64_t c = tid; c < nb32; c += 128) {
+    const uint8_t *b = qrow + c * 40;
+    const float d16f = __half2float(*reinterpret_cast<const __half *>(b));
+    gmax = fmaxf(gmax, split_range<kQ4>(d16f, *reinterpret_cast<const int *>(b + 36)));
+  }
+  __shared__ float wmax[4];
+#pragma unroll
+  for (int m = 16; m; m >>= 1) gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, m));
+  if (lane == 0) wmax[warp] = gmax;
+  __syncthreads();
+  gmax = fmaxf(fmaxf(wmax[0], wmax[1]), fmaxf(wmax[2], wmax[3]));
+  const int s = split_scale_exp(gmax);
+  const float scale = __uint_as_float(static_cast<uint32_t>(127 + s) << 23);
+  if (tid == 0) invp[t] = __uint_as_float(static_cast<uint32_t>(127 - s) << 23);
+  const int part = tid & 7;
+  for (int64_t c = tid >> 3; c < nb32; c += 16) {
+    const uint8_t *b = qrow + c * 40;
+    const float d16f = __half2float(*reinterpret_cast<const __half *>(b));
+    const int ssum = *reinterpret_cast<const int *>(b + 36);
+    const uint32_t q4b = *reinterpret_cast<const uint32_t *>(b + 4 + 4 * part);
+    uint32_t h[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int q0 = static_cast<int8_t>((q4b >> (16 * j)) & 0xFF);
+      const int q1 = static_cast<int8_t>((q4b >> (16 * j + 8)) & 0xFF);
+      h[j] = static_cast<uint32_t>(__half_as_ushort(__int2half_rn(q0))) |
+             (static_cast<uint32_t>(__half_as_ushort(__int2half_rn(q1))) << 16);
+    }
+    emit_split<kQ4>(aplane, t, c, nb32, part, h[0], h[1], d16f, ssum, scale);
+  }
+}
+
 // ---------------------------------------------------------------- the GEMM
 // acc[h*16 ..] = da * S (first chunk of a super-block) or += da * S, on one
 // 32-column half h of a chunk.
@@ -527,6 +705,39 @@ __device__ __forceinline__ void st_global_v8(float *p, float2 a, float2 b, float
   asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "f"(a.x), "f"(a.y),
                "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y), "f"(d.x), "f"(d.y)
                : "memory");
+}
+
+// The 64 outputs of one thread (row t, columns o0 .. o0 + 63) times inv.
+__device__ __forceinline__ void store_y_row(float *__restrict__ Y, int64_t t, int64_t od, int64_t o0,
+                                            const float2 (&y)[32], float inv) {
+  const float2 inv2 = make_float2(inv, inv);
+  float *yrow = Y + t * od + o0;
+  if ((od & 7) == 0 && (reinterpret_cast<uintptr_t>(Y) & 31) == 0) {
+    // 32-byte stores: each row segment of a warp's store is a whole sector
+#pragma unroll
+    for (int i = 0; i < 32; i += 4) {
+      if (o0 + 2 * i < od) {
+        const float2 a = __fmul2_rn(y[i], inv2), b = __fmul2_rn(y[i + 1], inv2);
+        const float2 c = __fmul2_rn(y[i + 2], inv2), d = __fmul2_rn(y[i + 3], inv2);
+        st_global_v8(yrow + 2 * i, a, b, c, d);
+      }
+    }
+  } else if ((od & 3) == 0) {
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+      if (o0 + 2 * i < od) {
+        const float2 a = __fmul2_rn(y[i], inv2), b = __fmul2_rn(y[i + 1], inv2);
+        *reinterpret_cast<float4 *>(yrow + 2 * i) = make_float4(a.x, a.y, b.x, b.y);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float2 a = __fmul2_rn(y[i], inv2);
+      if (o0 + 2 * i < od) yrow[2 * i] = a.x;
+      if (o0 + 2 * i + 1 < od) yrow[2 * i + 1] = a.y;
+    }
+  }
 }
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
@@ -973,37 +1184,263 @@ __global__ void __launch_bounds__(Shape<kRaw>::kThreads, 1)
         }
         if (!ok) break;
       }
-      if (t < nt) {
-        const float inv = __ldg(invp + t);
-        const float2 inv2 = make_float2(inv, inv);
-        float *yrow = Y + t * od + o0;
-        if ((od & 7) == 0 && (reinterpret_cast<uintptr_t>(Y) & 31) == 0) {
-          // 32-byte stores: each row segment of a warp's store is a whole sector
-#pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            if (o0 + 2 * i < od) {
-              const float2 a = __fmul2_rn(y[i], inv2), b = __fmul2_rn(y[i + 1], inv2);
-              const float2 c = __fmul2_rn(y[i + 2], inv2), d = __fmul2_rn(y[i + 3], inv2);
-              st_global_v8(yrow + 2 * i, a, b, c, d);
-            }
+      if (t < nt) store_y_row(Y, t, od, o0, y, __ldg(invp + t));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == ISSUER_WARP) {
+    tc_fence_after();
+    tmem_dealloc(tbase, TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------- the split arm's GEMM
+// Same tiles, operands and roles as mmq_gemm_kernel, with the activation scale
+// folded into A (hi + lo images, tiling.h): per 32-K chunk four 128x128x16
+// UMMAs (hi and lo, two K halves each) accumulate into one TMEM region for the
+// whole super-block, so the epilogue runs once per super-block:
+//   y[t][o] += d[o][sb] * ACC[t][o][sb]  -  dmin[o][sb] * MIN[t][o][sb]
+// Regions (128 columns each): q6_K four accumulators; q4_K two accumulators
+// (columns 0..255) each with its min-term region 256 columns on.  Stages of
+// 64 K (hi and lo activation K-blocks, one weight K-block, and in the last
+// quarter of a q4_K super-block the two min images); one issuer; whole tiles
+// per CTA.
+template <bool kQ4>
+struct SplitSmem {
+  static constexpr int kStages = kQ4 ? 3 : 4;
+  static constexpr int kA = kSplitQuarter + (kQ4 ? kMinBytes : 0);
+  static constexpr int kB = ((kTileN * 64 * 2 + (kQ4 ? kMinBytes : 0) + 1023) / 1024) * 1024;
+  static constexpr int kBK = kTileN * 64 * 2;  // one weight K-block: 16384
+  static constexpr int kStage = kA + kB;
+  static constexpr int kScale = scale_block_bytes(kQ4);
+  static constexpr int kScaleRing = kStages * kStage;
+  static constexpr int kRegions = kQ4 ? 2 : 4;
+  static constexpr int kBar = kScaleRing + SRING * kScale;
+  // full, empty per stage; rfull, rempty per region; sfull, sempty per scale entry; done
+  static constexpr int kNumBars = 2 * kStages + 2 * kRegions + 2 * SRING + 1;
+  static constexpr int kSlot = kBar + kNumBars * 8;
+  static constexpr int kBytes = kSlot + 16 + 1024;
+  static_assert(kA % 1024 == 0 && kStage % 1024 == 0, "stage buffers must keep 1 KB alignment");
+  static_assert(kBytes <= 227 * 1024, "shared memory budget");
+};
+
+template <bool kQ4>
+__global__ void __launch_bounds__(Shape<false>::kThreads, 1)
+    mmq_gemm_split_kernel(const uint8_t *__restrict__ aplane, const uint8_t *__restrict__ bplane,
+                          const uint8_t *__restrict__ bscale, const float *__restrict__ invp, int64_t nt,
+                          int64_t od, int64_t nb32, int n_tt, int n_ot, float *__restrict__ Y, WaitCtl wctl) {
+  using L = SplitSmem<kQ4>;
+  using S = Shape<false>;
+  constexpr int STAGES = L::kStages, NR = L::kRegions;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t *smem = smem_raw + (base - raw);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t nsb = nb32 / 8;
+  const int n_tiles = n_tt * n_ot;
+
+  const uint32_t bar = base + L::kBar;
+  auto full = [&](int s) { return bar + 8u * s; };
+  auto empty = [&](int s) { return bar + 8u * (STAGES + s); };
+  auto rfull = [&](int r) { return bar + 8u * (2 * STAGES + r); };
+  auto rempty = [&](int r) { return bar + 8u * (2 * STAGES + NR + r); };
+  auto sfull = [&](int e) { return bar + 8u * (2 * STAGES + 2 * NR + e); };
+  auto sempty = [&](int e) { return bar + 8u * (2 * STAGES + 2 * NR + SRING + e); };
+  const uint32_t done = bar + 8u * (2 * STAGES + 2 * NR + 2 * SRING);
+  auto a_smem = [&](int s) { return base + s * L::kStage; };
+  auto b_smem = [&](int s) { return base + s * L::kStage + L::kA; };
+  auto s_smem = [&](int e) { return base + L::kScaleRing + e * L::kScale; };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    for (int r = 0; r < NR; ++r) {
+      mbar_init(rfull(r), 1);
+      mbar_init(rempty(r), EPI_WARPS);
+    }
+    for (int e = 0; e < SRING; ++e) {
+      mbar_init(sfull(e), 1);
+      mbar_init(sempty(e), EPI_WARPS);
+    }
+    mbar_init(done, 1);
+    fence_mbar_init();
+  }
+  if (warp == ISSUER_WARP) {
+    tmem_alloc(base + L::kSlot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *reinterpret_cast<volatile uint32_t *>(smem + L::kSlot);
+  if (warp >= PRODUCER_WARP) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(S::kRegsCtl));
+  if (warp == PRODUCER_WARP) {
+    // ------------------------------------------------------------ producer
+    griddep_wait();  // the activation blocks come from the kernel before this one
+    uint32_t ks = 0, ns = 0, issued = 0, s_issued = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+      const int tt = tile % n_tt, ot = tile / n_tt;
+      for (int64_t sb = 0; sb < nsb && ok; ++sb, ++ns) {
+        const int e = static_cast<int>(ns % SRING);
+        ok = __all_sync(0xffffffffu, mbar_wait(sempty(e), ((ns / SRING) & 1) ^ 1, wctl));
+        if (!ok) break;
+        if (lane == 2) {
+          mbar_arrive_expect_tx(sfull(e), L::kScale);
+          bulk_load(s_smem(e), bscale + b_scale_block(ot, sb, nsb, kQ4), L::kScale, sfull(e));
+        }
+        __syncwarp();
+        s_issued = ns + 1;
+        for (int qq = 0; qq < 4; ++qq, ++ks) {  // 64-K quarters of the super-block
+          const int s = static_cast<int>(ks % STAGES);
+          ok = __all_sync(0xffffffffu, mbar_wait(empty(s), ((ks / STAGES) & 1) ^ 1, wctl));
+          if (!ok) break;
+          const int half = qq >> 1, kb = qq & 1;
+          const bool mins = kQ4 && qq == 3;
+          const uint8_t *ablk = aplane + as_block(tt, sb, half, nsb, kQ4);
+          const uint8_t *bblk = bplane + b_block(ot, sb, half, nsb, kQ4);
+          if (lane == 0) {
+            mbar_arrive_expect_tx(full(s), kSplitQuarter + L::kBK + (mins ? 2 * kMinBytes : 0));
+            bulk_load(a_smem(s), ablk + kb * kSplitQuarter, kSplitQuarter, full(s));
+            if (mins) bulk_load(a_smem(s) + kSplitQuarter, ablk + kSplitMin, kMinBytes, full(s));
+          } else if (lane == 1) {
+            bulk_load(b_smem(s), bblk + kb * L::kBK, L::kBK, full(s));
+            if (mins) bulk_load(b_smem(s) + L::kBK, bblk + kBMin, kMinBytes, full(s));
           }
-        } else if ((od & 3) == 0) {
-#pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            if (o0 + 2 * i < od) {
-              const float2 a = __fmul2_rn(y[i], inv2), b = __fmul2_rn(y[i + 1], inv2);
-              *reinterpret_cast<float4 *>(yrow + 2 * i) = make_float4(a.x, a.y, b.x, b.y);
-            }
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float2 a = __fmul2_rn(y[i], inv2);
-            if (o0 + 2 * i < od) yrow[2 * i] = a.x;
-            if (o0 + 2 * i + 1 < od) yrow[2 * i + 1] = a.y;
-          }
+          __syncwarp();
+          issued = ks + 1;
         }
       }
+    }
+    if (!ok) {  // drain this CTA's copies still in flight
+      for (uint32_t k = issued > STAGES ? issued - STAGES : 0; k < issued; ++k)
+        mbar_wait(full(k % STAGES), (k / STAGES) & 1, wctl, false);
+      for (uint32_t k = s_issued > SRING ? s_issued - SRING : 0; k < s_issued; ++k)
+        mbar_wait(sfull(k % SRING), (k / SRING) & 1, wctl, false);
+    }
+  } else if (warp == ISSUER_WARP) {
+    // ------------------------------------------------------------ UMMA issuer
+    uint32_t elected;
+    asm volatile("{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(elected));
+    constexpr uint32_t idesc = idesc_f16_f32(kTileM, kTileN);
+    constexpr uint64_t kStageDesc = L::kStage >> 4;
+    const uint64_t ah0 = sdesc_kmajor_sw128(a_smem(0)), al0 = sdesc_kmajor_sw128(a_smem(0) + kSplitLo);
+    const uint64_t b0 = sdesc_kmajor_sw128(b_smem(0));
+    const uint64_t am0 = sdesc_kmajor_sw32(a_smem(0) + kSplitQuarter), bm0 = sdesc_kmajor_sw32(b_smem(0) + L::kBK);
+    uint32_t ks = 0, nr = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+      for (int64_t sb = 0; sb < nsb && ok; ++sb, ++nr) {
+        const int r = static_cast<int>(nr % NR);
+        ok = __all_sync(0xffffffffu, mbar_wait(rempty(r), ((nr / NR) & 1) ^ 1, wctl));
+        if (!ok) break;
+        const uint32_t dacc = tbase + r * kTileN, dmin = tbase + 2 * kTileN + r * kTileN;
+        for (int qq = 0; qq < 4 && ok; ++qq, ++ks) {
+          const int s = static_cast<int>(ks % STAGES);
+          ok = __all_sync(0xffffffffu, mbar_wait(full(s), (ks / STAGES) & 1, wctl));
+          if (!ok) break;
+          tc_fence_after();
+          if (elected) {
+            const uint64_t so = s * kStageDesc;
+#pragma unroll
+            for (int lc = 0; lc < 2; ++lc) {  // 32-K chunks: 64 B into the swizzled rows
+              const uint64_t off = so + lc * (64 >> 4);
+              umma_f16(dacc, ah0 + off, b0 + off, idesc, (qq | lc) ? 1u : 0u);
+              umma_f16(dacc, ah0 + off + 2, b0 + off + 2, idesc, 1u);
+              umma_f16(dacc, al0 + off, b0 + off, idesc, 1u);
+              umma_f16(dacc, al0 + off + 2, b0 + off + 2, idesc, 1u);
+            }
+            if (kQ4 && qq == 3) umma_f16(dmin, am0 + so, bm0 + so, idesc, 0u);
+            umma_commit(empty(s));
+            if (qq == 3) umma_commit(rfull(r));
+          }
+          __syncwarp();
+        }
+      }
+    }
+    if (elected) umma_commit(done);
+    __syncwarp();
+    mbar_wait(done, 0, wctl, false);
+  }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(S::kRegsEpi));
+    // ------------------------------------------------------------ epilogue
+    const int quad = warp & 3;
+    const int chalf = warp >> 2;
+    const int row = quad * 32 + lane;
+    const uint32_t taddr = tbase + (static_cast<uint32_t>(quad * 32) << 16) + chalf * 64;
+    uint32_t nr = 0, ns = 0;
+    bool ok = true;
+    griddep_wait();  // 2^-s comes from the kernel before this one
+    for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+      const int tt = tile % n_tt, ot = tile / n_tt;
+      const int64_t t = static_cast<int64_t>(tt) * kTileM + row;
+      const int64_t o0 = static_cast<int64_t>(ot) * kTileN + chalf * 64;
+      float2 y[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) y[i] = make_float2(0.f, 0.f);
+      for (int64_t sb = 0; sb < nsb && ok; ++sb, ++nr, ++ns) {
+        const int r = static_cast<int>(nr % NR), e = static_cast<int>(ns % SRING);
+        ok = __all_sync(0xffffffffu, mbar_wait(rfull(r), (nr / NR) & 1, wctl));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t r0[32], r1[32];
+        tmem_ld_32x32b_x32(taddr + r * kTileN, r0);
+        tmem_ld_32x32b_x32(taddr + r * kTileN + 32, r1);
+        tmem_wait_ld(r0);
+        reg_fence(r1);
+        ok = __all_sync(0xffffffffu, mbar_wait(sfull(e), (ns / SRING) & 1, wctl));
+        if (!ok) break;
+        const uint8_t *sblk = smem + (s_smem(e) - base);
+        const float4 *d4 = reinterpret_cast<const float4 *>(sblk) + chalf * 16;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float4 d = d4[i];
+          const uint32_t(&rr)[32] = i < 8 ? r0 : r1;
+          const int q = (i & 7) * 4;
+          y[2 * i] = __ffma2_rn(make_float2(d.x, d.y),
+                                make_float2(__uint_as_float(rr[q]), __uint_as_float(rr[q + 1])), y[2 * i]);
+          y[2 * i + 1] = __ffma2_rn(make_float2(d.z, d.w),
+                                    make_float2(__uint_as_float(rr[q + 2]), __uint_as_float(rr[q + 3])),
+                                    y[2 * i + 1]);
+        }
+        if (kQ4) {
+          tmem_ld_32x32b_x32(taddr + 2 * kTileN + r * kTileN, r0);
+          tmem_ld_32x32b_x32(taddr + 2 * kTileN + r * kTileN + 32, r1);
+          tmem_wait_ld(r0);
+          reg_fence(r1);
+          const float4 *m4 = reinterpret_cast<const float4 *>(sblk + kSDmin) + chalf * 16;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float4 dm = m4[i];
+            const uint32_t(&rr)[32] = i < 8 ? r0 : r1;
+            const int q = (i & 7) * 4;
+            y[2 * i] = __ffma2_rn(make_float2(-dm.x, -dm.y),
+                                  make_float2(__uint_as_float(rr[q]), __uint_as_float(rr[q + 1])), y[2 * i]);
+            y[2 * i + 1] = __ffma2_rn(make_float2(-dm.z, -dm.w),
+                                      make_float2(__uint_as_float(rr[q + 2]), __uint_as_float(rr[q + 3])),
+                                      y[2 * i + 1]);
+          }
+        }
+        // the region and the scale entry go back
+        tc_fence_before();
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(rempty(r));
+          mbar_arrive(sempty(e));
+        }
+      }
+      if (!ok) break;
+      if (t < nt) store_y_row(Y, t, od, o0, y, __ldg(invp + t));
     }
   }
 
@@ -1218,6 +1655,90 @@ cudaError_t launch_gemm(const mmq_weights_s *h, const uint8_t *Q, const float *X
   if (e != cudaSuccess) return e;
   e = cudaGetLastError();
   if (e == cudaSuccess && ev1) e = cudaEventRecordWithFlags(ev1, s, ev_flags);
+  return e;
+}
+
+// ---------------------------------------------------------------- split arm launch
+size_t gemm_split_scratch_bytes(const mmq_weights_s *h, int64_t nt) {
+  const bool q4 = h->type == MMQ_Q4_K;
+  const int64_t n_tt = (nt + kTileM - 1) / kTileM;
+  const size_t a = static_cast<size_t>(n_tt * h->nsb) * as_pair_bytes(q4);
+  return (a + 255) / 256 * 256 + static_cast<size_t>(n_tt * kTileM) * 4;
+}
+
+cudaError_t launch_gemm_split(const mmq_weights_s *h, const uint8_t *Q, const float *X, int64_t nt, float *Y,
+                              void *scratch, DevStatus *st, unsigned epoch, uint64_t limit_ns,
+                              cudaStream_t s, cudaEvent_t ev0, cudaEvent_t ev1, unsigned ev_flags) {
+  const bool q4 = h->type == MMQ_Q4_K;
+  const int64_t n_tt = (nt + kTileM - 1) / kTileM, nt_pad = n_tt * kTileM, nsb = h->nsb, nb32 = h->nb32;
+  const int n_ot = static_cast<int>(h->od_pad / kTileN);
+  const int n_tiles = static_cast<int>(n_tt) * n_ot;
+  uint8_t *aplane = static_cast<uint8_t *>(scratch);
+  const size_t a_bytes = static_cast<size_t>(n_tt * nsb) * as_pair_bytes(q4);
+  float *invp = reinterpret_cast<float *>(aplane + (a_bytes + 255) / 256 * 256);
+  const int dev = h->device;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  cudaError_t e = cudaSuccess;
+  if (nt_pad != nt) {  // the last token tile's padding rows must read as zero
+    const size_t tail = static_cast<size_t>((n_tt - 1) * nsb) * as_pair_bytes(q4);
+    e = cudaMemsetAsync(aplane + tail, 0, a_bytes - tail, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(invp + nt, 0, static_cast<size_t>(nt_pad - nt) * 4, s);
+    if (e != cudaSuccess) return e;
+  }
+  const unsigned pgrid = static_cast<unsigned>(nt);
+  if (X) {
+    const size_t stash = static_cast<size_t>(nb32) * kSplitStashBytesPerBlock;
+    const bool fits = stash <= static_cast<size_t>(kStashMaxBytes);
+    if (q4) {
+      if (fits) split_prepass_f32_kernel<true, true><<<pgrid, 32 * kQuantWarps, stash, s>>>(X, nt, nb32, aplane, invp);
+      else split_prepass_f32_kernel<true, false><<<pgrid, 32 * kQuantWarps, 0, s>>>(X, nt, nb32, aplane, invp);
+    } else {
+      if (fits) split_prepass_f32_kernel<false, true><<<pgrid, 32 * kQuantWarps, stash, s>>>(X, nt, nb32, aplane, invp);
+      else split_prepass_f32_kernel<false, false><<<pgrid, 32 * kQuantWarps, 0, s>>>(X, nt, nb32, aplane, invp);
+    }
+  } else if (q4) {
+    split_prepass_q_kernel<true><<<pgrid, 128, 0, s>>>(Q, nt, nb32, aplane, invp);
+  } else {
+    split_prepass_q_kernel<false><<<pgrid, 128, 0, s>>>(Q, nt, nb32, aplane, invp);
+  }
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+  WaitCtl w{&st->status, &st->abort_epoch, epoch, limit_ns};
+  if (ev0 && (e = cudaEventRecordWithFlags(ev0, s, ev_flags)) != cudaSuccess) return e;
+  const uint8_t *bp = static_cast<const uint8_t *>(h->bplane);
+  const uint8_t *bs = bp + b_scale_region(n_ot, nsb, q4);
+  const int sms = num_sms(dev);
+  const int grid = n_tiles < sms ? n_tiles : sms;
+  auto go = [&](auto kern, int smem) -> cudaError_t {
+    static std::atomic<int> ready[2][64];  // per arm variant: 0 unknown, 1 ready, 2 unusable
+    std::atomic<int> &rd = ready[q4 ? 1 : 0][dev];
+    int stt = rd.load();
+    if (stt == 0) {
+      cudaFuncAttributes fa;
+      cudaError_t e2 = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e2 == cudaSuccess) e2 = cudaFuncGetAttributes(&fa, kern);
+      if (e2 != cudaSuccess) return e2;
+      stt = fa.numRegs == Shape<false>::kRegsLaunch ? 1 : 2;
+      rd.store(stt);
+    }
+    if (stt != 1) return cudaErrorInvalidKernelImage;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(Shape<false>::kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = ev0 ? 0 : 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<const uint8_t *>(aplane), bp, bs,
+                              static_cast<const float *>(invp), nt, h->od, nb32, static_cast<int>(n_tt), n_ot, Y, w);
+  };
+  e = q4 ? go(mmq_gemm_split_kernel<true>, SplitSmem<true>::kBytes)
+         : go(mmq_gemm_split_kernel<false>, SplitSmem<false>::kBytes);
+  if (e != cudaSuccess) return e;
+  if ((e = cudaGetLastError()) == cudaSuccess && ev1) e = cudaEventRecordWithFlags(ev1, s, ev_flags);
   return e;
 }
 

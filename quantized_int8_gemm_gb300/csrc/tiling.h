@@ -84,6 +84,29 @@ __host__ __device__ constexpr uint64_t b_scale_block(int64_t tile, int64_t sb, i
   return static_cast<uint64_t>((tile * nsb + sb) * scale_block_bytes(q4));
 }
 
+// ---------------------------------------------------------------- split arm
+// The split arm folds the activation scale into the A operand: each element
+// a = da' * qs (exact in fp32) travels as fp16 hi = rn(a) and lo = rn(a - hi).
+// Its activation block per (token tile, super-block, half) holds, per 64-K
+// quarter kb of the half, the hi and lo K-blocks side by side, so one 64-K
+// GEMM stage is one contiguous copy:
+//   [hi kb0 16384][lo kb0 16384][hi kb1 16384][lo kb1 16384][odd, q4_K: A min 4096]
+// (a K-block: 128 rows x 128 B with the 128-byte swizzle, as above).  The
+// weight side is the registered operand plane, unchanged.
+constexpr int kSplitQuarter = 2 * kTileM * 64 * 2;  // 32768: hi + lo of one 64-K quarter
+constexpr int kSplitLo = kTileM * 64 * 2;           // 16384: lo K-block after its hi
+constexpr int kSplitMin = 2 * kSplitQuarter;        // A min image in an odd split block (q4_K)
+__host__ __device__ constexpr int as_even_bytes() { return 2 * kSplitQuarter; }
+__host__ __device__ constexpr int as_odd_bytes(bool q4) { return 2 * kSplitQuarter + (q4 ? kMinBytes : 0); }
+__host__ __device__ constexpr int as_pair_bytes(bool q4) { return as_even_bytes() + as_odd_bytes(q4); }
+__host__ __device__ constexpr uint64_t as_block(int64_t tile, int64_t sb, int half, int64_t nsb, bool q4) {
+  return static_cast<uint64_t>((tile * nsb + sb) * as_pair_bytes(q4) + (half ? as_even_bytes() : 0));
+}
+// byte offset of the hi element (row, k), k in [0, 128), inside a split block
+__host__ __device__ constexpr uint32_t split_off(int row, int k) {
+  return static_cast<uint32_t>((k >> 6) * kSplitQuarter) + operand_off(row, k & 63);
+}
+
 // ---------------------------------------------------------------- raw plane
 // The raw arm streams the packed weight bytes and unpacks them in the GEMM.
 // Per (weight tile, super-block, half) one raw block holds the bytes of that

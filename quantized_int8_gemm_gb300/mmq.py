@@ -36,9 +36,10 @@ MMQ_REG_RAW = 0x2
 MMQ_ARM_AUTO = 0
 MMQ_ARM_F16 = 1
 MMQ_ARM_RAW = 2
+MMQ_ARM_SPLIT = 3
 MMQ_OUT_F16 = 1
 MMQ_OUT_F32 = 2
-ARM_NAMES = {MMQ_ARM_F16: "f16_plane", MMQ_ARM_RAW: "raw_unpack"}
+ARM_NAMES = {MMQ_ARM_F16: "f16_plane", MMQ_ARM_RAW: "raw_unpack", MMQ_ARM_SPLIT: "split_scale"}
 
 Q8_BLOCK_BYTES = 40
 BLOCK_BYTES = {MMQ_Q4_K: 144, MMQ_Q6_K: 210}

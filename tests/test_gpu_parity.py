@@ -409,3 +409,52 @@ def test_dequantize_weights_bit_exact(mmq, name, od, id_):
         want = ref.astype(npt)  # one rounding, to nearest even, from the exact fp64 weight
         assert np.array_equal(got.view(np.uint16 if npt is np.float16 else np.uint32),
                               want.view(np.uint16 if npt is np.float16 else np.uint32))
+
+
+# --------------------------------------------------------------------------
+# split arm: the activation scale folded into A as an exact fp16 hi + lo pair
+SPLIT_SHAPES = [
+    ("q6_K", 256, 512, 16, 41),
+    ("q4_K", 260, 512, 129, 42),
+    ("q6_K", 300, 768, 200, 43),
+    ("q4_K", 131, 256, 1, 44),
+    ("q4_K", 384, 1024, 256, 45),
+    ("q6_K", 1000, 4096, 300, 46),
+]
+
+
+@pytest.mark.parametrize("name,od,id_,nt,seed", SPLIT_SHAPES)
+def test_split_arm_parity(mmq, name, od, id_, nt, seed):
+    W = gen.weights(name, od, id_, seed=500 + seed)
+    X = gen.activations(nt, id_, seed=600 + seed, outlier_p=0.01, outlier_scale=20.0)
+    w = mmq.mmq_register_weights(name, torch.from_numpy(W).cuda(), od, id_)
+    Xd = torch.from_numpy(X).cuda()
+    Q = mmq.mmq_quantize_act(Xd)
+    Ys, arm = mmq.mmq_gemm(w, Q, nt, flags=mmq.MMQ_ARM_SPLIT, return_arm=True)
+    assert arm == mmq.MMQ_ARM_SPLIT
+    Yf = mmq.mmq_gemm_f32(w, Xd, flags=mmq.MMQ_ARM_SPLIT)
+    torch.cuda.synchronize()
+    assert mmq.mmq_last_device_error() == 0
+    # the same quantized operands from X or from Q: bit-identical
+    assert torch.equal(Ys, Yf)
+    Y_ref = oracle.gemm(QT[name], W, od, id_, oracle.quantize_q8_0(X), nt)
+    err, bound = _within_tol(Ys.cpu().numpy(), Y_ref)
+    assert err <= bound, (err, bound)
+    # and close to the exact-partials arm: both are within fp32 summation of Y_ref
+    Y16 = mmq.mmq_gemm(w, Q, nt, flags=mmq.MMQ_ARM_F16)
+    scale = float(np.abs(Y_ref).max()) + 1e-30
+    assert float((Ys - Y16).abs().max()) / scale < 1e-5
+    w.release()
+
+
+@pytest.mark.parametrize("cfg", gen.CONFIGS[1:3], ids=lambda c: c.name)
+def test_split_arm_workloads_sampled(mmq, cfg):
+    W, X = gen.config_inputs(cfg)
+    w = mmq.mmq_register_weights(cfg.qtype, torch.from_numpy(W).cuda(), cfg.od, cfg.id)
+    Y = mmq.mmq_gemm_f32(w, torch.from_numpy(X).cuda(), flags=mmq.MMQ_ARM_SPLIT).cpu().numpy()
+    assert mmq.mmq_last_device_error() == 0
+    ts, os_ = _sample_entries(cfg.nt, cfg.od, 3000, cfg.seed)
+    y_ref = oracle.gemm_entries(QT[cfg.qtype], W, cfg.od, cfg.id, oracle.quantize_q8_0(X), cfg.nt, ts, os_)
+    err, bound = _within_tol(Y[ts, os_], y_ref)
+    assert err <= bound, (err, bound)
+    w.release()
