@@ -88,7 +88,7 @@ typedef struct mmq_weights_s *mmq_weights_t;
 #define MMQ_REG_RAW 0x2u   /* also keep the packed bytes, regrouped, for MMQ_ARM_RAW */
 
 /* ---- GEMM arms (flags of mmq_gemm select one; arm_used reports it) ----- */
-#define MMQ_ARM_AUTO 0     /* library choice */
+#define MMQ_ARM_AUTO 0     /* library choice: MMQ_ARM_SPLIT for q6_K, MMQ_ARM_F16 for q4_K */
 #define MMQ_ARM_F16 1      /* operands from the registered fp16 operand plane (TMA copy) */
 #define MMQ_ARM_RAW 2      /* packed weight bytes streamed and unpacked to fp16 in shared
                               memory inside the GEMM ("47 · r44 — W_exp stride mismatch

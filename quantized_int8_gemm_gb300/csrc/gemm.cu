@@ -707,9 +707,11 @@ __device__ __forceinline__ void st_global_v8(float *p, float2 a, float2 b, float
                : "memory");
 }
 
-// The 64 outputs of one thread (row t, columns o0 .. o0 + 63) times inv.
+// 64 outputs of one thread (row t, columns o0 .. o0 + 63; y[OFF ..]) times inv.
+template <int OFF = 0, int N = 32>
 __device__ __forceinline__ void store_y_row(float *__restrict__ Y, int64_t t, int64_t od, int64_t o0,
-                                            const float2 (&y)[32], float inv) {
+                                            const float2 (&y)[N], float inv) {
+  static_assert(OFF + 32 <= N, "64 outputs");
   const float2 inv2 = make_float2(inv, inv);
   float *yrow = Y + t * od + o0;
   if ((od & 7) == 0 && (reinterpret_cast<uintptr_t>(Y) & 31) == 0) {
@@ -717,8 +719,8 @@ __device__ __forceinline__ void store_y_row(float *__restrict__ Y, int64_t t, in
 #pragma unroll
     for (int i = 0; i < 32; i += 4) {
       if (o0 + 2 * i < od) {
-        const float2 a = __fmul2_rn(y[i], inv2), b = __fmul2_rn(y[i + 1], inv2);
-        const float2 c = __fmul2_rn(y[i + 2], inv2), d = __fmul2_rn(y[i + 3], inv2);
+        const float2 a = __fmul2_rn(y[OFF + i], inv2), b = __fmul2_rn(y[OFF + i + 1], inv2);
+        const float2 c = __fmul2_rn(y[OFF + i + 2], inv2), d = __fmul2_rn(y[OFF + i + 3], inv2);
         st_global_v8(yrow + 2 * i, a, b, c, d);
       }
     }
@@ -726,14 +728,14 @@ __device__ __forceinline__ void store_y_row(float *__restrict__ Y, int64_t t, in
 #pragma unroll
     for (int i = 0; i < 32; i += 2) {
       if (o0 + 2 * i < od) {
-        const float2 a = __fmul2_rn(y[i], inv2), b = __fmul2_rn(y[i + 1], inv2);
+        const float2 a = __fmul2_rn(y[OFF + i], inv2), b = __fmul2_rn(y[OFF + i + 1], inv2);
         *reinterpret_cast<float4 *>(yrow + 2 * i) = make_float4(a.x, a.y, b.x, b.y);
       }
     }
   } else {
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-      const float2 a = __fmul2_rn(y[i], inv2);
+      const float2 a = __fmul2_rn(y[OFF + i], inv2);
       if (o0 + 2 * i < od) yrow[2 * i] = a.x;
       if (o0 + 2 * i + 1 < od) yrow[2 * i + 1] = a.y;
     }
@@ -1197,26 +1199,41 @@ __global__ void __launch_bounds__(Shape<kRaw>::kThreads, 1)
 }
 
 // ---------------------------------------------------------------- the split arm's GEMM
-// Same tiles, operands and roles as mmq_gemm_kernel, with the activation scale
-// folded into A (hi + lo images, tiling.h): per 32-K chunk four 128x128x16
-// UMMAs (hi and lo, two K halves each) accumulate into one TMEM region for the
-// whole super-block, so the epilogue runs once per super-block:
+// Same operands and roles as mmq_gemm_kernel, with the activation scale
+// folded into A (hi + lo images, tiling.h): per 32-K chunk four UMMAs (hi and
+// lo, two K halves each) accumulate into one TMEM region for the whole
+// super-block, so the epilogue runs once per super-block:
 //   y[t][o] += d[o][sb] * ACC[t][o][sb]  -  dmin[o][sb] * MIN[t][o][sb]
-// Regions (128 columns each): q6_K four accumulators; q4_K two accumulators
-// (columns 0..255) each with its min-term region 256 columns on.  Stages of
-// 64 K (hi and lo activation K-blocks, one weight K-block, and in the last
-// quarter of a q4_K super-block the two min images); one issuer; whole tiles
-// per CTA.
-template <bool kQ4>
+// kWide: output tiles of 128 tokens x 256 weight rows (two weight tiles side
+// by side, one N = 256 UMMA), so each activation K-block feeds twice the
+// MACs; otherwise 128 x 128.  Regions of kN columns, NR accumulators then
+// (q4_K) NR min-term regions: kWide q6_K two accumulators (a kWide q4_K
+// would have one of each, the issuer waiting for the epilogue between
+// super-blocks), 128 wide q6_K four, 128 wide q4_K two of each.  Stages of
+// 64 K; one issuer; whole tiles per CTA.
+// The split arm's register split: its epilogue holds no per-chunk pipeline,
+// its producer and issuer more addresses.
+struct SplitShape {
+  static constexpr int kThreads = 384;
+  static constexpr int kRegsLaunch = 168;
+  static constexpr int kRegsEpi = 208;
+  static constexpr int kRegsCtl = 88;
+  static_assert(256 * kRegsEpi + (kThreads - 256) * kRegsCtl == kThreads * kRegsLaunch,
+                "the register split must add up to what the launch holds");
+};
+
+template <bool kQ4, bool kWide>
 struct SplitSmem {
-  static constexpr int kStages = kQ4 ? 3 : 4;
-  static constexpr int kA = kSplitQuarter + (kQ4 ? kMinBytes : 0);
-  static constexpr int kB = ((kTileN * 64 * 2 + (kQ4 ? kMinBytes : 0) + 1023) / 1024) * 1024;
-  static constexpr int kBK = kTileN * 64 * 2;  // one weight K-block: 16384
+  static constexpr int kN = kWide ? 256 : 128;
+  static constexpr int kBK = kTileN * 64 * 2;  // one weight K-block of one tile: 16384
+  static constexpr int kMinA = kQ4 ? kMinBytes : 0, kMinB = kQ4 ? kMinBytes * (kN / 128) : 0;
+  static constexpr int kA = kSplitQuarter + kMinA;
+  static constexpr int kB = ((kBK * (kN / 128) + kMinB + 1023) / 1024) * 1024;
   static constexpr int kStage = kA + kB;
-  static constexpr int kScale = scale_block_bytes(kQ4);
+  static constexpr int kStages = kStage * 4 <= 200 * 1024 ? 4 : kStage * 3 <= 200 * 1024 ? 3 : 2;
+  static constexpr int kScale = scale_block_bytes(kQ4) * (kN / 128);
   static constexpr int kScaleRing = kStages * kStage;
-  static constexpr int kRegions = kQ4 ? 2 : 4;
+  static constexpr int kRegions = kWide ? (kQ4 ? 1 : 2) : (kQ4 ? 2 : 4);
   static constexpr int kBar = kScaleRing + SRING * kScale;
   // full, empty per stage; rfull, rempty per region; sfull, sempty per scale entry; done
   static constexpr int kNumBars = 2 * kStages + 2 * kRegions + 2 * SRING + 1;
@@ -1224,16 +1241,17 @@ struct SplitSmem {
   static constexpr int kBytes = kSlot + 16 + 1024;
   static_assert(kA % 1024 == 0 && kStage % 1024 == 0, "stage buffers must keep 1 KB alignment");
   static_assert(kBytes <= 227 * 1024, "shared memory budget");
+  static_assert(kRegions * kN * (kQ4 ? 2 : 1) <= TMEM_COLS, "TMEM columns");
 };
 
-template <bool kQ4>
-__global__ void __launch_bounds__(Shape<false>::kThreads, 1)
+template <bool kQ4, bool kWide>
+__global__ void __launch_bounds__(SplitShape::kThreads, 1)
     mmq_gemm_split_kernel(const uint8_t *__restrict__ aplane, const uint8_t *__restrict__ bplane,
                           const uint8_t *__restrict__ bscale, const float *__restrict__ invp, int64_t nt,
                           int64_t od, int64_t nb32, int n_tt, int n_ot, float *__restrict__ Y, WaitCtl wctl) {
-  using L = SplitSmem<kQ4>;
-  using S = Shape<false>;
-  constexpr int STAGES = L::kStages, NR = L::kRegions;
+  using L = SplitSmem<kQ4, kWide>;
+  using S = SplitShape;
+  constexpr int STAGES = L::kStages, NR = L::kRegions, NW = L::kN / 128;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -1241,7 +1259,10 @@ __global__ void __launch_bounds__(Shape<false>::kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t nsb = nb32 / 8;
-  const int n_tiles = n_tt * n_ot;
+  const int n_og = (n_ot + NW - 1) / NW;  // groups of NW weight tiles
+  const int n_tiles = n_tt * n_og;
+  // weight tile w of group og (the last group of an odd n_ot repeats its tile)
+  auto wtile = [&](int og, int w) { return min(og * NW + w, n_ot - 1); };
 
   const uint32_t bar = base + L::kBar;
   auto full = [&](int s) { return bar + 8u * s; };
@@ -1287,14 +1308,16 @@ __global__ void __launch_bounds__(Shape<false>::kThreads, 1)
     uint32_t ks = 0, ns = 0, issued = 0, s_issued = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-      const int tt = tile % n_tt, ot = tile / n_tt;
+      const int tt = tile % n_tt, og = tile / n_tt;
       for (int64_t sb = 0; sb < nsb && ok; ++sb, ++ns) {
         const int e = static_cast<int>(ns % SRING);
         ok = __all_sync(0xffffffffu, mbar_wait(sempty(e), ((ns / SRING) & 1) ^ 1, wctl));
         if (!ok) break;
         if (lane == 2) {
           mbar_arrive_expect_tx(sfull(e), L::kScale);
-          bulk_load(s_smem(e), bscale + b_scale_block(ot, sb, nsb, kQ4), L::kScale, sfull(e));
+          for (int w = 0; w < NW; ++w)
+            bulk_load(s_smem(e) + w * scale_block_bytes(kQ4), bscale + b_scale_block(wtile(og, w), sb, nsb, kQ4),
+                      scale_block_bytes(kQ4), sfull(e));
         }
         __syncwarp();
         s_issued = ns + 1;
@@ -1305,14 +1328,16 @@ __global__ void __launch_bounds__(Shape<false>::kThreads, 1)
           const int half = qq >> 1, kb = qq & 1;
           const bool mins = kQ4 && qq == 3;
           const uint8_t *ablk = aplane + as_block(tt, sb, half, nsb, kQ4);
-          const uint8_t *bblk = bplane + b_block(ot, sb, half, nsb, kQ4);
           if (lane == 0) {
-            mbar_arrive_expect_tx(full(s), kSplitQuarter + L::kBK + (mins ? 2 * kMinBytes : 0));
+            mbar_arrive_expect_tx(full(s), kSplitQuarter + NW * L::kBK + (mins ? L::kMinA + L::kMinB : 0));
             bulk_load(a_smem(s), ablk + kb * kSplitQuarter, kSplitQuarter, full(s));
             if (mins) bulk_load(a_smem(s) + kSplitQuarter, ablk + kSplitMin, kMinBytes, full(s));
           } else if (lane == 1) {
-            bulk_load(b_smem(s), bblk + kb * L::kBK, L::kBK, full(s));
-            if (mins) bulk_load(b_smem(s) + L::kBK, bblk + kBMin, kMinBytes, full(s));
+            for (int w = 0; w < NW; ++w) {
+              const uint8_t *bblk = bplane + b_block(wtile(og, w), sb, half, nsb, kQ4);
+              bulk_load(b_smem(s) + w * L::kBK, bblk + kb * L::kBK, L::kBK, full(s));
+              if (mins) bulk_load(b_smem(s) + NW * L::kBK + w * kMinBytes, bblk + kBMin, kMinBytes, full(s));
+            }
           }
           __syncwarp();
           issued = ks + 1;
@@ -1330,11 +1355,12 @@ __global__ void __launch_bounds__(Shape<false>::kThreads, 1)
     uint32_t elected;
     asm volatile("{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
                  : "=r"(elected));
-    constexpr uint32_t idesc = idesc_f16_f32(kTileM, kTileN);
+    constexpr uint32_t idesc = idesc_f16_f32(kTileM, L::kN);
     constexpr uint64_t kStageDesc = L::kStage >> 4;
     const uint64_t ah0 = sdesc_kmajor_sw128(a_smem(0)), al0 = sdesc_kmajor_sw128(a_smem(0) + kSplitLo);
     const uint64_t b0 = sdesc_kmajor_sw128(b_smem(0));
-    const uint64_t am0 = sdesc_kmajor_sw32(a_smem(0) + kSplitQuarter), bm0 = sdesc_kmajor_sw32(b_smem(0) + L::kBK);
+    const uint64_t am0 = sdesc_kmajor_sw32(a_smem(0) + kSplitQuarter);
+    const uint64_t bm0 = sdesc_kmajor_sw32(b_smem(0) + NW * L::kBK);
     uint32_t ks = 0, nr = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
@@ -1342,7 +1368,7 @@ __global__ void __launch_bounds__(Shape<false>::kThreads, 1)
         const int r = static_cast<int>(nr % NR);
         ok = __all_sync(0xffffffffu, mbar_wait(rempty(r), ((nr / NR) & 1) ^ 1, wctl));
         if (!ok) break;
-        const uint32_t dacc = tbase + r * kTileN, dmin = tbase + 2 * kTileN + r * kTileN;
+        const uint32_t dacc = tbase + r * L::kN, dmin = tbase + (NR + r) * L::kN;
         for (int qq = 0; qq < 4 && ok; ++qq, ++ks) {
           const int s = static_cast<int>(ks % STAGES);
           ok = __all_sync(0xffffffffu, mbar_wait(full(s), (ks / STAGES) & 1, wctl));
@@ -1373,61 +1399,67 @@ __global__ void __launch_bounds__(Shape<false>::kThreads, 1)
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(S::kRegsEpi));
     // ------------------------------------------------------------ epilogue
+    // warp w: TMEM lanes 32*(w%4).., columns (w/4)*kN/2 .. of a region
+    constexpr int CW = L::kN / 2;  // columns per warp
     const int quad = warp & 3;
     const int chalf = warp >> 2;
     const int row = quad * 32 + lane;
-    const uint32_t taddr = tbase + (static_cast<uint32_t>(quad * 32) << 16) + chalf * 64;
+    const uint32_t taddr = tbase + (static_cast<uint32_t>(quad * 32) << 16) + chalf * CW;
     uint32_t nr = 0, ns = 0;
     bool ok = true;
     griddep_wait();  // 2^-s comes from the kernel before this one
     for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-      const int tt = tile % n_tt, ot = tile / n_tt;
+      const int tt = tile % n_tt, og = tile / n_tt;
       const int64_t t = static_cast<int64_t>(tt) * kTileM + row;
-      const int64_t o0 = static_cast<int64_t>(ot) * kTileN + chalf * 64;
-      float2 y[32];
+      // this warp's columns: weight tile og*NW + chalf (kWide), else half chalf of tile og
+      const int wt = kWide ? og * NW + chalf : og;
+      const int64_t o0 = static_cast<int64_t>(wt) * kTileN + (kWide ? 0 : chalf * 64);
+      float2 y[CW / 2];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) y[i] = make_float2(0.f, 0.f);
+      for (int i = 0; i < CW / 2; ++i) y[i] = make_float2(0.f, 0.f);
       for (int64_t sb = 0; sb < nsb && ok; ++sb, ++nr, ++ns) {
         const int r = static_cast<int>(nr % NR), e = static_cast<int>(ns % SRING);
         ok = __all_sync(0xffffffffu, mbar_wait(rfull(r), (nr / NR) & 1, wctl));
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(sfull(e), (ns / SRING) & 1, wctl));
         if (!ok) break;
         tc_fence_after();
-        uint32_t r0[32], r1[32];
-        tmem_ld_32x32b_x32(taddr + r * kTileN, r0);
-        tmem_ld_32x32b_x32(taddr + r * kTileN + 32, r1);
-        tmem_wait_ld(r0);
-        reg_fence(r1);
-        ok = __all_sync(0xffffffffu, mbar_wait(sfull(e), (ns / SRING) & 1, wctl));
-        if (!ok) break;
-        const uint8_t *sblk = smem + (s_smem(e) - base);
-        const float4 *d4 = reinterpret_cast<const float4 *>(sblk) + chalf * 16;
+        const uint8_t *sblk = smem + (s_smem(e) - base) + (kWide ? chalf * scale_block_bytes(kQ4) : 0);
+        const float4 *d4 = reinterpret_cast<const float4 *>(sblk) + (kWide ? 0 : chalf * 16);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float4 d = d4[i];
-          const uint32_t(&rr)[32] = i < 8 ? r0 : r1;
-          const int q = (i & 7) * 4;
-          y[2 * i] = __ffma2_rn(make_float2(d.x, d.y),
-                                make_float2(__uint_as_float(rr[q]), __uint_as_float(rr[q + 1])), y[2 * i]);
-          y[2 * i + 1] = __ffma2_rn(make_float2(d.z, d.w),
-                                    make_float2(__uint_as_float(rr[q + 2]), __uint_as_float(rr[q + 3])),
-                                    y[2 * i + 1]);
-        }
-        if (kQ4) {
-          tmem_ld_32x32b_x32(taddr + 2 * kTileN + r * kTileN, r0);
-          tmem_ld_32x32b_x32(taddr + 2 * kTileN + r * kTileN + 32, r1);
+        for (int g = 0; g < CW / 64; ++g) {  // 64 columns at a time
+          uint32_t r0[32], r1[32];
+          tmem_ld_32x32b_x32(taddr + r * L::kN + g * 64, r0);
+          tmem_ld_32x32b_x32(taddr + r * L::kN + g * 64 + 32, r1);
           tmem_wait_ld(r0);
           reg_fence(r1);
-          const float4 *m4 = reinterpret_cast<const float4 *>(sblk + kSDmin) + chalf * 16;
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float4 dm = m4[i];
+            const float4 d = d4[g * 16 + i];
             const uint32_t(&rr)[32] = i < 8 ? r0 : r1;
             const int q = (i & 7) * 4;
-            y[2 * i] = __ffma2_rn(make_float2(-dm.x, -dm.y),
-                                  make_float2(__uint_as_float(rr[q]), __uint_as_float(rr[q + 1])), y[2 * i]);
-            y[2 * i + 1] = __ffma2_rn(make_float2(-dm.z, -dm.w),
-                                      make_float2(__uint_as_float(rr[q + 2]), __uint_as_float(rr[q + 3])),
-                                      y[2 * i + 1]);
+            float2 &y0 = y[g * 32 + 2 * i], &y1 = y[g * 32 + 2 * i + 1];
+            y0 = __ffma2_rn(make_float2(d.x, d.y), make_float2(__uint_as_float(rr[q]), __uint_as_float(rr[q + 1])), y0);
+            y1 = __ffma2_rn(make_float2(d.z, d.w), make_float2(__uint_as_float(rr[q + 2]), __uint_as_float(rr[q + 3])), y1);
+          }
+        }
+        if (kQ4) {
+          const float4 *m4 = reinterpret_cast<const float4 *>(sblk + kSDmin) + (kWide ? 0 : chalf * 16);
+#pragma unroll
+          for (int g = 0; g < CW / 64; ++g) {
+            uint32_t r0[32], r1[32];
+            tmem_ld_32x32b_x32(taddr + (NR + r) * L::kN + g * 64, r0);
+            tmem_ld_32x32b_x32(taddr + (NR + r) * L::kN + g * 64 + 32, r1);
+            tmem_wait_ld(r0);
+            reg_fence(r1);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float4 dm = m4[g * 16 + i];
+              const uint32_t(&rr)[32] = i < 8 ? r0 : r1;
+              const int q = (i & 7) * 4;
+              float2 &y0 = y[g * 32 + 2 * i], &y1 = y[g * 32 + 2 * i + 1];
+              y0 = __ffma2_rn(make_float2(-dm.x, -dm.y), make_float2(__uint_as_float(rr[q]), __uint_as_float(rr[q + 1])), y0);
+              y1 = __ffma2_rn(make_float2(-dm.z, -dm.w), make_float2(__uint_as_float(rr[q + 2]), __uint_as_float(rr[q + 3])), y1);
+            }
           }
         }
         // the region and the scale entry go back
@@ -1440,7 +1472,11 @@ __global__ void __launch_bounds__(Shape<false>::kThreads, 1)
         }
       }
       if (!ok) break;
-      if (t < nt) store_y_row(Y, t, od, o0, y, __ldg(invp + t));
+      if (t < nt && (!kWide || og * NW + chalf < n_ot)) {  // (a repeated last tile is not stored)
+        const float inv = __ldg(invp + t);
+        store_y_row<0>(Y, t, od, o0, y, inv);
+        if constexpr (CW > 64) store_y_row<32>(Y, t, od, o0 + 64, y, inv);
+      }
     }
   }
 
@@ -1708,23 +1744,30 @@ cudaError_t launch_gemm_split(const mmq_weights_s *h, const uint8_t *Q, const fl
   const uint8_t *bp = static_cast<const uint8_t *>(h->bplane);
   const uint8_t *bs = bp + b_scale_region(n_ot, nsb, q4);
   const int sms = num_sms(dev);
-  const int grid = n_tiles < sms ? n_tiles : sms;
-  auto go = [&](auto kern, int smem) -> cudaError_t {
-    static std::atomic<int> ready[2][64];  // per arm variant: 0 unknown, 1 ready, 2 unusable
-    std::atomic<int> &rd = ready[q4 ? 1 : 0][dev];
+  // q6_K tiles of 256 weight rows when they still give one and a half waves
+  // (q4_K keeps 128: with its min-term regions a 256-wide accumulator cannot be
+  // double-buffered in TMEM, and measured slower: 584 against 520 us on the
+  // 18944 x 3584 x 2630 workload)
+  const int n_wide = static_cast<int>(n_tt) * ((n_ot + 1) / 2);
+  const bool wide = !q4 && 2 * n_wide >= 3 * sms;
+  const int tiles = wide ? n_wide : n_tiles;
+  const int grid = tiles < sms ? tiles : sms;
+  auto go = [&](auto kern, int smem, int variant) -> cudaError_t {
+    static std::atomic<int> ready[3][64];  // per kernel variant: 0 unknown, 1 ready, 2 unusable
+    std::atomic<int> &rd = ready[variant][dev];
     int stt = rd.load();
     if (stt == 0) {
       cudaFuncAttributes fa;
       cudaError_t e2 = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
       if (e2 == cudaSuccess) e2 = cudaFuncGetAttributes(&fa, kern);
       if (e2 != cudaSuccess) return e2;
-      stt = fa.numRegs == Shape<false>::kRegsLaunch ? 1 : 2;
+      stt = fa.numRegs == SplitShape::kRegsLaunch ? 1 : 2;
       rd.store(stt);
     }
     if (stt != 1) return cudaErrorInvalidKernelImage;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(Shape<false>::kThreads);
+    cfg.blockDim = dim3(SplitShape::kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -1735,8 +1778,11 @@ cudaError_t launch_gemm_split(const mmq_weights_s *h, const uint8_t *Q, const fl
     return cudaLaunchKernelEx(&cfg, kern, static_cast<const uint8_t *>(aplane), bp, bs,
                               static_cast<const float *>(invp), nt, h->od, nb32, static_cast<int>(n_tt), n_ot, Y, w);
   };
-  e = q4 ? go(mmq_gemm_split_kernel<true>, SplitSmem<true>::kBytes)
-         : go(mmq_gemm_split_kernel<false>, SplitSmem<false>::kBytes);
+  if (q4)
+    e = go(mmq_gemm_split_kernel<true, false>, SplitSmem<true, false>::kBytes, 0);
+  else
+    e = wide ? go(mmq_gemm_split_kernel<false, true>, SplitSmem<false, true>::kBytes, 1)
+             : go(mmq_gemm_split_kernel<false, false>, SplitSmem<false, false>::kBytes, 2);
   if (e != cudaSuccess) return e;
   if ((e = cudaGetLastError()) == cudaSuccess && ev1) e = cudaEventRecordWithFlags(ev1, s, ev_flags);
   return e;

@@ -447,14 +447,38 @@ def test_split_arm_parity(mmq, name, od, id_, nt, seed):
     w.release()
 
 
-@pytest.mark.parametrize("cfg", gen.CONFIGS[1:3], ids=lambda c: c.name)
+@pytest.mark.parametrize("cfg", gen.CONFIGS[1:5], ids=lambda c: c.name)
 def test_split_arm_workloads_sampled(mmq, cfg):
     W, X = gen.config_inputs(cfg)
     w = mmq.mmq_register_weights(cfg.qtype, torch.from_numpy(W).cuda(), cfg.od, cfg.id)
     Y = mmq.mmq_gemm_f32(w, torch.from_numpy(X).cuda(), flags=mmq.MMQ_ARM_SPLIT).cpu().numpy()
     assert mmq.mmq_last_device_error() == 0
-    ts, os_ = _sample_entries(cfg.nt, cfg.od, 3000, cfg.seed)
+    ts, os_ = _sample_entries(cfg.nt, cfg.od, 3000 if cfg.id <= 4096 else 800, cfg.seed)
     y_ref = oracle.gemm_entries(QT[cfg.qtype], W, cfg.od, cfg.id, oracle.quantize_q8_0(X), cfg.nt, ts, os_)
     err, bound = _within_tol(Y[ts, os_], y_ref)
     assert err <= bound, (err, bound)
+    w.release()
+
+
+@pytest.mark.parametrize("name", ["q6_K", "q4_K"])
+@pytest.mark.parametrize("od", [3584, 3456])   # 28 weight tiles, and 27 (the last pair repeats a tile)
+def test_split_arm_wide_tiles(mmq, name, od):
+    """Enough tiles for the split arm's 256-row tiles (q6_K; q4_K keeps 128-row
+    tiles on the same shape)."""
+    id_, nt = 512, 2176
+    W = gen.weights(name, od, id_, seed=81 + od)
+    X = gen.activations(nt, id_, seed=82 + od, outlier_p=0.01, outlier_scale=20.0)
+    w = mmq.mmq_register_weights(name, torch.from_numpy(W).cuda(), od, id_)
+    Xd = torch.from_numpy(X).cuda()
+    Y = mmq.mmq_gemm_f32(w, Xd, flags=mmq.MMQ_ARM_SPLIT)
+    Y16 = mmq.mmq_gemm_f32(w, Xd, flags=mmq.MMQ_ARM_F16)
+    torch.cuda.synchronize()
+    assert mmq.mmq_last_device_error() == 0
+    Yn = Y.cpu().numpy()
+    ts, os_ = _sample_entries(nt, od, 4000, od)
+    y_ref = oracle.gemm_entries(QT[name], W, od, id_, oracle.quantize_q8_0(X), nt, ts, os_)
+    err, bound = _within_tol(Yn[ts, os_], y_ref)
+    assert err <= bound, (err, bound)
+    # every output written, and within fp32 summation of the exact-partials arm
+    assert float((Y - Y16).abs().max()) <= 1e-5 * float(Y16.abs().max())
     w.release()
