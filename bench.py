@@ -334,9 +334,16 @@ def run_mine(args, cfg, rank, world):
     with torch.cuda.stream(stream):
         for i in range(Wu):
             step(i)
+        if fused:  # one more untimed call that reports the arm the library picked
+            arm = mmq.mmq_gemm_f32(ws[0], Xs[0], Ys[0], return_arm=True)[1]
+        else:
+            mmq.mmq_quantize_act(Xs[0], Qs[0])
+            arm = mmq.mmq_gemm(ws[0], Qs[0], nt, Ys[0], return_arm=True)[1]
     stream.synchronize()
     if mmq.mmq_last_device_error() != 0:
         raise RuntimeError("device wait expired during warm-up")
+    arm_name = mmq.ARM_NAMES.get(arm, str(arm))
+    kernel_name = "mmq_gemm_split_kernel" if arm == mmq.MMQ_ARM_SPLIT else "mmq_gemm_kernel"
 
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(K)]
@@ -427,7 +434,7 @@ def run_mine(args, cfg, rank, world):
                 "frac": achieved / peak, "traffic": _profiled_traffic(cfg.name),
                 "peak_source": f"{peak_src} {'sustained' if long_region else 'burst'} bf16 "
                                f"(fp16 UMMA runs at the bf16 rate)",
-                "kernel": "mmq_gemm_kernel", "gemm_ms_avg": gemm_avg_ms,
+                "kernel": kernel_name, "arm": arm_name, "gemm_ms_avg": gemm_avg_ms,
                 "timing": "CUDA events around each GEMM launch, second pass over the same K steps "
                           f"(that pass: {ev_p0.elapsed_time(ev_p1) / K * 1e3:.1f} us per step)",
                 "hbm_floor_us": (info["operand_bytes"] + nt * id_ * 2 + nt * od * 4) /
