@@ -235,10 +235,11 @@ static int gemm_impl(mmq_weights_t h, const void *Q, const float *X, int64_t nt,
   if (flags != MMQ_ARM_AUTO && flags != MMQ_ARM_F16 && flags != MMQ_ARM_RAW && flags != MMQ_ARM_SPLIT)
     return MMQ_ERR_UNSUPPORTED;
   if (flags == MMQ_ARM_RAW && !h->rawplane) return MMQ_ERR_UNSUPPORTED;
-  // library choice: the split arm for q6_K, the fp16-plane arm for q4_K (measured faster on the
-  // q-proj and FFN workloads of each type)
+  // library choice: the split arm for q6_K, and for q4_K where it runs 256-row tiles; else the
+  // fp16-plane arm (measured fastest on the q-proj and FFN workloads of each type)
   const bool raw = flags == MMQ_ARM_RAW;
-  const bool split = flags == MMQ_ARM_SPLIT || (flags == MMQ_ARM_AUTO && h->type == MMQ_Q6_K);
+  const bool split = flags == MMQ_ARM_SPLIT ||
+                     (flags == MMQ_ARM_AUTO && (h->type == MMQ_Q6_K || mmq::gemm_split_wide(h, nt)));
   if (arm_used) *arm_used = raw ? MMQ_ARM_RAW : split ? MMQ_ARM_SPLIT : MMQ_ARM_F16;
   if (nt == 0) return MMQ_OK;
   const void *A = X ? static_cast<const void *>(X) : Q;

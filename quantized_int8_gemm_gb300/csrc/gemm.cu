@@ -1207,42 +1207,82 @@ __global__ void __launch_bounds__(Shape<kRaw>::kThreads, 1)
 // kWide: output tiles of 128 tokens x 256 weight rows (two weight tiles side
 // by side, one N = 256 UMMA), so each activation K-block feeds twice the
 // MACs; otherwise 128 x 128.  Regions of kN columns, NR accumulators then
-// (q4_K) NR min-term regions: kWide q6_K two accumulators (a kWide q4_K
-// would have one of each, the issuer waiting for the epilogue between
-// super-blocks), 128 wide q6_K four, 128 wide q4_K two of each.  Stages of
-// 64 K; one issuer; whole tiles per CTA.
+// (q4_K, 128 wide) NR min-term regions: 128 wide q6_K four accumulators, 128
+// wide q4_K two of each.  kWide tiles have two regions of 256 columns; a q4_K
+// min term then goes into the region its super-block's accumulator just left
+// (kShared): the issuer sends the K = 16 min UMMA of super-block n into region
+// n % 2 once the epilogue has read the accumulator there, so both regions stay
+// double-buffered; its operands wait in a ring of their own until then.
+// Stages of 64 K; one issuer; whole tiles per CTA.
 // The split arm's register split: its epilogue holds no per-chunk pipeline,
-// its producer and issuer more addresses.
+// its producer and issuer more addresses (kShared: the min ring's too).
 struct SplitShape {
   static constexpr int kThreads = 384;
   static constexpr int kRegsLaunch = 168;
-  static constexpr int kRegsEpi = 208;
-  static constexpr int kRegsCtl = 88;
-  static_assert(256 * kRegsEpi + (kThreads - 256) * kRegsCtl == kThreads * kRegsLaunch,
+};
+template <bool kShared>
+struct SplitRegs {
+  static constexpr int kEpi = kShared ? 192 : 208;
+  static constexpr int kCtl = kShared ? 120 : 88;
+  static_assert(256 * kEpi + (SplitShape::kThreads - 256) * kCtl == SplitShape::kThreads * SplitShape::kRegsLaunch,
                 "the register split must add up to what the launch holds");
 };
 
 template <bool kQ4, bool kWide>
 struct SplitSmem {
+  static constexpr bool kShared = kQ4 && kWide;  // min terms share the accumulator regions
   static constexpr int kN = kWide ? 256 : 128;
   static constexpr int kBK = kTileN * 64 * 2;  // one weight K-block of one tile: 16384
-  static constexpr int kMinA = kQ4 ? kMinBytes : 0, kMinB = kQ4 ? kMinBytes * (kN / 128) : 0;
+  static constexpr int kMinA = kQ4 && !kShared ? kMinBytes : 0;
+  static constexpr int kMinB = kQ4 && !kShared ? kMinBytes * (kN / 128) : 0;
   static constexpr int kA = kSplitQuarter + kMinA;
   static constexpr int kB = ((kBK * (kN / 128) + kMinB + 1023) / 1024) * 1024;
   static constexpr int kStage = kA + kB;
   static constexpr int kStages = kStage * 4 <= 200 * 1024 ? 4 : kStage * 3 <= 200 * 1024 ? 3 : 2;
+  // kShared: min operand ring, entry = A min image then kN / 128 B min images
+  static constexpr int kMR = kShared ? 2 : 0;
+  static constexpr int kMinEntry = kMinBytes * (1 + kN / 128);
+  static constexpr int kMinRing = kStages * kStage;
   static constexpr int kScale = scale_block_bytes(kQ4) * (kN / 128);
-  static constexpr int kScaleRing = kStages * kStage;
-  static constexpr int kRegions = kWide ? (kQ4 ? 1 : 2) : (kQ4 ? 2 : 4);
+  static constexpr int kScaleRing = kMinRing + kMR * kMinEntry;
+  static constexpr int kRegions = kWide ? 2 : (kQ4 ? 2 : 4);
   static constexpr int kBar = kScaleRing + SRING * kScale;
-  // full, empty per stage; rfull, rempty per region; sfull, sempty per scale entry; done
-  static constexpr int kNumBars = 2 * kStages + 2 * kRegions + 2 * SRING + 1;
+  // full, empty per stage; rfull, rempty per region; sfull, sempty per scale
+  // entry; (kShared) mfull, mempty per region, mrfull, mrempty per min entry; done
+  static constexpr int kNumBars = 2 * kStages + 2 * kRegions + 2 * SRING + (kShared ? 2 * kRegions + 2 * kMR : 0) + 1;
   static constexpr int kSlot = kBar + kNumBars * 8;
   static constexpr int kBytes = kSlot + 16 + 1024;
-  static_assert(kA % 1024 == 0 && kStage % 1024 == 0, "stage buffers must keep 1 KB alignment");
+  static_assert(kA % 1024 == 0 && kStage % 1024 == 0 && kMinEntry % 1024 == 0,
+                "stage and min buffers must keep 1 KB alignment");
   static_assert(kBytes <= 227 * 1024, "shared memory budget");
-  static_assert(kRegions * kN * (kQ4 ? 2 : 1) <= TMEM_COLS, "TMEM columns");
+  static_assert(kRegions * kN * (kQ4 && !kShared ? 2 : 1) <= TMEM_COLS, "TMEM columns");
 };
+
+// y[c / 2] += s[c] * T[lane][ta + c] for this thread's CW columns c of a TMEM
+// region (s negated for kNeg), kG = 32 or 64 columns per TMEM wait (32 holds
+// fewer registers, for the variant whose epilogue has 192).
+template <int CW, bool kNeg, int kG>
+__device__ __forceinline__ void fold_region(uint32_t ta, const float4 *s4, float2 (&y)[CW / 2]) {
+  static_assert(kG == 32 || kG == 64, "32 or 64 columns per wait");
+#pragma unroll
+  for (int g = 0; g < CW / kG; ++g) {
+    uint32_t r0[32], r1[32];
+    tmem_ld_32x32b_x32(ta + g * kG, r0);
+    if (kG == 64) tmem_ld_32x32b_x32(ta + g * kG + 32, r1);
+    tmem_wait_ld(r0);
+    if (kG == 64) reg_fence(r1);
+#pragma unroll
+    for (int i = 0; i < kG / 4; ++i) {
+      float4 d = s4[g * (kG / 4) + i];
+      if (kNeg) d = make_float4(-d.x, -d.y, -d.z, -d.w);
+      const uint32_t(&rr)[32] = i < 8 ? r0 : r1;
+      const int q = (i & 7) * 4;
+      float2 &y0 = y[g * (kG / 2) + 2 * i], &y1 = y[g * (kG / 2) + 2 * i + 1];
+      y0 = __ffma2_rn(make_float2(d.x, d.y), make_float2(__uint_as_float(rr[q]), __uint_as_float(rr[q + 1])), y0);
+      y1 = __ffma2_rn(make_float2(d.z, d.w), make_float2(__uint_as_float(rr[q + 2]), __uint_as_float(rr[q + 3])), y1);
+    }
+  }
+}
 
 template <bool kQ4, bool kWide>
 __global__ void __launch_bounds__(SplitShape::kThreads, 1)
@@ -1271,10 +1311,17 @@ __global__ void __launch_bounds__(SplitShape::kThreads, 1)
   auto rempty = [&](int r) { return bar + 8u * (2 * STAGES + NR + r); };
   auto sfull = [&](int e) { return bar + 8u * (2 * STAGES + 2 * NR + e); };
   auto sempty = [&](int e) { return bar + 8u * (2 * STAGES + 2 * NR + SRING + e); };
-  const uint32_t done = bar + 8u * (2 * STAGES + 2 * NR + 2 * SRING);
+  constexpr bool SH = L::kShared;
+  constexpr int MR = L::kMR;
+  auto mfull = [&](int r) { return bar + 8u * (2 * STAGES + 2 * NR + 2 * SRING + r); };
+  auto mempty = [&](int r) { return bar + 8u * (2 * STAGES + 3 * NR + 2 * SRING + r); };
+  auto mrfull = [&](int m) { return bar + 8u * (2 * STAGES + 4 * NR + 2 * SRING + m); };
+  auto mrempty = [&](int m) { return bar + 8u * (2 * STAGES + 4 * NR + 2 * SRING + MR + m); };
+  const uint32_t done = bar + 8u * (L::kNumBars - 1);
   auto a_smem = [&](int s) { return base + s * L::kStage; };
   auto b_smem = [&](int s) { return base + s * L::kStage + L::kA; };
   auto s_smem = [&](int e) { return base + L::kScaleRing + e * L::kScale; };
+  auto m_smem = [&](int m) { return base + L::kMinRing + m * L::kMinEntry; };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -1289,6 +1336,16 @@ __global__ void __launch_bounds__(SplitShape::kThreads, 1)
       mbar_init(sfull(e), 1);
       mbar_init(sempty(e), EPI_WARPS);
     }
+    if constexpr (SH) {
+      for (int r = 0; r < NR; ++r) {
+        mbar_init(mfull(r), 1);
+        mbar_init(mempty(r), EPI_WARPS);
+      }
+      for (int m = 0; m < MR; ++m) {
+        mbar_init(mrfull(m), 1);
+        mbar_init(mrempty(m), 1);
+      }
+    }
     mbar_init(done, 1);
     fence_mbar_init();
   }
@@ -1301,11 +1358,11 @@ __global__ void __launch_bounds__(SplitShape::kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *reinterpret_cast<volatile uint32_t *>(smem + L::kSlot);
   if (warp >= PRODUCER_WARP) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(S::kRegsCtl));
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(SplitRegs<L::kShared>::kCtl));
   if (warp == PRODUCER_WARP) {
     // ------------------------------------------------------------ producer
     griddep_wait();  // the activation blocks come from the kernel before this one
-    uint32_t ks = 0, ns = 0, issued = 0, s_issued = 0;
+    uint32_t ks = 0, ns = 0, issued = 0, s_issued = 0, m_issued = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
       const int tt = tile % n_tt, og = tile / n_tt;
@@ -1321,12 +1378,26 @@ __global__ void __launch_bounds__(SplitShape::kThreads, 1)
         }
         __syncwarp();
         s_issued = ns + 1;
+        if constexpr (SH) {  // the min images of this super-block, into their own ring
+          const int m = static_cast<int>(ns % MR);
+          ok = __all_sync(0xffffffffu, mbar_wait(mrempty(m), ((ns / MR) & 1) ^ 1, wctl));
+          if (!ok) break;
+          if (lane == 3) {
+            mbar_arrive_expect_tx(mrfull(m), L::kMinEntry);
+            bulk_load(m_smem(m), aplane + as_block(tt, sb, 1, nsb, kQ4) + kSplitMin, kMinBytes, mrfull(m));
+            for (int w = 0; w < NW; ++w)
+              bulk_load(m_smem(m) + (1 + w) * kMinBytes, bplane + b_block(wtile(og, w), sb, 1, nsb, kQ4) + kBMin,
+                        kMinBytes, mrfull(m));
+          }
+          __syncwarp();
+          m_issued = ns + 1;
+        }
         for (int qq = 0; qq < 4; ++qq, ++ks) {  // 64-K quarters of the super-block
           const int s = static_cast<int>(ks % STAGES);
           ok = __all_sync(0xffffffffu, mbar_wait(empty(s), ((ks / STAGES) & 1) ^ 1, wctl));
           if (!ok) break;
           const int half = qq >> 1, kb = qq & 1;
-          const bool mins = kQ4 && qq == 3;
+          const bool mins = kQ4 && !SH && qq == 3;
           const uint8_t *ablk = aplane + as_block(tt, sb, half, nsb, kQ4);
           if (lane == 0) {
             mbar_arrive_expect_tx(full(s), kSplitQuarter + NW * L::kBK + (mins ? L::kMinA + L::kMinB : 0));
@@ -1349,6 +1420,9 @@ __global__ void __launch_bounds__(SplitShape::kThreads, 1)
         mbar_wait(full(k % STAGES), (k / STAGES) & 1, wctl, false);
       for (uint32_t k = s_issued > SRING ? s_issued - SRING : 0; k < s_issued; ++k)
         mbar_wait(sfull(k % SRING), (k / SRING) & 1, wctl, false);
+      if constexpr (SH)
+        for (uint32_t k = m_issued > MR ? m_issued - MR : 0; k < m_issued; ++k)
+          mbar_wait(mrfull(k % MR), (k / MR) & 1, wctl, false);
     }
   } else if (warp == ISSUER_WARP) {
     // ------------------------------------------------------------ UMMA issuer
@@ -1359,17 +1433,56 @@ __global__ void __launch_bounds__(SplitShape::kThreads, 1)
     constexpr uint64_t kStageDesc = L::kStage >> 4;
     const uint64_t ah0 = sdesc_kmajor_sw128(a_smem(0)), al0 = sdesc_kmajor_sw128(a_smem(0) + kSplitLo);
     const uint64_t b0 = sdesc_kmajor_sw128(b_smem(0));
-    const uint64_t am0 = sdesc_kmajor_sw32(a_smem(0) + kSplitQuarter);
-    const uint64_t bm0 = sdesc_kmajor_sw32(b_smem(0) + NW * L::kBK);
+    const uint64_t am0 = sdesc_kmajor_sw32(SH ? m_smem(0) : a_smem(0) + kSplitQuarter);
+    const uint64_t bm0 = sdesc_kmajor_sw32(SH ? m_smem(0) + kMinBytes : b_smem(0) + NW * L::kBK);
     uint32_t ks = 0, nr = 0;
     bool ok = true;
+    // kShared: super-blocks below pmin have their min UMMA issued.  Min term n
+    // goes into region n % NR after the epilogue has read accumulator n there
+    // (rempty), and must be read (mempty) before accumulator n + NR starts.
+    uint32_t pmin = 0;
+    auto issue_min = [&](uint32_t n) {
+      if constexpr (!SH) return;
+      const int r = static_cast<int>(n % NR), m = static_cast<int>(n % (SH ? MR : 1));
+      ok = __all_sync(0xffffffffu, mbar_wait(rempty(r), (n / NR) & 1, wctl));
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(mrfull(m), (n / (SH ? MR : 1)) & 1, wctl));
+      if (!ok) return;
+      tc_fence_after();
+      if (elected) {
+        const uint64_t mo = static_cast<uint64_t>(m) * (L::kMinEntry >> 4);
+        umma_f16(tbase + r * L::kN, am0 + mo, bm0 + mo, idesc, 0u);
+        umma_commit(mfull(r));
+        umma_commit(mrempty(m));
+      }
+      __syncwarp();
+    };
     for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
       for (int64_t sb = 0; sb < nsb && ok; ++sb, ++nr) {
         const int r = static_cast<int>(nr % NR);
-        ok = __all_sync(0xffffffffu, mbar_wait(rempty(r), ((nr / NR) & 1) ^ 1, wctl));
+        if constexpr (SH) {
+          while (ok && pmin + NR <= nr) issue_min(pmin++);  // the region's last min term goes first
+          if (ok) ok = __all_sync(0xffffffffu, mbar_wait(mempty(r), ((nr / NR) & 1) ^ 1, wctl));
+        } else {
+          ok = __all_sync(0xffffffffu, mbar_wait(rempty(r), ((nr / NR) & 1) ^ 1, wctl));
+        }
         if (!ok) break;
         const uint32_t dacc = tbase + r * L::kN, dmin = tbase + (NR + r) * L::kN;
         for (int qq = 0; qq < 4 && ok; ++qq, ++ks) {
+          if constexpr (SH) {
+            // The previous super-block's min term: after this one's first
+            // stage if its region was read by then, at the latest after the
+            // second.  The issuer runs stages ahead of the tensor pipe; waiting
+            // longer would queue the min term behind most of this super-block
+            // and keep its region from the next accumulator.
+            if (pmin < nr && qq >= 1) {
+              const uint32_t n = pmin;
+              if (qq >= 2 || __all_sync(0xffffffffu, mbar_test_wait(rempty(n % NR), (n / NR) & 1))) {
+                issue_min(n);
+                ++pmin;
+                if (!ok) break;
+              }
+            }
+          }
           const int s = static_cast<int>(ks % STAGES);
           ok = __all_sync(0xffffffffu, mbar_wait(full(s), (ks / STAGES) & 1, wctl));
           if (!ok) break;
@@ -1384,7 +1497,7 @@ __global__ void __launch_bounds__(SplitShape::kThreads, 1)
               umma_f16(dacc, al0 + off, b0 + off, idesc, 1u);
               umma_f16(dacc, al0 + off + 2, b0 + off + 2, idesc, 1u);
             }
-            if (kQ4 && qq == 3) umma_f16(dmin, am0 + so, bm0 + so, idesc, 0u);
+            if (kQ4 && !SH && qq == 3) umma_f16(dmin, am0 + so, bm0 + so, idesc, 0u);
             umma_commit(empty(s));
             if (qq == 3) umma_commit(rfull(r));
           }
@@ -1392,12 +1505,14 @@ __global__ void __launch_bounds__(SplitShape::kThreads, 1)
         }
       }
     }
+    if constexpr (SH)
+      while (ok && pmin < nr) issue_min(pmin++);
     if (elected) umma_commit(done);
     __syncwarp();
     mbar_wait(done, 0, wctl, false);
   }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(S::kRegsEpi));
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(SplitRegs<L::kShared>::kEpi));
     // ------------------------------------------------------------ epilogue
     // warp w: TMEM lanes 32*(w%4).., columns (w/4)*kN/2 .. of a region
     constexpr int CW = L::kN / 2;  // columns per warp
@@ -1425,49 +1540,27 @@ __global__ void __launch_bounds__(SplitShape::kThreads, 1)
         tc_fence_after();
         const uint8_t *sblk = smem + (s_smem(e) - base) + (kWide ? chalf * scale_block_bytes(kQ4) : 0);
         const float4 *d4 = reinterpret_cast<const float4 *>(sblk) + (kWide ? 0 : chalf * 16);
-#pragma unroll
-        for (int g = 0; g < CW / 64; ++g) {  // 64 columns at a time
-          uint32_t r0[32], r1[32];
-          tmem_ld_32x32b_x32(taddr + r * L::kN + g * 64, r0);
-          tmem_ld_32x32b_x32(taddr + r * L::kN + g * 64 + 32, r1);
-          tmem_wait_ld(r0);
-          reg_fence(r1);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float4 d = d4[g * 16 + i];
-            const uint32_t(&rr)[32] = i < 8 ? r0 : r1;
-            const int q = (i & 7) * 4;
-            float2 &y0 = y[g * 32 + 2 * i], &y1 = y[g * 32 + 2 * i + 1];
-            y0 = __ffma2_rn(make_float2(d.x, d.y), make_float2(__uint_as_float(rr[q]), __uint_as_float(rr[q + 1])), y0);
-            y1 = __ffma2_rn(make_float2(d.z, d.w), make_float2(__uint_as_float(rr[q + 2]), __uint_as_float(rr[q + 3])), y1);
-          }
-        }
+        fold_region<CW, false, SH ? 32 : 64>(taddr + r * L::kN, d4, y);
         if (kQ4) {
-          const float4 *m4 = reinterpret_cast<const float4 *>(sblk + kSDmin) + (kWide ? 0 : chalf * 16);
-#pragma unroll
-          for (int g = 0; g < CW / 64; ++g) {
-            uint32_t r0[32], r1[32];
-            tmem_ld_32x32b_x32(taddr + (NR + r) * L::kN + g * 64, r0);
-            tmem_ld_32x32b_x32(taddr + (NR + r) * L::kN + g * 64 + 32, r1);
-            tmem_wait_ld(r0);
-            reg_fence(r1);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float4 dm = m4[g * 16 + i];
-              const uint32_t(&rr)[32] = i < 8 ? r0 : r1;
-              const int q = (i & 7) * 4;
-              float2 &y0 = y[g * 32 + 2 * i], &y1 = y[g * 32 + 2 * i + 1];
-              y0 = __ffma2_rn(make_float2(-dm.x, -dm.y), make_float2(__uint_as_float(rr[q]), __uint_as_float(rr[q + 1])), y0);
-              y1 = __ffma2_rn(make_float2(-dm.z, -dm.w), make_float2(__uint_as_float(rr[q + 2]), __uint_as_float(rr[q + 3])), y1);
-            }
+          uint32_t mreg = static_cast<uint32_t>(NR + r) * L::kN;
+          if constexpr (SH) {  // the accumulator's region goes back, its min term comes into it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(rempty(r));
+            ok = __all_sync(0xffffffffu, mbar_wait(mfull(r), (nr / NR) & 1, wctl));
+            if (!ok) break;
+            tc_fence_after();
+            mreg = static_cast<uint32_t>(r) * L::kN;
           }
+          const float4 *m4 = reinterpret_cast<const float4 *>(sblk + kSDmin) + (kWide ? 0 : chalf * 16);
+          fold_region<CW, true, SH ? 32 : 64>(taddr + mreg, m4, y);
         }
         // the region and the scale entry go back
         tc_fence_before();
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(rempty(r));
+          mbar_arrive(SH ? mempty(r) : rempty(r));
           mbar_arrive(sempty(e));
         }
       }
@@ -1695,23 +1788,67 @@ cudaError_t launch_gemm(const mmq_weights_s *h, const uint8_t *Q, const float *X
 }
 
 // ---------------------------------------------------------------- split arm launch
-size_t gemm_split_scratch_bytes(const mmq_weights_s *h, int64_t nt) {
-  const bool q4 = h->type == MMQ_Q4_K;
-  const int64_t n_tt = (nt + kTileM - 1) / kTileM;
-  const size_t a = static_cast<size_t>(n_tt * h->nsb) * as_pair_bytes(q4);
-  return (a + 255) / 256 * 256 + static_cast<size_t>(n_tt * kTileM) * 4;
+namespace {
+
+// Launch shape and scratch layout of one split-arm GEMM: whole tiles of 128
+// or 256 weight rows per CTA, whichever gives the busiest CTA the least time
+// by the per-super-block costs measured on the GB300 (clk, one CTA per SM): a
+// 128 x 128 super-block is bound by operand ingest at ~3150, a 128 x 256 one
+// by the tensor pipe at ~4100 (q6_K) and ~4450 (q4_K, with its min term).
+// (Stream-K over these tiles measured slower on the 3584 x 3584 x 512 shapes:
+// the groups' first super-blocks pull most of the working set from HBM at
+// once, the 128-row tiles are bound by the L2's total bandwidth rather than
+// by the SM count, and the owner's read of the other pieces' partial sums is
+// latency-bound.)
+struct SplitPlan {
+  bool q4, wide;
+  int64_t n_tt, nt_pad, nsb;
+  int n_ot, n_tiles, grid;
+  size_t inv_off, bytes;
+};
+
+SplitPlan plan_split(const mmq_weights_s *h, int64_t nt) {
+  SplitPlan p{};
+  p.q4 = h->type == MMQ_Q4_K;
+  p.n_tt = (nt + kTileM - 1) / kTileM;
+  p.nt_pad = p.n_tt * kTileM;
+  p.nsb = h->nsb;
+  p.n_ot = static_cast<int>(h->od_pad / kTileN);
+  const int64_t sms = num_sms(h->device);
+  int64_t best = -1;
+  for (int wide = 0; wide < 2; ++wide) {
+    const int64_t cost = wide ? (p.q4 ? 4450 : 4100) : 3150;
+    const int64_t tiles = p.n_tt * (wide ? (p.n_ot + 1) / 2 : p.n_ot);
+    const int64_t est = (tiles + sms - 1) / sms * cost;
+    if (best < 0 || est < best) {
+      best = est;
+      p.wide = wide;
+      p.n_tiles = static_cast<int>(tiles);
+      p.grid = static_cast<int>(tiles < sms ? tiles : sms);
+    }
+  }
+  p.inv_off = (static_cast<size_t>(p.n_tt * p.nsb) * as_pair_bytes(p.q4) + 255) / 256 * 256;
+  p.bytes = p.inv_off + static_cast<size_t>(p.nt_pad) * 4;
+  return p;
 }
+
+}  // namespace
+
+size_t gemm_split_scratch_bytes(const mmq_weights_s *h, int64_t nt) { return plan_split(h, nt).bytes; }
+
+bool gemm_split_wide(const mmq_weights_s *h, int64_t nt) { return plan_split(h, nt).wide; }
 
 cudaError_t launch_gemm_split(const mmq_weights_s *h, const uint8_t *Q, const float *X, int64_t nt, float *Y,
                               void *scratch, DevStatus *st, unsigned epoch, uint64_t limit_ns,
                               cudaStream_t s, cudaEvent_t ev0, cudaEvent_t ev1, unsigned ev_flags) {
-  const bool q4 = h->type == MMQ_Q4_K;
-  const int64_t n_tt = (nt + kTileM - 1) / kTileM, nt_pad = n_tt * kTileM, nsb = h->nsb, nb32 = h->nb32;
-  const int n_ot = static_cast<int>(h->od_pad / kTileN);
-  const int n_tiles = static_cast<int>(n_tt) * n_ot;
-  uint8_t *aplane = static_cast<uint8_t *>(scratch);
+  const SplitPlan p = plan_split(h, nt);
+  const bool q4 = p.q4, wide = p.wide;
+  const int64_t n_tt = p.n_tt, nt_pad = p.nt_pad, nsb = p.nsb, nb32 = h->nb32;
+  const int n_ot = p.n_ot;
+  uint8_t *base8 = static_cast<uint8_t *>(scratch);
+  uint8_t *aplane = base8;
   const size_t a_bytes = static_cast<size_t>(n_tt * nsb) * as_pair_bytes(q4);
-  float *invp = reinterpret_cast<float *>(aplane + (a_bytes + 255) / 256 * 256);
+  float *invp = reinterpret_cast<float *>(base8 + p.inv_off);
   const int dev = h->device;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   cudaError_t e = cudaSuccess;
@@ -1743,17 +1880,9 @@ cudaError_t launch_gemm_split(const mmq_weights_s *h, const uint8_t *Q, const fl
   if (ev0 && (e = cudaEventRecordWithFlags(ev0, s, ev_flags)) != cudaSuccess) return e;
   const uint8_t *bp = static_cast<const uint8_t *>(h->bplane);
   const uint8_t *bs = bp + b_scale_region(n_ot, nsb, q4);
-  const int sms = num_sms(dev);
-  // q6_K tiles of 256 weight rows when they still give one and a half waves
-  // (q4_K keeps 128: with its min-term regions a 256-wide accumulator cannot be
-  // double-buffered in TMEM, and measured slower: 584 against 520 us on the
-  // 18944 x 3584 x 2630 workload)
-  const int n_wide = static_cast<int>(n_tt) * ((n_ot + 1) / 2);
-  const bool wide = !q4 && 2 * n_wide >= 3 * sms;
-  const int tiles = wide ? n_wide : n_tiles;
-  const int grid = tiles < sms ? tiles : sms;
+  const int grid = p.grid;
   auto go = [&](auto kern, int smem, int variant) -> cudaError_t {
-    static std::atomic<int> ready[3][64];  // per kernel variant: 0 unknown, 1 ready, 2 unusable
+    static std::atomic<int> ready[4][64];  // per kernel variant: 0 unknown, 1 ready, 2 unusable
     std::atomic<int> &rd = ready[variant][dev];
     int stt = rd.load();
     if (stt == 0) {
@@ -1779,7 +1908,8 @@ cudaError_t launch_gemm_split(const mmq_weights_s *h, const uint8_t *Q, const fl
                               static_cast<const float *>(invp), nt, h->od, nb32, static_cast<int>(n_tt), n_ot, Y, w);
   };
   if (q4)
-    e = go(mmq_gemm_split_kernel<true, false>, SplitSmem<true, false>::kBytes, 0);
+    e = wide ? go(mmq_gemm_split_kernel<true, true>, SplitSmem<true, true>::kBytes, 3)
+             : go(mmq_gemm_split_kernel<true, false>, SplitSmem<true, false>::kBytes, 0);
   else
     e = wide ? go(mmq_gemm_split_kernel<false, true>, SplitSmem<false, true>::kBytes, 1)
              : go(mmq_gemm_split_kernel<false, false>, SplitSmem<false, false>::kBytes, 2);

@@ -67,6 +67,8 @@ cudaError_t launch_gemm(const mmq_weights_s *h, const uint8_t *Q, const float *X
 // Split arm (activation scale folded into A as an exact fp16 hi + lo pair):
 // scratch bytes, and the prepass + GEMM launch (whole tiles).
 size_t gemm_split_scratch_bytes(const mmq_weights_s *h, int64_t nt);
+// whether the split arm would run 256-row weight tiles for this many tokens
+bool gemm_split_wide(const mmq_weights_s *h, int64_t nt);
 cudaError_t launch_gemm_split(const mmq_weights_s *h, const uint8_t *Q, const float *X, int64_t nt, float *Y,
                               void *scratch, DevStatus *st, unsigned epoch, uint64_t limit_ns,
                               cudaStream_t s, cudaEvent_t ev0, cudaEvent_t ev1, unsigned ev_flags);

@@ -420,6 +420,10 @@ SPLIT_SHAPES = [
     ("q4_K", 131, 256, 1, 44),
     ("q4_K", 384, 1024, 256, 45),
     ("q6_K", 1000, 4096, 300, 46),
+    # 27 weight tiles, 14 super-blocks, ragged tokens
+    ("q6_K", 3456, 3584, 300, 47),
+    # 28 super-blocks per tile: the min term's region hand-off over a long tile
+    ("q4_K", 896, 7168, 200, 48),
 ]
 
 
@@ -463,8 +467,9 @@ def test_split_arm_workloads_sampled(mmq, cfg):
 @pytest.mark.parametrize("name", ["q6_K", "q4_K"])
 @pytest.mark.parametrize("od", [3584, 3456])   # 28 weight tiles, and 27 (the last pair repeats a tile)
 def test_split_arm_wide_tiles(mmq, name, od):
-    """Enough tiles for the split arm's 256-row tiles (q6_K; q4_K keeps 128-row
-    tiles on the same shape)."""
+    """Enough tiles for the split arm's 256-row tiles (for q4_K the min term then
+    shares the accumulator's TMEM region); two super-blocks per tile, so a CTA
+    carries the pending min term across tile boundaries."""
     id_, nt = 512, 2176
     W = gen.weights(name, od, id_, seed=81 + od)
     X = gen.activations(nt, id_, seed=82 + od, outlier_p=0.01, outlier_scale=20.0)
