@@ -339,6 +339,54 @@ def test_gemm_f32_matches_quantize_then_gemm(mmq, name, od, id_, nt, seed):
     w.release()
 
 
+def _tie_blocks(nt, id_, seed):
+    """Activation rows whose q8_0 quotients x / d sit on half-integers, one ulp
+    beside them, and just inside and outside 1e-4 of them, for block scales
+    from 1e-3 to 7e4 (d = 1 exactly when amax = 127); every block's first value
+    is +-amax."""
+    rng = np.random.default_rng(seed)
+    X = rng.standard_normal((nt, id_)).astype(np.float32)
+    one = np.float32(1)
+    for t in range(nt):
+        for c in range(id_ // 32):
+            kind = (t * 7 + c) % 5
+            amax = np.float32(rng.choice([127.0, 1.2345, 3.0e-3, 7.7e4, 0.5]))
+            d = np.float32(amax / np.float32(127))
+            x = ((rng.integers(-126, 126, size=31) + 0.5).astype(np.float32) * d).astype(np.float32)
+            if kind == 1:
+                x = np.nextafter(x, np.float32(np.inf))
+            elif kind == 2:
+                x = np.nextafter(x, np.float32(-np.inf))
+            elif kind == 3:
+                x = (x * (one + np.float32(3e-6))).astype(np.float32)
+            elif kind == 4:
+                x = (x * (one - np.float32(3e-6))).astype(np.float32)
+            X[t, c * 32] = amax if rng.random() < 0.5 else -amax
+            X[t, c * 32 + 1:(c + 1) * 32] = x
+    return X
+
+
+@pytest.mark.parametrize("name", ["q4_K", "q6_K"])
+def test_fused_quantization_at_rounding_ties(mmq, name):
+    """The fused quantization rounds x * fl(1/d) and divides only within 1e-4 of
+    a half-integer; quotients on and around the ties must still give the
+    blocks of the dividing quantizer (and so the oracle's), on both arms."""
+    nt, od, id_ = 40, 256, 512
+    X = _tie_blocks(nt, id_, 90)
+    Xd = torch.from_numpy(X).cuda()
+    Q = mmq.mmq_quantize_act(Xd)
+    assert np.array_equal(Q.cpu().numpy(), oracle.quantize_q8_0(X))
+    W = gen.weights(name, od, id_, seed=91)
+    w = mmq.mmq_register_weights(name, torch.from_numpy(W).cuda(), od, id_)
+    for arm in (mmq.MMQ_ARM_F16, mmq.MMQ_ARM_SPLIT):
+        Y1 = mmq.mmq_gemm_f32(w, Xd, flags=arm)
+        Y2 = mmq.mmq_gemm(w, Q, nt, flags=arm)
+        torch.cuda.synchronize()
+        assert mmq.mmq_last_device_error() == 0
+        assert torch.equal(Y1, Y2), arm
+    w.release()
+
+
 # --------------------------------------------------------------------------
 # raw arm: packed weight bytes unpacked inside the GEMM
 RAW_SHAPES = [
