@@ -89,9 +89,11 @@ void free_planes(mmq_weights_s *h) {
   if (h->bplane) cudaFree(h->bplane);
   if (h->wexp) cudaFree(h->wexp);
   if (h->rawplane) cudaFree(h->rawplane);
+  if (h->b0plane) cudaFree(h->b0plane);
   h->bplane = nullptr;
   h->wexp = nullptr;
   h->rawplane = nullptr;
+  h->b0plane = nullptr;
 }
 
 }  // namespace
@@ -169,8 +171,15 @@ int mmq_register_weights(int type, const void *W, int64_t od, int64_t id, uint32
   int bad_h = 0;
   if (e == cudaSuccess) e = cudaMemcpy(&bad_h, bad, sizeof(int), cudaMemcpyDeviceToHost);
   if (bad) cudaFree(bad);
+  // q6_K sub-block scales beyond +-64: a second pass splits the operand into
+  // the B1 plane and the B0 plane
+  if (e == cudaSuccess && bad_h) {
+    h->b0plane_bytes = mmq::bplane_operand_bytes(type, od, id);
+    e = cudaMalloc(reinterpret_cast<void **>(&h->b0plane), h->b0plane_bytes);
+    if (e == cudaSuccess) e = mmq::launch_register_b0(h, static_cast<const uint8_t *>(W), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  }
   if (e != cudaSuccess) rc = cuda_rc(e);
-  if (rc == MMQ_OK && bad_h) rc = MMQ_ERR_UNSUPPORTED;
   if (rc != MMQ_OK) {
     free_planes(h);
     delete h;
@@ -221,7 +230,7 @@ int mmq_weights_info(mmq_weights_t h, int *type, int64_t *od, int64_t *id,
   if (od) *od = h->od;
   if (id) *id = h->id;
   const int64_t operand = static_cast<int64_t>(mmq::bplane_operand_bytes(h->type, h->od, h->id));
-  if (operand_bytes) *operand_bytes = operand;
+  if (operand_bytes) *operand_bytes = operand + static_cast<int64_t>(h->b0plane_bytes);
   if (scale_bytes) *scale_bytes = static_cast<int64_t>(h->bplane_bytes) - operand;
   if (wexp_bytes) *wexp_bytes = static_cast<int64_t>(h->wexp_bytes);
   return MMQ_OK;
@@ -234,12 +243,14 @@ static int gemm_impl(mmq_weights_t h, const void *Q, const float *X, int64_t nt,
   if (!h || nt < 0 || nt > kMaxTokens) return MMQ_ERR_ARG;
   if (flags != MMQ_ARM_AUTO && flags != MMQ_ARM_F16 && flags != MMQ_ARM_RAW && flags != MMQ_ARM_SPLIT)
     return MMQ_ERR_UNSUPPORTED;
-  if (flags == MMQ_ARM_RAW && !h->rawplane) return MMQ_ERR_UNSUPPORTED;
-  // library choice: the split arm for q6_K, and for q4_K where it runs 256-row tiles; else the
-  // fp16-plane arm (measured fastest on the q-proj and FFN workloads of each type)
+  if (flags == MMQ_ARM_RAW && (!h->rawplane || h->b0plane)) return MMQ_ERR_UNSUPPORTED;
+  // library choice: the split arm for one-plane q6_K, and for q4_K where it runs 256-row tiles;
+  // else the fp16-plane arm (measured fastest on the q-proj and FFN workloads of each kind; a
+  // two-plane q6_K operand doubles the split arm's tensor work but hides in the other's hand-off)
   const bool raw = flags == MMQ_ARM_RAW;
   const bool split = flags == MMQ_ARM_SPLIT ||
-                     (flags == MMQ_ARM_AUTO && (h->type == MMQ_Q6_K || mmq::gemm_split_wide(h, nt)));
+                     (flags == MMQ_ARM_AUTO && ((h->type == MMQ_Q6_K && !h->b0plane) ||
+                                                (h->type == MMQ_Q4_K && mmq::gemm_split_wide(h, nt))));
   if (arm_used) *arm_used = raw ? MMQ_ARM_RAW : split ? MMQ_ARM_SPLIT : MMQ_ARM_F16;
   if (nt == 0) return MMQ_OK;
   const void *A = X ? static_cast<const void *>(X) : Q;

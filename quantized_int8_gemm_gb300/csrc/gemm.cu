@@ -80,9 +80,9 @@ constexpr int TMEM_COLS = SLOTS * kTileN;  // 512
 // kRegsLaunch per thread; warpgroup 2 (and the raw arm's converter
 // warpgroup 3) drop to kRegsCtl and the two epilogue warpgroups rise to
 // kRegsEpi, using the whole register file the launch holds.
-template <bool kRaw>
+template <bool kRaw, bool kB0 = false>
 struct Shape {
-  static constexpr int kStages = kRaw ? 2 : 3;
+  static constexpr int kStages = kB0 ? 4 : kRaw ? 2 : 3;
   static constexpr int kThreads = kRaw ? 512 : 384;
   static constexpr int kRegsLaunch = kRaw ? 128 : 168;
   static constexpr int kRegsEpi = kRaw ? 208 : 224;
@@ -92,11 +92,16 @@ struct Shape {
                 "the register split must add up to what the launch holds");
 };
 
-template <bool kQ4, bool kRaw>
+// kB0 (q6_K with |sc| > 64): stages of 64 K (one K-block of A, B1 and B0,
+// 16 KB each; four in the ring), each taken by one issuer; otherwise stages
+// of 128 K (a half super-block).
+template <bool kQ4, bool kRaw, bool kB0 = false>
 struct Smem {
-  using S = Shape<kRaw>;
-  static constexpr int kA = a_odd_bytes(kQ4);                          // A region per stage
-  static constexpr int kB = ((b_odd_bytes(kQ4) + 1023) / 1024) * 1024;  // B region per stage
+  using S = Shape<kRaw, kB0>;
+  static constexpr int kKB = kTileM * 64 * 2;  // one 64-K block of a tile: 16384
+  static constexpr int kA = kB0 ? kKB : a_odd_bytes(kQ4);                                // A region per stage
+  static constexpr int kB = kB0 ? 2 * kKB : ((b_odd_bytes(kQ4) + 1023) / 1024) * 1024;  // B region per stage
+  static constexpr int kB0Off = kKB;  // the B0 K-block after the B1 one
   static constexpr int kStage = kA + kB;
   static constexpr int kRaw_ = ((raw_block_bytes(kQ4) + 127) / 128) * 128;  // one raw ring entry
   static constexpr int kRawRing = S::kStages * kStage;
@@ -744,16 +749,17 @@ __device__ __forceinline__ void store_y_row(float *__restrict__ Y, int64_t t, in
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
-template <bool kQ4, bool kSK, bool kRaw>
+template <bool kQ4, bool kSK, bool kRaw, bool kB0>
 __global__ void __launch_bounds__(Shape<kRaw>::kThreads, 1)
     mmq_gemm_kernel(const uint8_t *__restrict__ aplane, const uint8_t *__restrict__ bplane,
-                    const uint8_t *__restrict__ rawplane,
+                    const uint8_t *__restrict__ rawplane, const uint8_t *__restrict__ b0plane,
                     const uint8_t *__restrict__ bscale, const float *__restrict__ dap,
                     const float *__restrict__ invp, int64_t nt, int64_t od, int64_t nb32, int n_tt,
                     int n_ot, float *__restrict__ Y, WaitCtl wctl, float4 *__restrict__ ws,
                     uint64_t *__restrict__ flags) {
-  using L = Smem<kQ4, kRaw>;
-  using S = Shape<kRaw>;
+  static_assert(!kB0 || (!kQ4 && !kRaw), "the B0 plane is q6_K's, read from the registered planes");
+  using L = Smem<kQ4, kRaw, kB0>;
+  using S = Shape<kRaw, kB0>;
   constexpr int STAGES = S::kStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
@@ -783,7 +789,7 @@ __global__ void __launch_bounds__(Shape<kRaw>::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full(s), 1);
-      mbar_init(empty(s), ISSUERS);  // one commit per issuer frees a stage
+      mbar_init(empty(s), kB0 ? 1 : ISSUERS);  // one commit per issuer (kB0: its one issuer) frees a stage
     }
     for (uint32_t i = 0; i < SLOTS; ++i) {
       mbar_init(rfull(i), 1);
@@ -840,36 +846,56 @@ __global__ void __launch_bounds__(Shape<kRaw>::kThreads, 1)
         }
         __syncwarp();
         s_issued = ns + 1;
-        for (int half = 0; half < 2; ++half, ++ks) {
-          if (kRaw) {  // the raw weight block first: its ring runs ahead of the stages
-            const int re = static_cast<int>(ks % RRING);
-            ok = __all_sync(0xffffffffu, mbar_wait(rawempty(re), ((ks / RRING) & 1) ^ 1, wctl));
+        if constexpr (kB0) {  // four 64-K stages per super-block: A, B1 and B0 K-blocks
+          for (int q = 0; q < 4 && ok; ++q, ++ks) {
+            const int half = q >> 1, kb = q & 1;
+            const int s = static_cast<int>(ks % STAGES);
+            ok = __all_sync(0xffffffffu, mbar_wait(empty(s), ((ks / STAGES) & 1) ^ 1, wctl));
             if (!ok) break;
-            if (lane == 3) {
-              mbar_arrive_expect_tx(rawfull(re), raw_block_bytes(kQ4));
-              bulk_load(raw_smem(re), rawplane + raw_block(ot, sb, half, nsb, kQ4), raw_block_bytes(kQ4),
-                        rawfull(re));
+            const uint32_t ko = static_cast<uint32_t>(kb) * L::kKB;
+            if (lane == 0) {
+              mbar_arrive_expect_tx(full(s), 3 * L::kKB);
+              bulk_load(a_smem(s), aplane + a_block(tt, sb, half, nsb, false) + ko, L::kKB, full(s));
+            } else if (lane == 1) {
+              bulk_load(b_smem(s), bplane + b_block(ot, sb, half, nsb, false) + ko, L::kKB, full(s));
+            } else if (lane == 3) {
+              bulk_load(b_smem(s) + L::kB0Off, b0plane + b_block(ot, sb, half, nsb, false) + ko, L::kKB, full(s));
             }
             __syncwarp();
-            r_issued = ks + 1;
+            issued = ks + 1;
           }
-          const int s = static_cast<int>(ks % STAGES);
-          ok = __all_sync(0xffffffffu, mbar_wait(empty(s), ((ks / STAGES) & 1) ^ 1, wctl));
-          if (!ok) break;
-          const uint32_t ab = half ? a_odd_bytes(kQ4) : a_even_bytes();
-          // raw arm: only the q4_K min image of the weight block is copied
-          const uint32_t bb = kRaw ? ((kQ4 && half) ? kMinBytes : 0) : (half ? b_odd_bytes(kQ4) : b_even_bytes());
-          if (lane == 0) {
-            mbar_arrive_expect_tx(full(s), ab + bb);
-            bulk_load(a_smem(s), aplane + a_block(tt, sb, half, nsb, kQ4), ab, full(s));
-          } else if (lane == 1 && bb) {
-            if (kRaw)
-              bulk_load(b_smem(s) + kBMin, bplane + b_block(ot, sb, half, nsb, kQ4) + kBMin, bb, full(s));
-            else
-              bulk_load(b_smem(s), bplane + b_block(ot, sb, half, nsb, kQ4), bb, full(s));
+        } else {
+          for (int half = 0; half < 2; ++half, ++ks) {
+            if (kRaw) {  // the raw weight block first: its ring runs ahead of the stages
+              const int re = static_cast<int>(ks % RRING);
+              ok = __all_sync(0xffffffffu, mbar_wait(rawempty(re), ((ks / RRING) & 1) ^ 1, wctl));
+              if (!ok) break;
+              if (lane == 3) {
+                mbar_arrive_expect_tx(rawfull(re), raw_block_bytes(kQ4));
+                bulk_load(raw_smem(re), rawplane + raw_block(ot, sb, half, nsb, kQ4), raw_block_bytes(kQ4),
+                          rawfull(re));
+              }
+              __syncwarp();
+              r_issued = ks + 1;
+            }
+            const int s = static_cast<int>(ks % STAGES);
+            ok = __all_sync(0xffffffffu, mbar_wait(empty(s), ((ks / STAGES) & 1) ^ 1, wctl));
+            if (!ok) break;
+            const uint32_t ab = half ? a_odd_bytes(kQ4) : a_even_bytes();
+            // raw arm: only the q4_K min image of the weight block is copied
+            const uint32_t bb = kRaw ? ((kQ4 && half) ? kMinBytes : 0) : (half ? b_odd_bytes(kQ4) : b_even_bytes());
+            if (lane == 0) {
+              mbar_arrive_expect_tx(full(s), ab + bb);
+              bulk_load(a_smem(s), aplane + a_block(tt, sb, half, nsb, kQ4), ab, full(s));
+            } else if (lane == 1 && bb) {
+              if (kRaw)
+                bulk_load(b_smem(s) + kBMin, bplane + b_block(ot, sb, half, nsb, kQ4) + kBMin, bb, full(s));
+              else
+                bulk_load(b_smem(s), bplane + b_block(ot, sb, half, nsb, kQ4), bb, full(s));
+            }
+            __syncwarp();
+            issued = ks + 1;
           }
-          __syncwarp();
-          issued = ks + 1;
         }
       }
     }
@@ -928,7 +954,9 @@ __global__ void __launch_bounds__(Shape<kRaw>::kThreads, 1)
     const uint64_t am0 = sdesc_kmajor_sw32(a_smem(0) + kAMin), bm0 = sdesc_kmajor_sw32(b_smem(0) + kBMin);
     uint32_t ks = 0, j = 0;  // stages consumed, items issued
     bool ok = true;
-    // one item: wait for the slot, 1 or 2 UMMAs, commit on the slot
+    // one item: wait for the slot, 1 or 2 UMMAs (kB0: then the same A against
+    // the B0 image, so the chunk's partial sums B1 + B0), commit on the slot.
+    // Every partial of a chunk stays an integer below 32 * 127 * 4096 < 2^24.
     auto item = [&](uint64_t ad, uint64_t bd, bool two) {
       const uint32_t slot = 2 * iw + (j & 1);
       const bool got = __all_sync(0xffffffffu, mbar_wait(rempty(slot), ((j >> 1) & 1) ^ 1, wctl));
@@ -938,6 +966,11 @@ __global__ void __launch_bounds__(Shape<kRaw>::kThreads, 1)
           const uint32_t d = tbase + slot * kTileN;
           umma_f16(d, ad, bd, idesc, 0);
           if (two) umma_f16(d, ad + 2, bd + 2, idesc, 1);
+          if (kB0 && two) {
+            constexpr uint64_t kB0Desc = L::kB0Off >> 4;
+            umma_f16(d, ad, bd + kB0Desc, idesc, 1);
+            umma_f16(d, ad + 2, bd + kB0Desc + 2, idesc, 1);
+          }
           umma_commit(rfull(slot));
         }
         __syncwarp();
@@ -950,24 +983,43 @@ __global__ void __launch_bounds__(Shape<kRaw>::kThreads, 1)
     int64_t sb0, sb1;
     while (ok && work_next(wk, n_tiles, n_tt, nsb, tile, sb0, sb1)) {
       for (int64_t sb = sb0; sb < sb1 && ok; ++sb) {
-        for (int half = 0; half < 2 && ok; ++half, ++ks) {
-          const int s = static_cast<int>(ks % STAGES);
-          ok = __all_sync(0xffffffffu, mbar_wait(full(s), (ks / STAGES) & 1, wctl));
-          if (ok && kRaw) ok = __all_sync(0xffffffffu, mbar_wait(conv(s), (ks / STAGES) & 1, wctl));
-          if (!ok) break;
-          tc_fence_after();
-          const uint64_t as = a0 + s * kStageDesc, bs = b0 + s * kStageDesc;
+        if constexpr (kB0) {
+          // 64-K stage q = (half, kb) holds chunks 4*half + 2*kb + {0, 1}: issuer
+          // kb takes it, so issuer 0 still gets chunks 0, 1, 4, 5 and issuer 1
+          // chunks 2, 3, 6, 7 (the order the epilogue reads the slots in)
+          for (int q = 0; q < 4 && ok; ++q, ++ks) {
+            if ((q & 1) != iw) continue;
+            const int s = static_cast<int>(ks % STAGES);
+            ok = __all_sync(0xffffffffu, mbar_wait(full(s), (ks / STAGES) & 1, wctl));
+            if (!ok) break;
+            tc_fence_after();
+            const uint64_t as = a0 + s * kStageDesc, bs = b0 + s * kStageDesc;
 #pragma unroll
-          for (int q = 0; q < 2 && ok; ++q) {
-            const int lc = 2 * iw + q;  // chunk in the stage: K = 32*lc .. 32*lc+31
-            const uint64_t off = (lc >> 1) * (16384 >> 4) + (lc & 1) * (64 >> 4);
-            ok = item(as + off, bs + off, true);
+            for (int c = 0; c < 2 && ok; ++c) ok = item(as + c * (64 >> 4), bs + c * (64 >> 4), true);
+            if (!ok) break;
+            if (elected) umma_commit(empty(s));
+            __syncwarp();
           }
-          if (ok && kQ4 && half == 1 && iw == 0)
-            ok = item(am0 + s * kStageDesc, bm0 + s * kStageDesc, false);
-          if (!ok) break;
-          if (elected) umma_commit(empty(s));
-          __syncwarp();
+        } else {
+          for (int half = 0; half < 2 && ok; ++half, ++ks) {
+            const int s = static_cast<int>(ks % STAGES);
+            ok = __all_sync(0xffffffffu, mbar_wait(full(s), (ks / STAGES) & 1, wctl));
+            if (ok && kRaw) ok = __all_sync(0xffffffffu, mbar_wait(conv(s), (ks / STAGES) & 1, wctl));
+            if (!ok) break;
+            tc_fence_after();
+            const uint64_t as = a0 + s * kStageDesc, bs = b0 + s * kStageDesc;
+  #pragma unroll
+            for (int q = 0; q < 2 && ok; ++q) {
+              const int lc = 2 * iw + q;  // chunk in the stage: K = 32*lc .. 32*lc+31
+              const uint64_t off = (lc >> 1) * (16384 >> 4) + (lc & 1) * (64 >> 4);
+              ok = item(as + off, bs + off, true);
+            }
+            if (ok && kQ4 && half == 1 && iw == 0)
+              ok = item(am0 + s * kStageDesc, bm0 + s * kStageDesc, false);
+            if (!ok) break;
+            if (elected) umma_commit(empty(s));
+            __syncwarp();
+          }
         }
       }
     }
@@ -990,6 +1042,7 @@ __global__ void __launch_bounds__(Shape<kRaw>::kThreads, 1)
             bulk_prefetch_l2(rawplane + raw_block(ot, sb, half, nsb, kQ4), raw_block_bytes(kQ4));
           else
             bulk_prefetch_l2(bplane + b_block(ot, sb, half, nsb, kQ4), half ? b_odd_bytes(kQ4) : b_even_bytes());
+          if (kB0) bulk_prefetch_l2(b0plane + b_block(ot, sb, half, nsb, false), kOperandBytes);
         }
       }
     }
@@ -1228,7 +1281,9 @@ struct SplitRegs {
                 "the register split must add up to what the launch holds");
 };
 
-template <bool kQ4, bool kWide>
+// kB0 (q6_K with |sc| > 64): after the kN / 128 B1 K-blocks of a stage come
+// as many B0 K-blocks.
+template <bool kQ4, bool kWide, bool kB0 = false>
 struct SplitSmem {
   static constexpr bool kShared = kQ4 && kWide;  // min terms share the accumulator regions
   static constexpr int kN = kWide ? 256 : 128;
@@ -1236,7 +1291,7 @@ struct SplitSmem {
   static constexpr int kMinA = kQ4 && !kShared ? kMinBytes : 0;
   static constexpr int kMinB = kQ4 && !kShared ? kMinBytes * (kN / 128) : 0;
   static constexpr int kA = kSplitQuarter + kMinA;
-  static constexpr int kB = ((kBK * (kN / 128) + kMinB + 1023) / 1024) * 1024;
+  static constexpr int kB = ((kBK * (kN / 128) * (kB0 ? 2 : 1) + kMinB + 1023) / 1024) * 1024;
   static constexpr int kStage = kA + kB;
   static constexpr int kStages = kStage * 4 <= 200 * 1024 ? 4 : kStage * 3 <= 200 * 1024 ? 3 : 2;
   // kShared: min operand ring, entry = A min image then kN / 128 B min images
@@ -1284,12 +1339,14 @@ __device__ __forceinline__ void fold_region(uint32_t ta, const float4 *s4, float
   }
 }
 
-template <bool kQ4, bool kWide>
+template <bool kQ4, bool kWide, bool kB0>
 __global__ void __launch_bounds__(SplitShape::kThreads, 1)
     mmq_gemm_split_kernel(const uint8_t *__restrict__ aplane, const uint8_t *__restrict__ bplane,
                           const uint8_t *__restrict__ bscale, const float *__restrict__ invp, int64_t nt,
-                          int64_t od, int64_t nb32, int n_tt, int n_ot, float *__restrict__ Y, WaitCtl wctl) {
-  using L = SplitSmem<kQ4, kWide>;
+                          int64_t od, int64_t nb32, int n_tt, int n_ot, float *__restrict__ Y, WaitCtl wctl,
+                          const uint8_t *__restrict__ b0plane) {
+  static_assert(!kB0 || !kQ4, "the B0 plane is q6_K's");
+  using L = SplitSmem<kQ4, kWide, kB0>;
   using S = SplitShape;
   constexpr int STAGES = L::kStages, NR = L::kRegions, NW = L::kN / 128;
   extern __shared__ uint8_t smem_raw[];
@@ -1400,7 +1457,8 @@ __global__ void __launch_bounds__(SplitShape::kThreads, 1)
           const bool mins = kQ4 && !SH && qq == 3;
           const uint8_t *ablk = aplane + as_block(tt, sb, half, nsb, kQ4);
           if (lane == 0) {
-            mbar_arrive_expect_tx(full(s), kSplitQuarter + NW * L::kBK + (mins ? L::kMinA + L::kMinB : 0));
+            mbar_arrive_expect_tx(full(s), kSplitQuarter + NW * L::kBK * (kB0 ? 2 : 1) +
+                                               (mins ? L::kMinA + L::kMinB : 0));
             bulk_load(a_smem(s), ablk + kb * kSplitQuarter, kSplitQuarter, full(s));
             if (mins) bulk_load(a_smem(s) + kSplitQuarter, ablk + kSplitMin, kMinBytes, full(s));
           } else if (lane == 1) {
@@ -1408,6 +1466,12 @@ __global__ void __launch_bounds__(SplitShape::kThreads, 1)
               const uint8_t *bblk = bplane + b_block(wtile(og, w), sb, half, nsb, kQ4);
               bulk_load(b_smem(s) + w * L::kBK, bblk + kb * L::kBK, L::kBK, full(s));
               if (mins) bulk_load(b_smem(s) + NW * L::kBK + w * kMinBytes, bblk + kBMin, kMinBytes, full(s));
+            }
+          } else if constexpr (kB0) {
+            if (lane == 4) {
+              for (int w = 0; w < NW; ++w)
+                bulk_load(b_smem(s) + (NW + w) * L::kBK,
+                          b0plane + b_block(wtile(og, w), sb, half, nsb, false) + kb * L::kBK, L::kBK, full(s));
             }
           }
           __syncwarp();
@@ -1496,6 +1560,13 @@ __global__ void __launch_bounds__(SplitShape::kThreads, 1)
               umma_f16(dacc, ah0 + off + 2, b0 + off + 2, idesc, 1u);
               umma_f16(dacc, al0 + off, b0 + off, idesc, 1u);
               umma_f16(dacc, al0 + off + 2, b0 + off + 2, idesc, 1u);
+              if (kB0) {  // the same A against the B0 images
+                constexpr uint64_t kB0Desc = (NW * L::kBK) >> 4;
+                umma_f16(dacc, ah0 + off, b0 + kB0Desc + off, idesc, 1u);
+                umma_f16(dacc, ah0 + off + 2, b0 + kB0Desc + off + 2, idesc, 1u);
+                umma_f16(dacc, al0 + off, b0 + kB0Desc + off, idesc, 1u);
+                umma_f16(dacc, al0 + off + 2, b0 + kB0Desc + off + 2, idesc, 1u);
+              }
             }
             if (kQ4 && !SH && qq == 3) umma_f16(dmin, am0 + so, bm0 + so, idesc, 0u);
             umma_commit(empty(s));
@@ -1684,13 +1755,13 @@ namespace {
 // One GEMM kernel variant: its function, launch shape and a one-time check,
 // per device, of the shared-memory opt-in and of the register count the
 // register split was planned for (a mismatch would stall setmaxnreg).
-template <bool kQ4, bool kSK, bool kRaw>
+template <bool kQ4, bool kSK, bool kRaw, bool kB0>
 cudaError_t launch_variant(int dev, int grid, cudaStream_t s, const uint8_t *aplane, const uint8_t *bplane,
-                           const uint8_t *rawplane, const uint8_t *bscale, const float *dap,
+                           const uint8_t *rawplane, const uint8_t *b0plane, const uint8_t *bscale, const float *dap,
                            const float *invp, int64_t nt, int64_t od, int64_t nb32, int n_tt, int n_ot,
                            float *Y, WaitCtl w, float4 *ws, uint64_t *flags, bool pdl) {
-  auto kern = mmq_gemm_kernel<kQ4, kSK, kRaw>;
-  constexpr int smem = Smem<kQ4, kRaw>::kBytes;
+  auto kern = mmq_gemm_kernel<kQ4, kSK, kRaw, kB0>;
+  constexpr int smem = Smem<kQ4, kRaw, kB0>::kBytes;
   static std::atomic<int> ready[64];  // 0 unknown, 1 ready, 2 unusable
   int st = ready[dev].load();
   if (st == 0) {
@@ -1712,8 +1783,8 @@ cudaError_t launch_variant(int dev, int grid, cudaStream_t s, const uint8_t *apl
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kern, aplane, bplane, rawplane, bscale, dap, invp, nt, od, nb32, n_tt,
-                            n_ot, Y, w, ws, flags);
+  return cudaLaunchKernelEx(&cfg, kern, aplane, bplane, rawplane, b0plane, bscale, dap, invp, nt, od, nb32,
+                            n_tt, n_ot, Y, w, ws, flags);
 }
 
 }  // namespace
@@ -1722,7 +1793,7 @@ cudaError_t launch_gemm(const mmq_weights_s *h, const uint8_t *Q, const float *X
                         float *Y, void *scratch, bool streamk_allowed, bool raw, DevStatus *st,
                         unsigned epoch, uint64_t limit_ns, cudaStream_t s, cudaEvent_t ev0,
                         cudaEvent_t ev1, unsigned ev_flags) {
-  if (raw && !h->rawplane) return cudaErrorInvalidValue;
+  if (raw && (!h->rawplane || h->b0plane)) return cudaErrorInvalidValue;
   const GemmPlan p = plan_gemm(h, nt, streamk_allowed);
   const bool q4 = p.q4;
   const int64_t n_tt = p.n_tt, nt_pad = p.nt_pad, nsb = p.nsb, nb32 = p.nb32;
@@ -1771,15 +1842,17 @@ cudaError_t launch_gemm(const mmq_weights_s *h, const uint8_t *Q, const float *X
   const uint8_t *bs = bp + b_scale_region(p.n_ot, nsb, q4);
   const uint8_t *rp = h->rawplane;
   const int nti = static_cast<int>(n_tt);
-#define MMQ_LAUNCH(Q4, SK, RAW)                                                                 \
-  launch_variant<Q4, SK, RAW>(dev, p.grid, s, aplane, bp, rp, bs, dap, invp, nt, h->od, nb32, nti, \
-                              p.n_ot, Y, w, ws, flags, ev0 == nullptr)
+#define MMQ_LAUNCH(Q4, SK, RAW, B0)                                                                   \
+  launch_variant<Q4, SK, RAW, B0>(dev, p.grid, s, aplane, bp, rp, h->b0plane, bs, dap, invp, nt, h->od, nb32, \
+                                  nti, p.n_ot, Y, w, ws, flags, ev0 == nullptr)
   if (q4)
-    e = p.streamk ? (raw ? MMQ_LAUNCH(true, true, true) : MMQ_LAUNCH(true, true, false))
-                  : (raw ? MMQ_LAUNCH(true, false, true) : MMQ_LAUNCH(true, false, false));
+    e = p.streamk ? (raw ? MMQ_LAUNCH(true, true, true, false) : MMQ_LAUNCH(true, true, false, false))
+                  : (raw ? MMQ_LAUNCH(true, false, true, false) : MMQ_LAUNCH(true, false, false, false));
+  else if (h->b0plane)  // (the raw arm has no B0 image: the API refuses it for such handles)
+    e = p.streamk ? MMQ_LAUNCH(false, true, false, true) : MMQ_LAUNCH(false, false, false, true);
   else
-    e = p.streamk ? (raw ? MMQ_LAUNCH(false, true, true) : MMQ_LAUNCH(false, true, false))
-                  : (raw ? MMQ_LAUNCH(false, false, true) : MMQ_LAUNCH(false, false, false));
+    e = p.streamk ? (raw ? MMQ_LAUNCH(false, true, true, false) : MMQ_LAUNCH(false, true, false, false))
+                  : (raw ? MMQ_LAUNCH(false, false, true, false) : MMQ_LAUNCH(false, false, false, false));
 #undef MMQ_LAUNCH
   if (e != cudaSuccess) return e;
   e = cudaGetLastError();
@@ -1794,7 +1867,8 @@ namespace {
 // or 256 weight rows per CTA, whichever gives the busiest CTA the least time
 // by the per-super-block costs measured on the GB300 (clk, one CTA per SM): a
 // 128 x 128 super-block is bound by operand ingest at ~3150, a 128 x 256 one
-// by the tensor pipe at ~4100 (q6_K) and ~4450 (q4_K, with its min term).
+// by the tensor pipe at ~4100 (q6_K) and ~4450 (q4_K, with its min term);
+// with a B0 plane (twice the UMMAs) ~4200 and ~8200.
 // (Stream-K over these tiles measured slower on the 3584 x 3584 x 512 shapes:
 // the groups' first super-blocks pull most of the working set from HBM at
 // once, the 128-row tiles are bound by the L2's total bandwidth rather than
@@ -1817,7 +1891,7 @@ SplitPlan plan_split(const mmq_weights_s *h, int64_t nt) {
   const int64_t sms = num_sms(h->device);
   int64_t best = -1;
   for (int wide = 0; wide < 2; ++wide) {
-    const int64_t cost = wide ? (p.q4 ? 4450 : 4100) : 3150;
+    const int64_t cost = h->b0plane ? (wide ? 8200 : 4200) : wide ? (p.q4 ? 4450 : 4100) : 3150;
     const int64_t tiles = p.n_tt * (wide ? (p.n_ot + 1) / 2 : p.n_ot);
     const int64_t est = (tiles + sms - 1) / sms * cost;
     if (best < 0 || est < best) {
@@ -1882,7 +1956,7 @@ cudaError_t launch_gemm_split(const mmq_weights_s *h, const uint8_t *Q, const fl
   const uint8_t *bs = bp + b_scale_region(n_ot, nsb, q4);
   const int grid = p.grid;
   auto go = [&](auto kern, int smem, int variant) -> cudaError_t {
-    static std::atomic<int> ready[4][64];  // per kernel variant: 0 unknown, 1 ready, 2 unusable
+    static std::atomic<int> ready[6][64];  // per kernel variant: 0 unknown, 1 ready, 2 unusable
     std::atomic<int> &rd = ready[variant][dev];
     int stt = rd.load();
     if (stt == 0) {
@@ -1905,14 +1979,18 @@ cudaError_t launch_gemm_split(const mmq_weights_s *h, const uint8_t *Q, const fl
     cfg.attrs = attr;
     cfg.numAttrs = ev0 ? 0 : 1;
     return cudaLaunchKernelEx(&cfg, kern, static_cast<const uint8_t *>(aplane), bp, bs,
-                              static_cast<const float *>(invp), nt, h->od, nb32, static_cast<int>(n_tt), n_ot, Y, w);
+                              static_cast<const float *>(invp), nt, h->od, nb32, static_cast<int>(n_tt), n_ot, Y, w,
+                              static_cast<const uint8_t *>(h->b0plane));
   };
   if (q4)
-    e = wide ? go(mmq_gemm_split_kernel<true, true>, SplitSmem<true, true>::kBytes, 3)
-             : go(mmq_gemm_split_kernel<true, false>, SplitSmem<true, false>::kBytes, 0);
+    e = wide ? go(mmq_gemm_split_kernel<true, true, false>, SplitSmem<true, true>::kBytes, 3)
+             : go(mmq_gemm_split_kernel<true, false, false>, SplitSmem<true, false>::kBytes, 0);
+  else if (h->b0plane)
+    e = wide ? go(mmq_gemm_split_kernel<false, true, true>, SplitSmem<false, true, true>::kBytes, 5)
+             : go(mmq_gemm_split_kernel<false, false, true>, SplitSmem<false, false, true>::kBytes, 4);
   else
-    e = wide ? go(mmq_gemm_split_kernel<false, true>, SplitSmem<false, true>::kBytes, 1)
-             : go(mmq_gemm_split_kernel<false, false>, SplitSmem<false, false>::kBytes, 2);
+    e = wide ? go(mmq_gemm_split_kernel<false, true, false>, SplitSmem<false, true>::kBytes, 1)
+             : go(mmq_gemm_split_kernel<false, false, false>, SplitSmem<false, false>::kBytes, 2);
   if (e != cudaSuccess) return e;
   if ((e = cudaGetLastError()) == cudaSuccess && ev1) e = cudaEventRecordWithFlags(ev1, s, ev_flags);
   return e;

@@ -24,7 +24,11 @@ struct mmq_weights_s {
   void *bplane = nullptr;
   int8_t *wexp = nullptr;
   uint8_t *rawplane = nullptr;  // MMQ_REG_RAW: packed bytes regrouped for the raw arm
-  size_t bplane_bytes = 0, wexp_bytes = 0, rawplane_bytes = 0;
+  // q6_K with a sub-block scale |sc| > 64: sc*(q - 32) needs up to 13 bits, so
+  // the operand plane holds B1 = 2*sc*((q-32) >> 1) and this plane, same
+  // layout, B0 = sc*((q-32) & 1); both exact in fp16, B1 + B0 = sc*(q - 32)
+  uint8_t *b0plane = nullptr;
+  size_t bplane_bytes = 0, wexp_bytes = 0, rawplane_bytes = 0, b0plane_bytes = 0;
 };
 
 namespace mmq {
@@ -51,6 +55,9 @@ cudaError_t launch_dequant(int type, const uint8_t *W, int64_t od, int64_t id, v
                            int out_type, cudaStream_t s);
 cudaError_t launch_register(const mmq_weights_s *h, const uint8_t *W, int *bad_scale,
                             cudaStream_t s);
+// second pass for q6_K handles with |sc| > 64: B1 into the operand plane, B0
+// into h->b0plane (allocated by the caller, b0plane_bytes)
+cudaError_t launch_register_b0(const mmq_weights_s *h, const uint8_t *W, cudaStream_t s);
 
 // GEMM: scratch bytes for nt tokens, and the launch of the activation
 // prepass + GEMM kernel.  With streamk_allowed the GEMM may split tiles

@@ -5,8 +5,12 @@
 // a dense layout contract ("47 · r44 — W_exp stride mismatch root cause",
 // §2.2: element (j, sb, e) at j*id + sb*256 + e).  Registration here writes
 // the GEMM's pre-tiled weight plane (tiling.h), per weight element (o, k):
-//   operand  fp16  q6_K: sc[k/16] * (q - 32)   (|.| <= 64*32, exact)
+//   operand  fp16  q6_K: sc[k/16] * (q - 32)   (exact while |sc| <= 64)
 //                  q4_K: sc[k/32] * q          (<= 63*15, exact)
+// A q6_K tensor with some |sc| > 64 (the int8 range allows 128) gets a second
+// pass: with c = q - 32, B1 = 2*sc*(c >> 1) (even, |.| <= 4096) in the
+// operand plane and B0 = sc*(c & 1) (|.| <= 128) in a second plane of the
+// same layout; both are exact fp16 integers and B1 + B0 = sc*c.
 // and per (row, super-block) the fp32 scale d, plus for q4_K dmin (both in
 // the plane's scale region) and the integer mins m of the eight sub-blocks
 // (the min-term image).
@@ -73,12 +77,13 @@ __global__ void __launch_bounds__(256) expand_wexp_kernel(const uint8_t *__restr
   wexp[o * id + sb * MMQ_QK + e] = static_cast<int8_t>(kQ4 ? q4k_code(blk, e) : q6k_centered(blk, e));
 }
 
-template <bool kQ4, bool kFromWexp>
+template <bool kQ4, bool kFromWexp, bool kB0 = false>
 __global__ void __launch_bounds__(256) register_kernel(const uint8_t *__restrict__ W,
                                                        const int8_t *__restrict__ wexp, int64_t id,
                                                        uint8_t *__restrict__ bplane,
                                                        uint64_t scale_region,
-                                                       int *__restrict__ bad_scale) {
+                                                       int *__restrict__ bad_scale,
+                                                       uint8_t *__restrict__ b0plane = nullptr) {
   constexpr int kBytes = kQ4 ? MMQ_Q4K_BLOCK_BYTES : MMQ_Q6K_BLOCK_BYTES;
   __shared__ uint8_t blk[kBytes + 2];
   const int64_t nsb = id / MMQ_QK;
@@ -113,8 +118,14 @@ __global__ void __launch_bounds__(256) register_kernel(const uint8_t *__restrict
     if constexpr (kFromWexp) c = wexp[o * id + sb * MMQ_QK + e];
     else c = q6k_centered(blk, e);
     const int sc = static_cast<int8_t>(blk[MMQ_Q6K_SC_OFF + (e >> 4)]);
-    if ((e & 15) == 0 && (sc > 64 || sc < -64)) atomicOr(bad_scale, 1);
-    val = sc * c;
+    if (!kB0 && (e & 15) == 0 && (sc > 64 || sc < -64)) atomicOr(bad_scale, 1);
+    if constexpr (kB0) {
+      val = 2 * sc * (c >> 1);  // arithmetic shift: floor(c / 2)
+      *reinterpret_cast<__half *>(b0plane + b_block(ot, sb, half, nsb, false) + operand_off(r, k)) =
+          __int2half_rn(sc * (c & 1));
+    } else {
+      val = sc * c;
+    }
     d = f16_at(blk + MMQ_Q6K_D_OFF);
   }
   *reinterpret_cast<__half *>(dst + operand_off(r, k)) = __int2half_rn(val);
@@ -266,6 +277,20 @@ cudaError_t launch_register(const mmq_weights_s *h, const uint8_t *W, int *bad_s
   } else {
     register_kernel<false, false><<<grid, 256, 0, s>>>(W, nullptr, h->id, bp, sr, bad_scale);
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_register_b0(const mmq_weights_s *h, const uint8_t *W, cudaStream_t s) {
+  if (h->type != MMQ_Q6_K || !h->b0plane) return cudaErrorInvalidValue;
+  cudaError_t e = cudaMemsetAsync(h->b0plane, 0, h->b0plane_bytes, s);
+  if (e != cudaSuccess) return e;
+  const dim3 grid(static_cast<unsigned>(h->od), static_cast<unsigned>(h->nsb));
+  uint8_t *bp = static_cast<uint8_t *>(h->bplane);
+  const uint64_t sr = b_scale_region(h->od_pad / kTileN, h->nsb, false);
+  if (h->wexp)
+    register_kernel<false, true, true><<<grid, 256, 0, s>>>(W, h->wexp, h->id, bp, sr, nullptr, h->b0plane);
+  else
+    register_kernel<false, false, true><<<grid, 256, 0, s>>>(W, nullptr, h->id, bp, sr, nullptr, h->b0plane);
   return cudaGetLastError();
 }
 

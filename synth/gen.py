@@ -14,8 +14,12 @@ Workloads (the task's five configurations; the log pages measured them on a
   2 q6_K q-proj        od=3584  id=3584   nt=512
   3 q4_K FFN up/gate   od=18944 id=3584   nt=2630  X ~ N(0, 1.5)
   4 q6_K FFN down      od=3584  id=18944  nt=2630  X ~ N(0,1), 1% outliers x20
-q6_K blocks: ql/qh bytes uniform, int8 sub-block scales uniform in [-32, 31],
-fp16 d = fp16_rn(U[1e-4, 1e-3]).  q4_K blocks: qs bytes uniform, the 12
+q6_K blocks: ql/qh bytes uniform; int8 sub-block scales spread the way the
+format is usually encoded, the sub-block of largest magnitude at -128 and the
+rest in proportion: per super-block 16 magnitudes U[0.3, 1] with random signs
+s_i, sc_i = clip(rint(-128 s_i / s_k), -128, 127) with k the largest |s_i|
+(so most |sc| exceed 64; scales="small" draws them uniform in [-32, 31]
+instead); fp16 d = fp16_rn(U[1e-4, 1e-3]).  q4_K blocks: qs bytes uniform, the 12
 packed scale/min bytes uniform (every 6-bit field is then uniform in [0, 63]),
 fp16 d and dmin = fp16_rn(U[1e-4, 1e-3]).
 """
@@ -36,6 +40,7 @@ TAG_W_BYTES = 3
 TAG_W_SCALE = 4
 TAG_W_D = 5
 TAG_W_DMIN = 6
+TAG_W_SCALE_SIGN = 7
 
 
 def _mix(z: np.ndarray) -> np.ndarray:
@@ -83,11 +88,20 @@ def f16_uniform(seed: int, tag: int, n: int, lo: float, hi: float) -> np.ndarray
     return u.astype(np.float16).view(np.uint16)
 
 
-def q6k_blocks(seed: int, nblk: int) -> np.ndarray:
+def q6k_blocks(seed: int, nblk: int, scales: str = "int8") -> np.ndarray:
     """nblk packed 210-byte q6_K blocks: ql[128] qh[64] sc[16] d(fp16)."""
     out = np.empty((nblk, 210), dtype=np.uint8)
     out[:, 0:192] = uniform_bytes(seed, TAG_W_BYTES, nblk * 192).reshape(nblk, 192)
-    sc = (uniform_bytes(seed, TAG_W_SCALE, nblk * 16).astype(np.int16) & 63) - 32
+    if scales == "small":
+        sc = (uniform_bytes(seed, TAG_W_SCALE, nblk * 16).astype(np.int16) & 63) - 32
+    elif scales == "int8":
+        mag = 0.3 + 0.7 * uniform01(seed, TAG_W_SCALE, nblk * 16).reshape(nblk, 16)
+        sign = np.where(uniform_bytes(seed, TAG_W_SCALE_SIGN, nblk * 16).reshape(nblk, 16) & 1, -1.0, 1.0)
+        s = mag * sign
+        sk = s[np.arange(nblk), np.argmax(mag, axis=1)][:, None]
+        sc = np.clip(np.rint(-128.0 * s / sk), -128, 127).astype(np.int16)
+    else:
+        raise ValueError(f"q6_K scales: {scales!r}")
     out[:, 192:208] = sc.astype(np.int8).view(np.uint8).reshape(nblk, 16)
     d = f16_uniform(seed, TAG_W_D, nblk, 1e-4, 1e-3)
     out[:, 208:210] = d.astype("<u2").view(np.uint8).reshape(nblk, 2)
@@ -141,10 +155,10 @@ def config_by_name(name: str) -> Config:
     raise KeyError(name)
 
 
-def weights(qtype: str, od: int, id_: int, seed: int) -> np.ndarray:
+def weights(qtype: str, od: int, id_: int, seed: int, q6_scales: str = "int8") -> np.ndarray:
     """Packed weight rows: od x (id/256) blocks, row-major, as a flat uint8 array."""
     nblk = od * (id_ // 256)
-    blk = q6k_blocks(seed, nblk) if qtype == "q6_K" else q4k_blocks(seed, nblk)
+    blk = q6k_blocks(seed, nblk, q6_scales) if qtype == "q6_K" else q4k_blocks(seed, nblk)
     return blk.reshape(-1)
 
 

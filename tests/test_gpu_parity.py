@@ -172,12 +172,21 @@ def test_error_codes(mmq):
     with pytest.raises(mmq.MMQError) as e:
         mmq.mmq_register_weights("q4_K", W, 8, 256, 0x80)  # no such flag
     assert e.value.code == -1
-    # q6_K sub-block scale beyond +-64: sc*(q-32) would not be exact in fp16
-    Wb = gen.weights("q6_K", 8, 256, seed=2).reshape(8, 210)
+    # a q6_K sub-block scale beyond +-64 (one, in otherwise small scales) takes
+    # the two-plane operand; the raw arm has no B0 image and refuses it
+    Wb = gen.weights("q6_K", 8, 256, seed=2, q6_scales="small").reshape(8, 210)
     Wb[3, 192 + 5] = np.uint8(np.int8(-100).view(np.uint8))
+    wb = mmq.mmq_register_weights("q6_K", torch.from_numpy(Wb.reshape(-1)).to(dev), 8, 256, mmq.MMQ_REG_RAW)
+    Xb = gen.activations(4, 256, seed=3)
+    Qb4 = mmq.mmq_quantize_act(torch.from_numpy(Xb).to(dev))
     with pytest.raises(mmq.MMQError) as e:
-        mmq.mmq_register_weights("q6_K", torch.from_numpy(Wb.reshape(-1)).to(dev), 8, 256)
+        mmq.mmq_gemm(wb, Qb4, 4, flags=mmq.MMQ_ARM_RAW)
     assert e.value.code == -7
+    for arm in (mmq.MMQ_ARM_F16, mmq.MMQ_ARM_SPLIT):
+        Yb = mmq.mmq_gemm(wb, Qb4, 4, flags=arm).cpu().numpy()
+        err, bound = _within_tol(Yb, oracle.gemm(oracle.Q6_K, Wb.reshape(-1), 8, 256, oracle.quantize_q8_0(Xb), 4))
+        assert err <= bound, (arm, err, bound)
+    wb.release()
     # misaligned activations
     X = torch.zeros(4 * 256 + 4, dtype=torch.float32, device=dev)
     Qb = torch.empty(4 * 8 * 40, dtype=torch.uint8, device=dev)
@@ -214,10 +223,14 @@ def _fp16_bits(v):
 def test_extreme_weight_blocks(mmq):
     """The exactness boundary of the fp16 operands and extreme block scales:
     q6_K sub-block scales of exactly +-64 with codes 0 and 63 give |sc*(q-32)|
-    up to 2048; q4_K scales and mins of 63 with codes 15; d and dmin at the
-    fp16 maximum, at a subnormal and at zero."""
+    up to 2048 (one operand plane); scales -128 and 127 up to 4096 (the B1 + B0
+    planes), against rows of +-1 activations (qs = +-127), so a 32-K partial
+    reaches 32 * 127 * 4096; q4_K scales and mins of 63 with codes 15; d and
+    dmin at the fp16 maximum, at a subnormal and at zero."""
     od, id_, nt = 160, 768, 130
     X = gen.activations(nt, id_, seed=61, outlier_p=0.02, outlier_scale=30.0)
+    X[0:8] = 1.0
+    X[8:16] = np.where(np.arange(id_) % 64 < 32, 1.0, -1.0).astype(np.float32)
     Q_ref = oracle.quantize_q8_0(X)
     rng = np.random.default_rng(62)
     # q6_K: 210-byte blocks, ql @0, qh @128, sc @192 (int8), d @208
@@ -233,6 +246,12 @@ def test_extreme_weight_blocks(mmq):
     W6[5::20, 208:210] = _fp16_bits(6e-8)
     W6[10::20, 208:210] = _fp16_bits(0.0)
     W6 = W6.reshape(-1)
+    # q6_K at the ends of the int8 scale range: the two-plane operand
+    W8 = gen.weights("q6_K", od, id_, seed=65).reshape(-1, 210).copy()
+    W8[:, 192:208] = np.where(rng.random((n, 16)) < 0.5, 127, np.uint8(np.int8(-128).view(np.uint8)))
+    W8[0::3, 0:192] = 0xFF       # q = 63: (q - 32) = 31, 127 * 31 = 3937 (odd)
+    W8[1::3, 0:192] = 0x00       # q = 0: -32, -128 * -32 = 4096
+    W8 = W8.reshape(-1)
     # q4_K: 144-byte blocks, d @0, dmin @2, packed scales/mins @4, qs @16
     W4 = gen.weights("q4_K", od, id_, seed=64).reshape(-1, 144).copy()
     W4[0::2, 4:16] = 0xFF        # every 6-bit scale and min = 63
@@ -244,7 +263,7 @@ def test_extreme_weight_blocks(mmq):
     big4 = (W4[:, 0:2].view(np.uint16)[:, 0] == 0x7BFF) | (W4[:, 2:4].view(np.uint16)[:, 0] == 0x7BFF)
     W4[big4, 4:16] = 0x41        # small scales and mins there
     W4 = W4.reshape(-1)
-    for name, W in (("q6_K", W6), ("q4_K", W4)):
+    for name, W in (("q6_K", W6), ("q6_K", W8), ("q4_K", W4)):
         _, Q, Y, _ = _run(mmq, name, W, od, id_, X)
         assert np.array_equal(Q, Q_ref)
         Y_ref = oracle.gemm(QT[name], W, od, id_, Q_ref, nt)
@@ -402,7 +421,8 @@ RAW_SHAPES = [
 
 @pytest.mark.parametrize("name,od,id_,nt,seed", RAW_SHAPES)
 def test_raw_arm_bit_identical_to_operand_plane(mmq, name, od, id_, nt, seed):
-    W = gen.weights(name, od, id_, seed=500 + seed)
+    # (q6_K scales within +-64: the raw arm unpacks into one operand image)
+    W = gen.weights(name, od, id_, seed=500 + seed, q6_scales="small")
     X = gen.activations(nt, id_, seed=600 + seed, outlier_p=0.01, outlier_scale=20.0)
     w = mmq.mmq_register_weights(name, torch.from_numpy(W).cuda(), od, id_, mmq.MMQ_REG_RAW)
     Q = mmq.mmq_quantize_act(torch.from_numpy(X).cuda())
@@ -497,6 +517,30 @@ def test_split_arm_parity(mmq, name, od, id_, nt, seed):
     scale = float(np.abs(Y_ref).max()) + 1e-30
     assert float((Ys - Y16).abs().max()) / scale < 1e-5
     w.release()
+
+
+@pytest.mark.parametrize("od,id_,nt", [(300, 768, 200), (1000, 4096, 300), (3584, 512, 2176)])
+def test_q6k_one_plane_and_two_plane_operands(mmq, od, id_, nt):
+    """q6_K with every |sc| <= 64 registers one operand plane, with the int8
+    range two (B1 + B0); both arms on both against the oracle."""
+    X = gen.activations(nt, id_, seed=70 + od, outlier_p=0.01, outlier_scale=20.0)
+    Q_ref = oracle.quantize_q8_0(X)
+    Q = mmq.mmq_quantize_act(torch.from_numpy(X).cuda())
+    operand_bytes = {}
+    for scales in ("small", "int8"):
+        W = gen.weights("q6_K", od, id_, seed=71 + od, q6_scales=scales)
+        w = mmq.mmq_register_weights("q6_K", torch.from_numpy(W).cuda(), od, id_)
+        operand_bytes[scales] = mmq.mmq_weights_info(w)["operand_bytes"]
+        ts, os_ = _sample_entries(nt, od, 2000, od)
+        y_ref = oracle.gemm_entries(oracle.Q6_K, W, od, id_, Q_ref, nt, ts, os_)
+        for arm in (mmq.MMQ_ARM_F16, mmq.MMQ_ARM_SPLIT):
+            Y = mmq.mmq_gemm(w, Q, nt, flags=arm).cpu().numpy()
+            assert mmq.mmq_last_device_error() == 0
+            err, bound = _within_tol(Y[ts, os_], y_ref)
+            assert err <= bound, (scales, arm, err, bound)
+        w.release()
+    # the two-plane handle holds twice the operand bytes
+    assert operand_bytes["int8"] == 2 * operand_bytes["small"]
 
 
 @pytest.mark.parametrize("cfg", gen.CONFIGS[1:5], ids=lambda c: c.name)
