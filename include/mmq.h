@@ -95,7 +95,9 @@ typedef struct mmq_weights_s *mmq_weights_t;
 #define MMQ_ARM_RAW 2      /* packed weight bytes streamed and unpacked to fp16 in shared
                               memory inside the GEMM ("47 · r44 — W_exp stride mismatch
                               root cause", §3.2: the in-kernel recombination); needs a
-                              handle registered with MMQ_REG_RAW; bit-identical to F16 */
+                              handle registered with MMQ_REG_RAW whose operand is one
+                              plane (q4_K, or q6_K with every |sc| <= 64; otherwise
+                              MMQ_ERR_UNSUPPORTED); bit-identical to F16 */
 #define MMQ_ARM_SPLIT 3    /* the activation scale folded into the A operand as an exact
                               fp16 pair (hi = rn(da'*qs), lo = rn(da'*qs - hi)), so the
                               tensor core sums a whole 256-K super-block and the scales
@@ -140,9 +142,12 @@ int mmq_quantize_act(const float *X, int64_t nt, int64_t id, void *Q, mmq_stream
  *         with sub-block scales folded in, fp32 scale planes, optional
  *         W_exp) until mmq_release_weights.
  * Synchronizes `stream` before returning (registration is a one-time cost).
- * q6_K blocks with a sub-block scale |sc| > 64 are rejected with
- * MMQ_ERR_UNSUPPORTED: the folded operand sc*(q-32) would not be exact in
- * fp16.  Errors: MMQ_ERR_ARG, MMQ_ERR_TYPE, MMQ_ERR_OOM, MMQ_ERR_UNSUPPORTED,
+ * q6_K sub-block scales take the whole int8 range.  While every |sc| <= 64
+ * the folded operand sc*(q-32) (|.| <= 2048) is one exact fp16 plane; if any
+ * |sc| > 64 (up to 4096, not always exact in fp16) the handle holds two
+ * planes, B1 = 2*sc*((q-32) >> 1) and B0 = sc*((q-32) & 1), each exact, whose
+ * sum the GEMM forms on the tensor core (twice the operand bytes; see
+ * mmq_weights_info).  Errors: MMQ_ERR_ARG, MMQ_ERR_TYPE, MMQ_ERR_OOM,
  * MMQ_ERR_NO_DEVICE, MMQ_ERR_CUDA.
  */
 int mmq_register_weights(int type, const void *W, int64_t od, int64_t id, uint32_t flags,
