@@ -98,19 +98,24 @@ def _code_sha1(path):
     return hashlib.sha1(code.encode()).hexdigest()
 
 
-def _profiled_traffic(workload):
-    """DRAM bytes per GEMM launch from the committed ncu summary of this
-    workload, if it was taken on the current kernel source; else None."""
+def _workload_name(cfg, args):
+    """The workload's name, marked when its q6_K scales are not the recipe's."""
+    return cfg.name + ("_int8scales" if cfg.qtype == "q6_K" and args.q6_scales == "int8" else "")
+
+
+def _profiled_traffic(workload, kernel):
+    """DRAM bytes per GEMM launch from the committed ncu summary of this kernel
+    on this workload (profiles/<kernel>_<workload>.md), if it was taken on the
+    current kernel source; else None."""
     src = os.path.join(ROOT, "quantized_int8_gemm_gb300", "csrc", "gemm.cu")
-    sha = _code_sha1(src)
-    for p in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
-        text = open(p).read()
-        if workload not in text:
-            continue
-        m_sha = re.search(r"gemm_cu_code_sha1:\s*([0-9a-f]{40})", text)
-        m_b = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
-        if m_sha and m_b and m_sha.group(1) == sha:
-            return int(m_b.group(1))
+    p = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    if not os.path.exists(p):
+        return None
+    text = open(p).read()
+    m_sha = re.search(r"gemm_cu_code_sha1:\s*([0-9a-f]{40})", text)
+    m_b = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
+    if m_sha and m_b and m_sha.group(1) == _code_sha1(src):
+        return int(m_b.group(1))
     return None
 
 
@@ -228,6 +233,8 @@ def run_reference(args, cfg, rank):
     from synth import gen
     oracle.build()
     W, X = gen.config_inputs(cfg)
+    if cfg.qtype == "q6_K" and args.q6_scales != "small":
+        W = gen.weights(cfg.qtype, cfg.od, cfg.id, cfg.seed, q6_scales=args.q6_scales)
     qt = oracle.Q4_K if cfg.qtype == "q4_K" else oracle.Q6_K
     row_bytes = (cfg.id // 256) * (144 if cfg.qtype == "q4_K" else 210)
     target = max(1e-3, min(2.0, 150.0 / max(1, args.steps + args.warmup)))
@@ -263,7 +270,7 @@ def run_reference(args, cfg, rank):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": cfg.name, "qtype": cfg.qtype, "od": cfg.od, "id": cfg.id,
+        "config": {"workload": _workload_name(cfg, args), "qtype": cfg.qtype, "od": cfg.od, "id": cfg.id,
                    "nt": cfg.nt, "sample_tokens": nt_s, "sample_rows": n_rows},
         "tokens_per_s": value * 1e12 / (2 * cfg.od * cfg.id),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
@@ -292,7 +299,8 @@ def run_mine(args, cfg, rank, world):
     stream = torch.cuda.Stream()
     nt, od, id_ = cfg.nt, cfg.od, cfg.id
     seed = cfg.seed + 1000 * rank
-    W_host = gen.weights(cfg.qtype, od, id_, seed)
+    W_host = gen.weights(cfg.qtype, od, id_, seed, q6_scales=args.q6_scales)
+    wname = _workload_name(cfg, args)
     W_dev = torch.from_numpy(W_host).to(dev)
 
     # ---- registration (one-time cost, timed once)
@@ -431,7 +439,7 @@ def run_mine(args, cfg, rank, world):
     peak = peaks["bf16_tflops_sustained" if long_region else "bf16_tflops"]
     achieved = ops / (gemm_avg_ms * 1e-3) / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": _profiled_traffic(cfg.name),
+                "frac": achieved / peak, "traffic": _profiled_traffic(wname, kernel_name),
                 "peak_source": f"{peak_src} {'sustained' if long_region else 'burst'} bf16 "
                                f"(fp16 UMMA runs at the bf16 rate)",
                 "kernel": kernel_name, "arm": arm_name, "gemm_ms_avg": gemm_avg_ms,
@@ -542,9 +550,9 @@ def run_mine(args, cfg, rank, world):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": Wu, "ms_per_step": elapsed_ms / K, "higher_is_better": True,
             "scaling": "weak",
-            "vs_baseline": (value / PAGES_TOPS[cfg.name]) if cfg.name in PAGES_TOPS else None,
+            "vs_baseline": (value / PAGES_TOPS[wname]) if wname in PAGES_TOPS else None,
             "dtype": "s8 x k-quant ints on f16 UMMA, f32 accumulate", "data": "synthetic",
-            "config": {"workload": cfg.name, "qtype": cfg.qtype, "od": od, "id": id_, "nt": nt,
+            "config": {"workload": wname, "qtype": cfg.qtype, "od": od, "id": id_, "nt": nt,
                        "step": ("mmq_gemm_f32 (fused q8_0 quantization + GEMM)" if fused
                                 else "mmq_quantize_act + mmq_gemm"),
                        "cuda_graph": (f"{len(graphs)} graphs of <= {args.graph_chunk} steps"
@@ -584,6 +592,10 @@ def main(argv=None):
     ap.add_argument("--graph-chunk", type=int, default=500)
     ap.add_argument("--step", choices=("fused", "two"), default="fused",
                     help="fused: mmq_gemm_f32; two: mmq_quantize_act then mmq_gemm")
+    ap.add_argument("--q6-scales", choices=("small", "int8"), default="small",
+                    help="q6_K sub-block scales: small = the workloads' recipe, uniform in [-32, 31]; "
+                         "int8 = the format's usual encoding over the int8 range (two-plane operand); "
+                         "the workload is then named <workload>_int8scales")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -14,12 +14,13 @@ Workloads (the task's five configurations; the log pages measured them on a
   2 q6_K q-proj        od=3584  id=3584   nt=512
   3 q4_K FFN up/gate   od=18944 id=3584   nt=2630  X ~ N(0, 1.5)
   4 q6_K FFN down      od=3584  id=18944  nt=2630  X ~ N(0,1), 1% outliers x20
-q6_K blocks: ql/qh bytes uniform; int8 sub-block scales spread the way the
-format is usually encoded, the sub-block of largest magnitude at -128 and the
-rest in proportion: per super-block 16 magnitudes U[0.3, 1] with random signs
-s_i, sc_i = clip(rint(-128 s_i / s_k), -128, 127) with k the largest |s_i|
-(so most |sc| exceed 64; scales="small" draws them uniform in [-32, 31]
-instead); fp16 d = fp16_rn(U[1e-4, 1e-3]).  q4_K blocks: qs bytes uniform, the 12
+q6_K blocks: ql/qh bytes uniform, int8 sub-block scales uniform in [-32, 31]
+(the workloads' recipe), fp16 d = fp16_rn(U[1e-4, 1e-3]).  scales="int8"
+spreads the scales the way the format is usually encoded instead, the
+sub-block of largest magnitude at -128 and the rest in proportion: per
+super-block 16 magnitudes U[0.3, 1] with random signs s_i, sc_i =
+clip(rint(-128 s_i / s_k), -128, 127), k the largest |s_i| (most |sc| then
+exceed 64, which the GEMM handles with a two-plane operand).  q4_K blocks: qs bytes uniform, the 12
 packed scale/min bytes uniform (every 6-bit field is then uniform in [0, 63]),
 fp16 d and dmin = fp16_rn(U[1e-4, 1e-3]).
 """
@@ -88,7 +89,7 @@ def f16_uniform(seed: int, tag: int, n: int, lo: float, hi: float) -> np.ndarray
     return u.astype(np.float16).view(np.uint16)
 
 
-def q6k_blocks(seed: int, nblk: int, scales: str = "int8") -> np.ndarray:
+def q6k_blocks(seed: int, nblk: int, scales: str = "small") -> np.ndarray:
     """nblk packed 210-byte q6_K blocks: ql[128] qh[64] sc[16] d(fp16)."""
     out = np.empty((nblk, 210), dtype=np.uint8)
     out[:, 0:192] = uniform_bytes(seed, TAG_W_BYTES, nblk * 192).reshape(nblk, 192)
@@ -155,7 +156,7 @@ def config_by_name(name: str) -> Config:
     raise KeyError(name)
 
 
-def weights(qtype: str, od: int, id_: int, seed: int, q6_scales: str = "int8") -> np.ndarray:
+def weights(qtype: str, od: int, id_: int, seed: int, q6_scales: str = "small") -> np.ndarray:
     """Packed weight rows: od x (id/256) blocks, row-major, as a flat uint8 array."""
     nblk = od * (id_ // 256)
     blk = q6k_blocks(seed, nblk, q6_scales) if qtype == "q6_K" else q4k_blocks(seed, nblk)

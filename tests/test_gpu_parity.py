@@ -543,6 +543,26 @@ def test_q6k_one_plane_and_two_plane_operands(mmq, od, id_, nt):
     assert operand_bytes["int8"] == 2 * operand_bytes["small"]
 
 
+@pytest.mark.parametrize("cfg", [c for c in gen.CONFIGS[1:5] if c.qtype == "q6_K"], ids=lambda c: c.name)
+def test_two_plane_q6k_workloads_sampled(mmq, cfg):
+    """The q6_K workloads' shapes with scales over the int8 range (the format's
+    usual encoding): the two-plane operand on both arms, at full size, sampled
+    against the oracle; the library's choice is the fp16-plane arm."""
+    W = gen.weights("q6_K", cfg.od, cfg.id, cfg.seed, q6_scales="int8")
+    _, X = gen.config_inputs(cfg)
+    w = mmq.mmq_register_weights("q6_K", torch.from_numpy(W).cuda(), cfg.od, cfg.id)
+    Xd = torch.from_numpy(X).cuda()
+    ts, os_ = _sample_entries(cfg.nt, cfg.od, 3000 if cfg.id <= 4096 else 800, cfg.seed)
+    y_ref = oracle.gemm_entries(oracle.Q6_K, W, cfg.od, cfg.id, oracle.quantize_q8_0(X), cfg.nt, ts, os_)
+    for arm in (mmq.MMQ_ARM_AUTO, mmq.MMQ_ARM_SPLIT):
+        Y, used = mmq.mmq_gemm_f32(w, Xd, flags=arm, return_arm=True)
+        assert mmq.mmq_last_device_error() == 0
+        assert used == (mmq.MMQ_ARM_F16 if arm == mmq.MMQ_ARM_AUTO else mmq.MMQ_ARM_SPLIT)
+        err, bound = _within_tol(Y.cpu().numpy()[ts, os_], y_ref)
+        assert err <= bound, (arm, err, bound)
+    w.release()
+
+
 @pytest.mark.parametrize("cfg", gen.CONFIGS[1:5], ids=lambda c: c.name)
 def test_split_arm_workloads_sampled(mmq, cfg):
     W, X = gen.config_inputs(cfg)
