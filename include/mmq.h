@@ -88,9 +88,10 @@ typedef struct mmq_weights_s *mmq_weights_t;
 #define MMQ_REG_RAW 0x2u   /* also keep the packed bytes, regrouped, for MMQ_ARM_RAW */
 
 /* ---- GEMM arms (flags of mmq_gemm select one; arm_used reports it) ----- */
-#define MMQ_ARM_AUTO 0     /* library choice: MMQ_ARM_SPLIT for q6_K, and for q4_K when
-                              the split arm runs 256-row weight tiles (problems with more
-                              128 x 128 output tiles than SMs); else MMQ_ARM_F16 */
+#define MMQ_ARM_AUTO 0     /* library choice: MMQ_ARM_SPLIT for q6_K with a one-plane
+                              operand (every |sc| <= 64), and for q4_K when the split arm
+                              runs 256-row weight tiles (problems with more 128 x 128
+                              output tiles than SMs); else MMQ_ARM_F16 */
 #define MMQ_ARM_F16 1      /* operands from the registered fp16 operand plane (TMA copy) */
 #define MMQ_ARM_RAW 2      /* packed weight bytes streamed and unpacked to fp16 in shared
                               memory inside the GEMM ("47 · r44 — W_exp stride mismatch
