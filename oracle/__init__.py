@@ -12,6 +12,7 @@ from .oracle import (  # noqa: F401
     Q4_K,
     Q6_K,
     build,
+    chunk_partials,
     dequant_act,
     dequant_weights,
     expand_q4k_dense,

@@ -357,6 +357,47 @@ int mmq_oracle_gemm_entries_int(int type, const uint8_t *W, int64_t od, int64_t 
     return 0;
 }
 
+/* The exact integer partial of each 32-element chunk c, with the weight's
+ * sub-block scales applied but not d or the activation scale -- the sum the
+ * pages' integer MMA produces per chunk before its float rescale:
+ *   q6_K:  S[t][c][o] = sum_{j in c} sc_j * P_j,  P_j over 16 elements
+ *   q4_K:  S[t][c][o] = sc_c * P_c,               P_c over 32 elements
+ * (P as in formulation B).  S row-major nt x nb32 x od, int64. */
+int mmq_oracle_chunk_partials(int type, const uint8_t *W, int64_t od, int64_t id,
+                              const uint8_t *Q, int64_t nt, int64_t *S) {
+    int bb = block_bytes(type);
+    if (bb < 0 || id <= 0 || id % 256 != 0 || nt < 0 || od < 0) return -1;
+    int64_t nsb = id / 256, nb32 = id / 32;
+    for (int64_t t = 0; t < nt; ++t)
+        for (int64_t c = 0; c < nb32; ++c) {
+            const int8_t *qs = (const int8_t *)(Q + (t * nb32 + c) * OR_Q8_PITCH + OR_Q8_QS);
+            int64_t sb = c / 8;
+            int cc = (int)(c % 8);
+            for (int64_t o = 0; o < od; ++o) {
+                const uint8_t *blk = W + (o * nsb + sb) * bb;
+                int64_t s = 0;
+                if (type == OR_Q6_K) {
+                    for (int half = 0; half < 2; ++half) {
+                        int e0 = cc * 32 + half * 16;
+                        int64_t p = 0;
+                        for (int i2 = 0; i2 < 16; ++i2)
+                            p += (int64_t)mmq_oracle_q6k_centered(blk, e0 + i2) * qs[half * 16 + i2];
+                        s += (int64_t)q6k_scale(blk, e0) * p;
+                    }
+                } else {
+                    int sc, m;
+                    mmq_oracle_q4k_scale_min(blk, cc, &sc, &m);
+                    int64_t p = 0;
+                    for (int i2 = 0; i2 < 32; ++i2)
+                        p += (int64_t)mmq_oracle_q4k_quant(blk, cc * 32 + i2) * qs[i2];
+                    s = (int64_t)sc * p;
+                }
+                S[(t * nb32 + c) * od + o] = s;
+            }
+        }
+    return 0;
+}
+
 /* Full nt x od output (formulation A) for small problems: dequantizes the
  * activations once and one weight row at a time.  Y row-major nt x od. */
 int mmq_oracle_gemm(int type, const uint8_t *W, int64_t od, int64_t id, const uint8_t *Q,

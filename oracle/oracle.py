@@ -74,6 +74,8 @@ def lib() -> ctypes.CDLL:
                 fn.restype = ctypes.c_int
             L.mmq_oracle_gemm.argtypes = [ctypes.c_int, _ptr, _i64, _i64, _ptr, _i64, _ptr]
             L.mmq_oracle_gemm.restype = ctypes.c_int
+            L.mmq_oracle_chunk_partials.argtypes = [ctypes.c_int, _ptr, _i64, _i64, _ptr, _i64, _ptr]
+            L.mmq_oracle_chunk_partials.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -201,6 +203,20 @@ def gemm_entries(qtype, W, od, id_, Q, nt, ts, os_) -> np.ndarray:
 def gemm_entries_int(qtype, W, od, id_, Q, nt, ts, os_) -> np.ndarray:
     """Same entries via exact int64 sub-block partials, then the scales."""
     return _entries(lib().mmq_oracle_gemm_entries_int, qtype, W, od, id_, Q, nt, ts, os_)
+
+
+def chunk_partials(qtype: int, W: np.ndarray, od: int, id_: int, Q: np.ndarray, nt: int) -> np.ndarray:
+    """Exact int64 partial of every 32-element chunk, sub-block scales applied,
+    d and the activation scale not: S (nt, id/32, od)."""
+    W = np.ascontiguousarray(W, dtype=np.uint8)
+    Q = np.ascontiguousarray(Q, dtype=np.uint8)
+    assert W.size == od * (id_ // 256) * _block_bytes(qtype)
+    assert Q.size == nt * (id_ // 32) * 40
+    S = np.empty((nt, id_ // 32, od), dtype=np.int64)
+    rc = lib().mmq_oracle_chunk_partials(qtype, _p(W), od, id_, _p(Q), nt, _p(S))
+    if rc != 0:
+        raise ValueError(f"oracle chunk_partials failed rc={rc}")
+    return S
 
 
 def gemm(qtype: int, W: np.ndarray, od: int, id_: int, Q: np.ndarray, nt: int) -> np.ndarray:

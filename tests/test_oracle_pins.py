@@ -491,3 +491,50 @@ def test_q4k_dense_plane_codes():
     # e=0: byte 0 low = 0; e=33: byte 1 high = 0; e=65: byte 33 low = 1;
     # e=100: byte 36 high (36 = 0x24) = 2; e=255: byte 127 high (0x7f) = 7
     assert (P1[0], P1[33], P1[65], P1[100], P1[255]) == (0, 0, 1, 2, 7)
+
+
+# --------------------------------------------------------------------------
+# exact chunk partials (the integer sums a GPU dump is compared with)
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("name,qtype,scales", [("q6_K", oracle.Q6_K, "small"), ("q6_K", oracle.Q6_K, "int8"),
+                                                ("q4_K", oracle.Q4_K, "small")])
+def test_chunk_partials_brute_force_and_recombination(name, qtype, scales):
+    """S[t][c][o] against a numpy int64 contraction of the dense code plane
+    (pinned above) with the sub-block scales read from the block bytes, and
+    recombined with d, da (and the q4_K min term) into the fp64 GEMM."""
+    od, id_, nt = 5, 512, 7
+    W = gen.weights(name, od, id_, seed=81, q6_scales=scales)
+    X = gen.activations(nt, id_, seed=82, outlier_p=0.05, outlier_scale=30.0)
+    Q = oracle.quantize_q8_0(X)
+    S = oracle.chunk_partials(qtype, W, od, id_, Q, nt)
+    nsb, nb32 = id_ // 256, id_ // 32
+    qs = Q.reshape(nt, nb32, 40)[:, :, 4:36].view(np.int8).astype(np.int64).reshape(nt, id_)
+    bb = 210 if name == "q6_K" else 144
+    blocks = W.reshape(od, nsb, bb)
+    if name == "q6_K":
+        codes = oracle.expand_q6k_dense(W, od, id_).astype(np.int64)
+        sc = blocks[:, :, 192:208].view(np.int8).astype(np.int64)          # (od, nsb, 16)
+        scale_k = np.repeat(sc.reshape(od, nsb * 16), 16, axis=1)         # per element
+    else:
+        codes = oracle.expand_q4k_dense(W, od, id_).astype(np.int64)
+        sc = np.array([[oracle.q4k_scale_min(blocks[o, s], j)[0] for s in range(nsb) for j in range(8)]
+                       for o in range(od)], dtype=np.int64)                 # (od, nsb*8)
+        scale_k = np.repeat(sc, 32, axis=1)
+    B = codes * scale_k                                                     # (od, id)
+    want = np.einsum("tck,ock->tco", qs.reshape(nt, nb32, 32), B.reshape(od, nb32, 32))
+    assert np.array_equal(S, want)
+    # recombined with the float scales: the GEMM
+    da = oracle.f16_to_f64(Q.reshape(nt, nb32, 40)[:, :, 0:2].copy().view(np.uint16).reshape(nt, nb32))
+    if name == "q6_K":
+        d = oracle.f16_to_f64(blocks[:, :, 208:210].copy().view(np.uint16).reshape(od, nsb))
+        Y = np.einsum("tco,tc,oc->to", S.astype(np.float64), da, np.repeat(d, 8, axis=1))
+    else:
+        d = oracle.f16_to_f64(blocks[:, :, 0:2].copy().view(np.uint16).reshape(od, nsb))
+        dmin = oracle.f16_to_f64(blocks[:, :, 2:4].copy().view(np.uint16).reshape(od, nsb))
+        m = np.array([[oracle.q4k_scale_min(blocks[o, s], j)[1] for s in range(nsb) for j in range(8)]
+                      for o in range(od)], dtype=np.float64)
+        ssum = Q.reshape(nt, nb32, 40)[:, :, 36:40].copy().view(np.int32).reshape(nt, nb32).astype(np.float64)
+        Y = (np.einsum("tco,tc,oc->to", S.astype(np.float64), da, np.repeat(d, 8, axis=1))
+             - np.einsum("tc,tc,oc,oc->to", da, ssum, np.repeat(dmin, 8, axis=1), m))
+    Y_ref = oracle.gemm(qtype, W, od, id_, Q, nt)
+    assert np.allclose(Y, Y_ref, rtol=1e-12, atol=1e-12 * np.abs(Y_ref).max())
