@@ -271,6 +271,24 @@ int mmq_gemm_f32_profiled(mmq_weights_t h, const float *X, int64_t nt, float *Y,
  */
 int mmq_gemm_noalloc(mmq_weights_t h, const void *Q, int64_t nt, float *Y, mmq_stream_t stream);
 
+/*
+ * mmq_debug_chunk_partials -- test hook for the integer exactness of the
+ * fp16-plane arm: runs its GEMM (whole tiles) on Q and writes, for every
+ * token t, 32-element chunk c and output row o, the raw partial the tensor
+ * core left in TMEM before any float scale was applied:
+ *   P[t][c][o] = sum_{k in chunk c} qs[t][k] * B[o][k],
+ * B the registered operand (sc*(q-32) for q6_K, sc*q for q4_K; for a
+ * two-plane q6_K handle the sum of both planes' UMMAs).  Each is an integer
+ * below 2^24 in magnitude, stored exactly in fp32 (the per-sub-block integer
+ * dot products of "47 · r44 — W_exp stride mismatch root cause", §1.1,
+ * rescaled by sc).
+ *   Q   device pad40 blocks as for mmq_gemm, 16-byte aligned.
+ *   P   device, fp32, nt x (id/32) x od, 16-byte aligned; overwritten.
+ * Takes nt_pad*(id/32)*od_pad*4 bytes of scratch beside the GEMM's (meant
+ * for small problems).  Errors as mmq_gemm.
+ */
+int mmq_debug_chunk_partials(mmq_weights_t h, const void *Q, int64_t nt, float *P, mmq_stream_t stream);
+
 /* Synchronizes the current device, then returns and clears the device status
  * word: MMQ_OK, or MMQ_ERR_DEVICE_TIMEOUT if a bounded wait expired since
  * the last call. */

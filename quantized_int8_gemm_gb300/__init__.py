@@ -23,6 +23,7 @@ from .mmq import (  # noqa: F401
     mmq_gemm_f32,
     mmq_gemm_f32_profiled,
     mmq_gemm_noalloc,
+    mmq_debug_chunk_partials,
     mmq_gemm_profiled,
     mmq_last_device_error,
     mmq_quantize_act,

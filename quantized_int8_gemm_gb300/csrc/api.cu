@@ -311,6 +311,38 @@ int mmq_gemm_profiled(mmq_weights_t h, const void *Q, int64_t nt, float *Y, mmq_
                    static_cast<cudaEvent_t>(ev_stop));
 }
 
+int mmq_debug_chunk_partials(mmq_weights_t h, const void *Q, int64_t nt, float *P, mmq_stream_t stream) {
+  if (!h || nt < 0 || nt > kMaxTokens) return MMQ_ERR_ARG;
+  if (nt == 0) return MMQ_OK;
+  if (!Q || !P) return MMQ_ERR_ARG;
+  if (!aligned16(Q) || !aligned16(P)) return MMQ_ERR_ALIGN;
+  int dev;
+  DeviceState *d;
+  if (int rc = device_state(&dev, &d)) return rc;
+  if (dev != h->device) return MMQ_ERR_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  const int64_t nt_pad = (nt + 127) / 128 * 128;
+  const size_t gemm_bytes = up(mmq::gemm_scratch_bytes(h, nt, false, false));
+  const size_t dump_bytes = up(static_cast<size_t>(nt_pad * h->nb32 * h->od_pad) * sizeof(float));
+  const size_t y_bytes = static_cast<size_t>(nt * h->od) * sizeof(float);
+  void *scratch = nullptr;
+  cudaError_t e = cudaMallocFromPoolAsync(&scratch, gemm_bytes + dump_bytes + y_bytes, d->pool, s);
+  if (e != cudaSuccess) return cuda_rc(e);
+  uint8_t *base = static_cast<uint8_t *>(scratch);
+  float *dump = reinterpret_cast<float *>(base + gemm_bytes);
+  float *Y = reinterpret_cast<float *>(base + gemm_bytes + dump_bytes);
+  e = mmq::launch_gemm(h, static_cast<const uint8_t *>(Q), nullptr, nt, Y, scratch, false, false, d->words,
+                       next_epoch(), g_limit_ns.load(), s, nullptr, nullptr, 0, dump);
+  if (e == cudaSuccess)  // rows (t, chunk) of od partials, out of rows of od_pad
+    e = cudaMemcpy2DAsync(P, static_cast<size_t>(h->od) * sizeof(float), dump,
+                          static_cast<size_t>(h->od_pad) * sizeof(float), static_cast<size_t>(h->od) * sizeof(float),
+                          static_cast<size_t>(nt * h->nb32), cudaMemcpyDeviceToDevice, s);
+  cudaError_t ef = cudaFreeAsync(scratch, s);
+  if (e == cudaSuccess) e = ef;
+  return cuda_rc(e);
+}
+
 int mmq_gemm_noalloc(mmq_weights_t h, const void *Q, int64_t nt, float *Y, mmq_stream_t stream) {
   if (!h || nt < 0 || nt > kMaxTokens) return MMQ_ERR_ARG;
   if (nt == 0) return MMQ_OK;

@@ -749,15 +749,28 @@ __device__ __forceinline__ void store_y_row(float *__restrict__ Y, int64_t t, in
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
-template <bool kQ4, bool kSK, bool kRaw, bool kB0>
+// 32 fp32 values of a TMEM row half to dump[at .. at + 31] (16-byte stores).
+__device__ __forceinline__ void dump_half(float *__restrict__ dump, int64_t at, const uint32_t (&r)[32]) {
+  float4 *p = reinterpret_cast<float4 *>(dump + at);
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    p[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]), __uint_as_float(r[4 * i + 2]),
+                       __uint_as_float(r[4 * i + 3]));
+}
+
+// kDump (a test hook, whole tiles only): each chunk's raw TMEM partial -- the
+// exact integer sum of qs times the folded operand -- is also stored, fp32,
+// to dump[(t * nb32 + chunk) * od_pad + o].
+template <bool kQ4, bool kSK, bool kRaw, bool kB0, bool kDump = false>
 __global__ void __launch_bounds__(Shape<kRaw>::kThreads, 1)
     mmq_gemm_kernel(const uint8_t *__restrict__ aplane, const uint8_t *__restrict__ bplane,
                     const uint8_t *__restrict__ rawplane, const uint8_t *__restrict__ b0plane,
                     const uint8_t *__restrict__ bscale, const float *__restrict__ dap,
                     const float *__restrict__ invp, int64_t nt, int64_t od, int64_t nb32, int n_tt,
                     int n_ot, float *__restrict__ Y, WaitCtl wctl, float4 *__restrict__ ws,
-                    uint64_t *__restrict__ flags) {
+                    uint64_t *__restrict__ flags, float *__restrict__ dump) {
   static_assert(!kB0 || (!kQ4 && !kRaw), "the B0 plane is q6_K's, read from the registered planes");
+  static_assert(!kDump || (!kSK && !kRaw), "the partial dump runs whole tiles from the registered planes");
   using L = Smem<kQ4, kRaw, kB0>;
   using S = Shape<kRaw, kB0>;
   constexpr int STAGES = S::kStages;
@@ -1122,6 +1135,7 @@ __global__ void __launch_bounds__(Shape<kRaw>::kThreads, 1)
             ready = mbar_test_wait(rfull(nb), npb);
           }
           reg_fence(r0);
+          if constexpr (kDump) dump_half(dump, (t * nb32 + sb * 8 + c) * (n_ot * kTileN) + o0, r0);
           fold_half(acc, 0, r0, das[c], c == 0);
           tmem_wait_ld(r1);
           give(slot);
@@ -1135,6 +1149,7 @@ __global__ void __launch_bounds__(Shape<kRaw>::kThreads, 1)
             }
             tmem_ld_32x32b_x32(taddr + slot * kTileN, r0);
           }
+          if constexpr (kDump) dump_half(dump, (t * nb32 + sb * 8 + c) * (n_ot * kTileN) + o0 + 32, r1);
           fold_half(acc, 1, r1, das[c], c == 0);
           if (c < 7) tmem_wait_ld(r0);
         }
@@ -1755,12 +1770,13 @@ namespace {
 // One GEMM kernel variant: its function, launch shape and a one-time check,
 // per device, of the shared-memory opt-in and of the register count the
 // register split was planned for (a mismatch would stall setmaxnreg).
-template <bool kQ4, bool kSK, bool kRaw, bool kB0>
+template <bool kQ4, bool kSK, bool kRaw, bool kB0, bool kDump = false>
 cudaError_t launch_variant(int dev, int grid, cudaStream_t s, const uint8_t *aplane, const uint8_t *bplane,
                            const uint8_t *rawplane, const uint8_t *b0plane, const uint8_t *bscale, const float *dap,
                            const float *invp, int64_t nt, int64_t od, int64_t nb32, int n_tt, int n_ot,
-                           float *Y, WaitCtl w, float4 *ws, uint64_t *flags, bool pdl) {
-  auto kern = mmq_gemm_kernel<kQ4, kSK, kRaw, kB0>;
+                           float *Y, WaitCtl w, float4 *ws, uint64_t *flags, bool pdl,
+                           float *dump = nullptr) {
+  auto kern = mmq_gemm_kernel<kQ4, kSK, kRaw, kB0, kDump>;
   constexpr int smem = Smem<kQ4, kRaw, kB0>::kBytes;
   static std::atomic<int> ready[64];  // 0 unknown, 1 ready, 2 unusable
   int st = ready[dev].load();
@@ -1784,7 +1800,7 @@ cudaError_t launch_variant(int dev, int grid, cudaStream_t s, const uint8_t *apl
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kern, aplane, bplane, rawplane, b0plane, bscale, dap, invp, nt, od, nb32,
-                            n_tt, n_ot, Y, w, ws, flags);
+                            n_tt, n_ot, Y, w, ws, flags, dump);
 }
 
 }  // namespace
@@ -1792,8 +1808,9 @@ cudaError_t launch_variant(int dev, int grid, cudaStream_t s, const uint8_t *apl
 cudaError_t launch_gemm(const mmq_weights_s *h, const uint8_t *Q, const float *X, int64_t nt,
                         float *Y, void *scratch, bool streamk_allowed, bool raw, DevStatus *st,
                         unsigned epoch, uint64_t limit_ns, cudaStream_t s, cudaEvent_t ev0,
-                        cudaEvent_t ev1, unsigned ev_flags) {
+                        cudaEvent_t ev1, unsigned ev_flags, float *dump) {
   if (raw && (!h->rawplane || h->b0plane)) return cudaErrorInvalidValue;
+  if (dump && (raw || streamk_allowed)) return cudaErrorInvalidValue;
   const GemmPlan p = plan_gemm(h, nt, streamk_allowed);
   const bool q4 = p.q4;
   const int64_t n_tt = p.n_tt, nt_pad = p.nt_pad, nsb = p.nsb, nb32 = p.nb32;
@@ -1845,7 +1862,12 @@ cudaError_t launch_gemm(const mmq_weights_s *h, const uint8_t *Q, const float *X
 #define MMQ_LAUNCH(Q4, SK, RAW, B0)                                                                   \
   launch_variant<Q4, SK, RAW, B0>(dev, p.grid, s, aplane, bp, rp, h->b0plane, bs, dap, invp, nt, h->od, nb32, \
                                   nti, p.n_ot, Y, w, ws, flags, ev0 == nullptr)
-  if (q4)
+#define MMQ_LAUNCH_DUMP(Q4, B0)                                                                          \
+  launch_variant<Q4, false, false, B0, true>(dev, p.grid, s, aplane, bp, rp, h->b0plane, bs, dap, invp, nt, \
+                                             h->od, nb32, nti, p.n_ot, Y, w, ws, flags, ev0 == nullptr, dump)
+  if (dump)
+    e = q4 ? MMQ_LAUNCH_DUMP(true, false) : h->b0plane ? MMQ_LAUNCH_DUMP(false, true) : MMQ_LAUNCH_DUMP(false, false);
+  else if (q4)
     e = p.streamk ? (raw ? MMQ_LAUNCH(true, true, true, false) : MMQ_LAUNCH(true, true, false, false))
                   : (raw ? MMQ_LAUNCH(true, false, true, false) : MMQ_LAUNCH(true, false, false, false));
   else if (h->b0plane)  // (the raw arm has no B0 image: the API refuses it for such handles)
@@ -1854,6 +1876,7 @@ cudaError_t launch_gemm(const mmq_weights_s *h, const uint8_t *Q, const float *X
     e = p.streamk ? (raw ? MMQ_LAUNCH(false, true, true, false) : MMQ_LAUNCH(false, true, false, false))
                   : (raw ? MMQ_LAUNCH(false, false, true, false) : MMQ_LAUNCH(false, false, false, false));
 #undef MMQ_LAUNCH
+#undef MMQ_LAUNCH_DUMP
   if (e != cudaSuccess) return e;
   e = cudaGetLastError();
   if (e == cudaSuccess && ev1) e = cudaEventRecordWithFlags(ev1, s, ev_flags);

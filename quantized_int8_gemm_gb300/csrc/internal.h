@@ -66,10 +66,12 @@ cudaError_t launch_register_b0(const mmq_weights_s *h, const uint8_t *W, cudaStr
 // ev_flags).
 // raw: stream the handle's raw plane and unpack it in the kernel.
 size_t gemm_scratch_bytes(const mmq_weights_s *h, int64_t nt, bool streamk_allowed, bool raw);
+// dump (test hook; whole tiles, not the raw arm): also store every chunk's raw
+// partial, fp32, at dump[(t * nb32 + chunk) * od_pad + o] (nt_pad x nb32 x od_pad)
 cudaError_t launch_gemm(const mmq_weights_s *h, const uint8_t *Q, const float *X, int64_t nt,
                         float *Y, void *scratch, bool streamk_allowed, bool raw, DevStatus *st,
                         unsigned epoch, uint64_t limit_ns, cudaStream_t s, cudaEvent_t ev0,
-                        cudaEvent_t ev1, unsigned ev_flags);
+                        cudaEvent_t ev1, unsigned ev_flags, float *dump = nullptr);
 
 // Split arm (activation scale folded into A as an exact fp16 hi + lo pair):
 // scratch bytes, and the prepass + GEMM launch (whole tiles).

@@ -47,7 +47,7 @@ BLOCK_BYTES = {MMQ_Q4_K: 144, MMQ_Q6_K: 210}
 EXPORTS = [
     "mmq_quantize_act", "mmq_register_weights", "mmq_release_weights", "mmq_weights_wexp",
     "mmq_weights_info", "mmq_gemm", "mmq_gemm_f32", "mmq_gemm_profiled", "mmq_gemm_f32_profiled",
-    "mmq_gemm_noalloc", "mmq_dequantize_weights",
+    "mmq_gemm_noalloc", "mmq_debug_chunk_partials", "mmq_dequantize_weights",
     "mmq_last_device_error", "mmq_set_wait_timeout_ns",
     "mmq_selftest_wait_timeout", "mmq_strerror",
 ]
@@ -85,6 +85,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         L.mmq_gemm_profiled.argtypes = [vp, vp, i64, vp, vp, u32, ctypes.POINTER(i32), vp, vp]
         L.mmq_gemm_f32_profiled.argtypes = [vp, vp, i64, vp, vp, u32, ctypes.POINTER(i32), vp, vp]
         L.mmq_gemm_noalloc.argtypes = [vp, vp, i64, vp, vp]
+        L.mmq_debug_chunk_partials.argtypes = [vp, vp, i64, vp, vp]
         L.mmq_dequantize_weights.argtypes = [i32, vp, i64, i64, vp, i32, vp]
         L.mmq_last_device_error.argtypes = []
         L.mmq_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
@@ -258,6 +259,15 @@ def mmq_gemm_f32_profiled(w: Weights, X: torch.Tensor, Y: torch.Tensor,
                                         ctypes.c_void_p(ev_stop.cuda_event)),
            "mmq_gemm_f32_profiled")
     return arm.value
+
+
+def mmq_debug_chunk_partials(w: Weights, Q: torch.Tensor, nt: int, stream=None) -> torch.Tensor:
+    """Test hook: the fp16-plane arm's raw per-chunk TMEM partials, fp32
+    (nt, id/32, od): exact integers, before any float scale."""
+    P = torch.empty((nt, w.id // 32, w.od), dtype=torch.float32, device=Q.device)
+    _check(load().mmq_debug_chunk_partials(w.handle, _dev_ptr(Q, "Q"), nt, _dev_ptr(P, "P"), _stream(stream)),
+           "mmq_debug_chunk_partials")
+    return P
 
 
 def mmq_gemm_noalloc(w: Weights, Q: torch.Tensor, nt: int, Y: torch.Tensor, stream=None):

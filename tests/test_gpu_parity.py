@@ -407,6 +407,47 @@ def test_fused_quantization_at_rounding_ties(mmq, name):
 
 
 # --------------------------------------------------------------------------
+# integer exactness: the raw per-chunk TMEM partials against the oracle's int64
+def _extreme_q6k(od, id_, seed):
+    """q6_K blocks at the ends of both ranges: sc in {-128, 127}, codes 0 or 63."""
+    W = gen.weights("q6_K", od, id_, seed=seed).reshape(-1, 210).copy()
+    rng = np.random.default_rng(seed)
+    n = W.shape[0]
+    W[:, 192:208] = np.where(rng.random((n, 16)) < 0.5, 127, np.uint8(np.int8(-128).view(np.uint8)))
+    W[:, 0:192] = np.where(rng.random((n, 1)) < 0.5, 0x00, 0xFF).astype(np.uint8)
+    return W.reshape(-1)
+
+
+@pytest.mark.parametrize("case", ["q6_K one plane", "q6_K two planes", "q4_K", "q6_K extremes"])
+def test_chunk_partials_are_exact_integers(mmq, case):
+    """Every 32-K chunk partial the tensor core leaves in TMEM equals the
+    oracle's int64 sum exactly (two-plane q6_K: the B1 and B0 UMMAs summed);
+    the extreme case drives partials to 32 * 127 * 4096, just under 2^24."""
+    if case == "q4_K":
+        name, od, id_, nt = "q4_K", 200, 768, 130
+        W = gen.weights(name, od, id_, seed=93)
+    else:
+        name, od, id_, nt = "q6_K", 256, 512, 40
+        if case == "q6_K extremes":
+            W = _extreme_q6k(od, id_, 94)
+        else:
+            W = gen.weights(name, od, id_, seed=95, q6_scales="int8" if "two" in case else "small")
+    X = gen.activations(nt, id_, seed=96, outlier_p=0.02, outlier_scale=30.0)
+    X[0:8] = 1.0                                                   # qs = 127 everywhere
+    X[8:16] = np.where(np.arange(id_) % 64 < 32, 1.0, -1.0).astype(np.float32)
+    w = mmq.mmq_register_weights(name, torch.from_numpy(W).cuda(), od, id_)
+    Q = mmq.mmq_quantize_act(torch.from_numpy(X).cuda())
+    P = mmq.mmq_debug_chunk_partials(w, Q, nt).cpu().numpy()
+    assert mmq.mmq_last_device_error() == 0
+    S = oracle.chunk_partials(QT[name], W, od, id_, Q.cpu().numpy(), nt)
+    assert np.abs(S).max() < 2 ** 24
+    assert np.array_equal(P.astype(np.int64), S) and np.array_equal(P, S.astype(np.float32))
+    if case == "q6_K extremes":
+        assert np.abs(S).max() > 2 ** 23   # the boundary was reached
+    w.release()
+
+
+# --------------------------------------------------------------------------
 # raw arm: packed weight bytes unpacked inside the GEMM
 RAW_SHAPES = [
     ("q6_K", 256, 512, 16, 31),
