@@ -238,14 +238,15 @@ __global__ void __launch_bounds__(128) gemm_prepass_kernel(const uint8_t *__rest
                                                            float *__restrict__ invp) {
   griddep_launch_dependents();
   const int64_t t = blockIdx.x;
+  const bool live = t < nt;  // rows nt .. nt_pad - 1 of the last tile: a zero activation row
   const int tid = threadIdx.x;
-  const uint8_t *qrow = Q + t * nb32 * MMQ_Q8_BLOCK_BYTES;
+  const uint8_t *qrow = Q + (live ? t : 0) * nb32 * MMQ_Q8_BLOCK_BYTES;
   const int64_t nsb = nb32 / 8;
   int s = 0;
   if (kQ4) {  // s_t: the token's largest |g| lands in [2^14, 2^15)
     __shared__ float wmax[4];
     float gmax = 0.f;
-    for (int64_t c = tid; c < nb32; c += 128) {
+    for (int64_t c = tid; c < nb32 && live; c += 128) {
       const uint8_t *b = qrow + c * MMQ_Q8_BLOCK_BYTES;
       const float da = __half2float(__ushort_as_half(*reinterpret_cast<const unsigned short *>(b)));
       const int ssum = *reinterpret_cast<const int *>(b + MMQ_Q8_SSUM_OFF);
@@ -267,8 +268,9 @@ __global__ void __launch_bounds__(128) gemm_prepass_kernel(const uint8_t *__rest
   if (tid == 0) invp[t] = __uint_as_float(static_cast<uint32_t>(127 - s) << 23);
   for (int64_t c = tid; c < nb32; c += 128) {
     const uint2 *src = reinterpret_cast<const uint2 *>(qrow + c * MMQ_Q8_BLOCK_BYTES);
-    const uint2 w0 = __ldg(src + 0), w1 = __ldg(src + 1), w2 = __ldg(src + 2),
-                w3 = __ldg(src + 3), w4 = __ldg(src + 4);
+    const uint2 z = make_uint2(0u, 0u);
+    const uint2 w0 = live ? __ldg(src + 0) : z, w1 = live ? __ldg(src + 1) : z, w2 = live ? __ldg(src + 2) : z,
+                w3 = live ? __ldg(src + 3) : z, w4 = live ? __ldg(src + 4) : z;
     const uint32_t qw[8] = {w0.y, w1.x, w1.y, w2.x, w2.y, w3.x, w3.y, w4.x};
     const int64_t sb = c >> 3;
     const int half = static_cast<int>((c >> 2) & 1);
@@ -382,7 +384,8 @@ __global__ void __launch_bounds__(32 * kQuantWarps) quantize_prepass_kernel(cons
   const int64_t t = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int part = lane & 7, grp = lane >> 3;
-  const float4 *xrow = reinterpret_cast<const float4 *>(X + t * nb32 * 32);
+  const bool live = t < nt;  // rows nt .. nt_pad - 1 of the last tile: a zero activation row
+  const float4 *xrow = reinterpret_cast<const float4 *>(X + (live ? t : 0) * nb32 * 32);
   float *sd16 = stash;
   int *sssum = reinterpret_cast<int *>(stash + nb32);
   float gmax = 0.f;
@@ -392,7 +395,7 @@ __global__ void __launch_bounds__(32 * kQuantWarps) quantize_prepass_kernel(cons
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int64_t c = base + u * 4 + grp;
-      v[u] = c < nb32 ? __ldg(xrow + c * 8 + part) : make_float4(0.f, 0.f, 0.f, 0.f);
+      v[u] = c < nb32 && live ? __ldg(xrow + c * 8 + part) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
@@ -442,7 +445,7 @@ __global__ void __launch_bounds__(32 * kQuantWarps) quantize_prepass_kernel(cons
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int64_t c = base + u * 4 + grp;
-        v[u] = c < nb32 ? __ldg(xrow + c * 8 + part) : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[u] = c < nb32 && live ? __ldg(xrow + c * 8 + part) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
@@ -529,7 +532,8 @@ __global__ void __launch_bounds__(32 * kQuantWarps) split_prepass_f32_kernel(con
   const int64_t t = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int part = lane & 7, grp = lane >> 3;
-  const float4 *xrow = reinterpret_cast<const float4 *>(X + t * nb32 * 32);
+  const bool live = t < nt;  // rows nt .. nt_pad - 1 of the last tile: a zero activation row
+  const float4 *xrow = reinterpret_cast<const float4 *>(X + (live ? t : 0) * nb32 * 32);
   float *sd16 = reinterpret_cast<float *>(sstash + nb32 * 16);
   int *sssum = reinterpret_cast<int *>(sd16 + nb32);
   float gmax = 0.f;
@@ -538,7 +542,7 @@ __global__ void __launch_bounds__(32 * kQuantWarps) split_prepass_f32_kernel(con
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int64_t c = base + u * 4 + grp;
-      v[u] = c < nb32 ? __ldg(xrow + c * 8 + part) : make_float4(0.f, 0.f, 0.f, 0.f);
+      v[u] = c < nb32 && live ? __ldg(xrow + c * 8 + part) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
@@ -579,7 +583,7 @@ __global__ void __launch_bounds__(32 * kQuantWarps) split_prepass_f32_kernel(con
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int64_t c = base + u * 4 + grp;
-        v[u] = c < nb32 ? __ldg(xrow + c * 8 + part) : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[u] = c < nb32 && live ? __ldg(xrow + c * 8 + part) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
@@ -602,9 +606,10 @@ __global__ void __launch_bounds__(128) split_prepass_q_kernel(const uint8_t *__r
   griddep_launch_dependents();
   const int64_t t = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const uint8_t *qrow = Q + t * nb32 * 40;
+  const bool live = t < nt;  // rows nt .. nt_pad - 1 of the last tile: a zero activation row
+  const uint8_t *qrow = Q + (live ? t : 0) * nb32 * 40;
   float gmax = 0.f;
-  for (int64_t c = tid; c < nb32; c += 128) {
+  for (int64_t c = tid; c < nb32 && live; c += 128) {
     const uint8_t *b = qrow + c * 40;
     const float d16f = __half2float(*reinterpret_cast<const __half *>(b));
     gmax = fmaxf(gmax, split_range<kQ4>(d16f, *reinterpret_cast<const int *>(b + 36)));
@@ -621,9 +626,9 @@ __global__ void __launch_bounds__(128) split_prepass_q_kernel(const uint8_t *__r
   const int part = tid & 7;
   for (int64_t c = tid >> 3; c < nb32; c += 16) {
     const uint8_t *b = qrow + c * 40;
-    const float d16f = __half2float(*reinterpret_cast<const __half *>(b));
-    const int ssum = *reinterpret_cast<const int *>(b + 36);
-    const uint32_t q4b = *reinterpret_cast<const uint32_t *>(b + 4 + 4 * part);
+    const float d16f = live ? __half2float(*reinterpret_cast<const __half *>(b)) : 0.f;
+    const int ssum = live ? *reinterpret_cast<const int *>(b + 36) : 0;
+    const uint32_t q4b = live ? *reinterpret_cast<const uint32_t *>(b + 4 + 4 * part) : 0u;
     uint32_t h[2];
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
@@ -1821,20 +1826,11 @@ cudaError_t launch_gemm(const mmq_weights_s *h, const uint8_t *Q, const float *X
   float4 *ws = p.streamk ? reinterpret_cast<float4 *>(base8 + p.ws_off) : nullptr;
   uint64_t *flags = p.streamk ? reinterpret_cast<uint64_t *>(base8 + p.flag_off) : nullptr;
 
-  // the last token tile's padding rows must read as zero
+  // activation operand plane: from pad40 blocks, or quantized from fp32 X.
+  // One CTA per row of the padded token tiles: rows nt .. nt_pad - 1 quantize
+  // a zero activation row, so the last tile's padding reads as zero.
   cudaError_t e = cudaSuccess;
-  if (nt_pad != nt) {
-    const size_t a_bytes = static_cast<size_t>(n_tt * nsb) * a_pair_bytes(q4);
-    const uint64_t tail = static_cast<uint64_t>((n_tt - 1) * nsb) * a_pair_bytes(q4);
-    e = cudaMemsetAsync(aplane + tail, 0, a_bytes - tail, s);
-    if (e == cudaSuccess)
-      e = cudaMemsetAsync(dap + nt * nb32, 0, static_cast<size_t>((nt_pad - nt) * nb32) * 4, s);
-    if (e == cudaSuccess)
-      e = cudaMemsetAsync(invp + nt, 0, static_cast<size_t>(nt_pad - nt) * 4, s);
-    if (e != cudaSuccess) return e;
-  }
-  // activation operand plane: from pad40 blocks, or quantized from fp32 X
-  const unsigned pgrid = static_cast<unsigned>(nt);
+  const unsigned pgrid = static_cast<unsigned>(nt_pad);
   if (X) {
     const size_t stash = static_cast<size_t>(nb32) * kStashBytesPerBlock;
     if (!q4)
@@ -1944,18 +1940,12 @@ cudaError_t launch_gemm_split(const mmq_weights_s *h, const uint8_t *Q, const fl
   const int n_ot = p.n_ot;
   uint8_t *base8 = static_cast<uint8_t *>(scratch);
   uint8_t *aplane = base8;
-  const size_t a_bytes = static_cast<size_t>(n_tt * nsb) * as_pair_bytes(q4);
   float *invp = reinterpret_cast<float *>(base8 + p.inv_off);
   const int dev = h->device;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   cudaError_t e = cudaSuccess;
-  if (nt_pad != nt) {  // the last token tile's padding rows must read as zero
-    const size_t tail = static_cast<size_t>((n_tt - 1) * nsb) * as_pair_bytes(q4);
-    e = cudaMemsetAsync(aplane + tail, 0, a_bytes - tail, s);
-    if (e == cudaSuccess) e = cudaMemsetAsync(invp + nt, 0, static_cast<size_t>(nt_pad - nt) * 4, s);
-    if (e != cudaSuccess) return e;
-  }
-  const unsigned pgrid = static_cast<unsigned>(nt);
+  // one CTA per row of the padded token tiles (padding rows: a zero activation row)
+  const unsigned pgrid = static_cast<unsigned>(nt_pad);
   if (X) {
     const size_t stash = static_cast<size_t>(nb32) * kSplitStashBytesPerBlock;
     const bool fits = stash <= static_cast<size_t>(kStashMaxBytes);
