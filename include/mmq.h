@@ -204,7 +204,11 @@ int mmq_weights_info(mmq_weights_t h, int *type, int64_t *od, int64_t *id,
  *   Y     device, fp32, nt x od row-major, 16-byte aligned; overwritten.
  *   flags MMQ_ARM_AUTO or one MMQ_ARM_*; arm_used (may be NULL) receives
  *         the arm that ran.
- * Allocates its scratch (nt*id*2 + nt*(id/32)*8 bytes) stream-ordered from a
+ * Allocates its scratch -- the activation operand plane for tokens padded to
+ * a multiple of 128 (nt_pad*id*2 bytes for MMQ_ARM_F16 and MMQ_ARM_RAW, plus
+ * nt_pad*(id/32)*8 of per-block scales; nt_pad*id*4 of hi + lo images for
+ * MMQ_ARM_SPLIT; about 1/16 more for q4_K's min images), and for a stream-K
+ * launch of the fp16-plane arm one 64 KB partial tile per CTA -- stream-ordered from a
  * library-private memory pool and frees it stream-ordered; while `stream` is
  * being captured into a CUDA graph the scratch becomes a graph memory node
  * (cudaMallocAsync), so the call can be captured and replayed.
