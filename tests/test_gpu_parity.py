@@ -18,6 +18,8 @@ pytestmark = pytest.mark.gpu
 RTOL_MAX = 1e-3
 ATOL = 1e-5
 QT = {"q4_K": oracle.Q4_K, "q6_K": oracle.Q6_K}
+# the four layer-sized workloads (q-proj 3584 x 3584 and the FFN matrices)
+FULL_SIZE = [c for c in gen.CONFIGS if c.od * c.id >= 3584 * 3584]
 
 
 @pytest.fixture(scope="module")
@@ -584,7 +586,7 @@ def test_q6k_one_plane_and_two_plane_operands(mmq, od, id_, nt):
     assert operand_bytes["int8"] == 2 * operand_bytes["small"]
 
 
-@pytest.mark.parametrize("cfg", [c for c in gen.CONFIGS[1:5] if c.qtype == "q6_K"], ids=lambda c: c.name)
+@pytest.mark.parametrize("cfg", [c for c in FULL_SIZE if c.qtype == "q6_K"], ids=lambda c: c.name)
 def test_two_plane_q6k_workloads_sampled(mmq, cfg):
     """The q6_K workloads' shapes with scales over the int8 range (the format's
     usual encoding): the two-plane operand on both arms, at full size, sampled
@@ -604,7 +606,7 @@ def test_two_plane_q6k_workloads_sampled(mmq, cfg):
     w.release()
 
 
-@pytest.mark.parametrize("cfg", gen.CONFIGS[1:5], ids=lambda c: c.name)
+@pytest.mark.parametrize("cfg", FULL_SIZE, ids=lambda c: c.name)
 def test_split_arm_workloads_sampled(mmq, cfg):
     W, X = gen.config_inputs(cfg)
     w = mmq.mmq_register_weights(cfg.qtype, torch.from_numpy(W).cuda(), cfg.od, cfg.id)

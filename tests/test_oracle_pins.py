@@ -371,7 +371,7 @@ def test_misstrided_consumer_fails_except_row_zero():
 # --------------------------------------------------------------------------
 def test_mac_count_golden(golden):
     kv = {r[0]: int(r[1]) for r in golden("mac_count.txt")}
-    cfg = gen.CONFIGS[1]
+    cfg = gen.config_by_name("q4_K_qproj_3584x3584_nt512")
     assert (cfg.nt, cfg.od, cfg.id) == (kv["nt"], kv["od"], kv["id"])
     assert cfg.ops == 2 * kv["imma_count"] * kv["macs_per_imma"]
 
