@@ -474,14 +474,15 @@ __device__ __forceinline__ int split_scale_exp(float m) {
   return min(30, max(-30, 14 - e));
 }
 
-// two fp16 integers (one word) times da_s -> hi word and lo word
+// two fp16 integers (one word) times da_s -> hi word and lo word, both lanes
+// of the pair at once (packed fp32x2 arithmetic, paired fp16 conversions)
 __device__ __forceinline__ void split_word(uint32_t hq, float da_s, uint32_t &hi, uint32_t &lo) {
-  const __half2 q2 = *reinterpret_cast<const __half2 *>(&hq);
-  const float a0 = da_s * __low2float(q2), a1 = da_s * __high2float(q2);  // exact
-  const __half h0 = __float2half_rn(a0), h1 = __float2half_rn(a1);
-  const __half l0 = __float2half_rn(a0 - __half2float(h0)), l1 = __float2half_rn(a1 - __half2float(h1));
-  hi = static_cast<uint32_t>(__half_as_ushort(h0)) | (static_cast<uint32_t>(__half_as_ushort(h1)) << 16);
-  lo = static_cast<uint32_t>(__half_as_ushort(l0)) | (static_cast<uint32_t>(__half_as_ushort(l1)) << 16);
+  const float2 a = __fmul2_rn(make_float2(da_s, da_s), __half22float2(*reinterpret_cast<const __half2 *>(&hq)));
+  const __half2 h = __float22half2_rn(a);  // a is exact; h = rn(a) per lane
+  // a - h is exact in fp32; fma(h, -1, a) forms it in one packed instruction
+  const __half2 l = __float22half2_rn(__ffma2_rn(__half22float2(h), make_float2(-1.0f, -1.0f), a));
+  hi = *reinterpret_cast<const uint32_t *>(&h);
+  lo = *reinterpret_cast<const uint32_t *>(&l);
 }
 
 // Lane `part` of block c's eight: its 4 values into the hi and lo images, and
