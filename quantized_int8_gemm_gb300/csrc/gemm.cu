@@ -310,13 +310,13 @@ __global__ void __launch_bounds__(128) gemm_prepass_kernel(const uint8_t *__rest
 // min slots are bit-identical to the two-kernel path.  For q4_K the token's
 // scale exponent s_t needs every block first: a first pass computes it, the
 // second (reading X again, from L2) writes the planes.
-__device__ __forceinline__ void quant_block8(float4 v, float &d, float &d16f, uint32_t &h01,
-                                             uint32_t &h23, int &ssum) {
+__device__ __forceinline__ void quant_codes8(float4 v, float &d, float &d16f, int (&q)[4], int &ssum) {
   float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
 #pragma unroll
   for (int m = 1; m < 8; m <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
   d = amax / 127.0f;
-  int q[4] = {0, 0, 0, 0};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) q[i] = 0;
   if (amax != 0.0f) {
     const float xs[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -326,6 +326,13 @@ __device__ __forceinline__ void quant_block8(float4 v, float &d, float &d16f, ui
 #pragma unroll
   for (int m = 1; m < 8; m <<= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, m);
   d16f = amax != 0.0f ? __half2float(__float2half_rn(d)) : 0.0f;
+}
+
+// the same, with the codes as two words of fp16 integers
+__device__ __forceinline__ void quant_block8(float4 v, float &d, float &d16f, uint32_t &h01,
+                                             uint32_t &h23, int &ssum) {
+  int q[4];
+  quant_codes8(v, d, d16f, q, ssum);
   h01 = static_cast<uint32_t>(__half_as_ushort(__int2half_rn(q[0]))) |
         (static_cast<uint32_t>(__half_as_ushort(__int2half_rn(q[1]))) << 16);
   h23 = static_cast<uint32_t>(__half_as_ushort(__int2half_rn(q[2]))) |
@@ -474,10 +481,10 @@ __device__ __forceinline__ int split_scale_exp(float m) {
   return min(30, max(-30, 14 - e));
 }
 
-// two fp16 integers (one word) times da_s -> hi word and lo word, both lanes
+// two integer codes (as fp32) times da_s -> hi word and lo word, both lanes
 // of the pair at once (packed fp32x2 arithmetic, paired fp16 conversions)
-__device__ __forceinline__ void split_word(uint32_t hq, float da_s, uint32_t &hi, uint32_t &lo) {
-  const float2 a = __fmul2_rn(make_float2(da_s, da_s), __half22float2(*reinterpret_cast<const __half2 *>(&hq)));
+__device__ __forceinline__ void split_pair(float2 q, float da_s, uint32_t &hi, uint32_t &lo) {
+  const float2 a = __fmul2_rn(make_float2(da_s, da_s), q);
   const __half2 h = __float22half2_rn(a);  // a is exact; h = rn(a) per lane
   // a - h is exact in fp32; fma(h, -1, a) forms it in one packed instruction
   const __half2 l = __float22half2_rn(__ffma2_rn(__half22float2(h), make_float2(-1.0f, -1.0f), a));
@@ -489,7 +496,7 @@ __device__ __forceinline__ void split_word(uint32_t hq, float da_s, uint32_t &hi
 // (part 0, q4_K) the block's min-term slots.
 template <bool kQ4>
 __device__ __forceinline__ void emit_split(uint8_t *__restrict__ aplane, int64_t t, int64_t c, int64_t nb32,
-                                           int part, uint32_t h01, uint32_t h23, float d16f, int ssum,
+                                           int part, float2 q01, float2 q23, float d16f, int ssum,
                                            float scale) {
   const int64_t nsb = nb32 / 8;
   const int r = static_cast<int>(t & (kTileM - 1));
@@ -497,8 +504,8 @@ __device__ __forceinline__ void emit_split(uint8_t *__restrict__ aplane, int64_t
   const uint32_t off = split_off(r, static_cast<int>(c & 3) * 32 + 4 * part);
   const float da_s = d16f * scale;
   uint32_t hi0, lo0, hi1, lo1;
-  split_word(h01, da_s, hi0, lo0);
-  split_word(h23, da_s, hi1, lo1);
+  split_pair(q01, da_s, hi0, lo0);
+  split_pair(q23, da_s, hi1, lo1);
   *reinterpret_cast<uint2 *>(blk + off) = make_uint2(hi0, hi1);
   *reinterpret_cast<uint2 *>(blk + kSplitLo + off) = make_uint2(lo0, lo1);
   if (kQ4 && part == 0) {
@@ -518,24 +525,32 @@ __device__ __forceinline__ float split_range(float d16f, int ssum) {
   return kQ4 ? fmaxf(m, fabsf(d16f * static_cast<float>(ssum))) : m;
 }
 
-constexpr int kSplitStashBytesPerBlock = 72;  // 16 words of fp16 q, d16, ssum
+constexpr int kSplitStashBytesPerBlock = 40;  // 8 words of four int8 codes, d16, ssum
+
+// the four int8 codes of one word as two fp32 pairs (low byte first)
+__device__ __forceinline__ void codes_of_word(uint32_t w, float2 &q01, float2 &q23) {
+  q01 = make_float2(static_cast<float>(static_cast<int8_t>(w & 0xFF)),
+                    static_cast<float>(static_cast<int8_t>((w >> 8) & 0xFF)));
+  q23 = make_float2(static_cast<float>(static_cast<int8_t>((w >> 16) & 0xFF)),
+                    static_cast<float>(static_cast<int8_t>(w >> 24)));
+}
 
 // From fp32 X: one CTA of eight warps per token, eight lanes per block; the
 // first pass quantizes (q8_0, as quantize.cu) and keeps each block in shared
 // memory (kStash) for the second, or the second quantizes again.
 template <bool kQ4, bool kStash>
-__global__ void __launch_bounds__(32 * kQuantWarps) split_prepass_f32_kernel(const float *__restrict__ X,
+__global__ void __launch_bounds__(32 * kQuantWarps, kStash ? 5 : 4) split_prepass_f32_kernel(const float *__restrict__ X,
                                                                    int64_t nt, int64_t nb32,
                                                                    uint8_t *__restrict__ aplane,
                                                                    float *__restrict__ invp) {
-  extern __shared__ uint32_t sstash[];  // [nb32][16] fp16 q words, then [nb32] d16, [nb32] ssum
+  extern __shared__ uint32_t sstash[];  // [nb32][8] words of int8 codes, then [nb32] d16, [nb32] ssum
   griddep_launch_dependents();
   const int64_t t = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int part = lane & 7, grp = lane >> 3;
   const bool live = t < nt;  // rows nt .. nt_pad - 1 of the last tile: a zero activation row
   const float4 *xrow = reinterpret_cast<const float4 *>(X + (live ? t : 0) * nb32 * 32);
-  float *sd16 = reinterpret_cast<float *>(sstash + nb32 * 16);
+  float *sd16 = reinterpret_cast<float *>(sstash + nb32 * 8);
   int *sssum = reinterpret_cast<int *>(sd16 + nb32);
   float gmax = 0.f;
   for (int64_t base = warp * 16; base < nb32; base += 16 * kQuantWarps) {
@@ -549,13 +564,13 @@ __global__ void __launch_bounds__(32 * kQuantWarps) split_prepass_f32_kernel(con
     for (int u = 0; u < 4; ++u) {
       const int64_t c = base + u * 4 + grp;
       float d, d16f;
-      uint32_t h01, h23;
-      int ssum;
-      quant_block8(v[u], d, d16f, h01, h23, ssum);
+      int q[4], ssum;
+      quant_codes8(v[u], d, d16f, q, ssum);
       if (c >= nb32) continue;
       gmax = fmaxf(gmax, split_range<kQ4>(d16f, ssum));
       if (kStash) {
-        reinterpret_cast<uint2 *>(sstash + c * 16)[part] = make_uint2(h01, h23);
+        sstash[c * 8 + part] = (static_cast<uint32_t>(q[0]) & 0xFFu) | ((static_cast<uint32_t>(q[1]) & 0xFFu) << 8) |
+                               ((static_cast<uint32_t>(q[2]) & 0xFFu) << 16) | (static_cast<uint32_t>(q[3]) << 24);
         if (part == 0) {
           sd16[c] = d16f;
           sssum[c] = ssum;
@@ -575,8 +590,9 @@ __global__ void __launch_bounds__(32 * kQuantWarps) split_prepass_f32_kernel(con
   if (tid == 0) invp[t] = __uint_as_float(static_cast<uint32_t>(127 - s) << 23);
   if (kStash) {
     for (int64_t c = tid >> 3; c < nb32; c += 4 * kQuantWarps) {
-      const uint2 hw = reinterpret_cast<const uint2 *>(sstash + c * 16)[part];
-      emit_split<kQ4>(aplane, t, c, nb32, part, hw.x, hw.y, sd16[c], sssum[c], scale);
+      float2 q01, q23;
+      codes_of_word(sstash[c * 8 + part], q01, q23);
+      emit_split<kQ4>(aplane, t, c, nb32, part, q01, q23, sd16[c], sssum[c], scale);
     }
   } else {
     for (int64_t base = warp * 16; base < nb32; base += 16 * kQuantWarps) {
@@ -590,10 +606,11 @@ __global__ void __launch_bounds__(32 * kQuantWarps) split_prepass_f32_kernel(con
       for (int u = 0; u < 4; ++u) {
         const int64_t c = base + u * 4 + grp;
         float d, d16f;
-        uint32_t h01, h23;
-        int ssum;
-        quant_block8(v[u], d, d16f, h01, h23, ssum);
-        if (c < nb32) emit_split<kQ4>(aplane, t, c, nb32, part, h01, h23, d16f, ssum, scale);
+        int q[4], ssum;
+        quant_codes8(v[u], d, d16f, q, ssum);
+        if (c < nb32)
+          emit_split<kQ4>(aplane, t, c, nb32, part, make_float2(static_cast<float>(q[0]), static_cast<float>(q[1])),
+                          make_float2(static_cast<float>(q[2]), static_cast<float>(q[3])), d16f, ssum, scale);
       }
     }
   }
@@ -630,15 +647,9 @@ __global__ void __launch_bounds__(128) split_prepass_q_kernel(const uint8_t *__r
     const float d16f = live ? __half2float(*reinterpret_cast<const __half *>(b)) : 0.f;
     const int ssum = live ? *reinterpret_cast<const int *>(b + 36) : 0;
     const uint32_t q4b = live ? *reinterpret_cast<const uint32_t *>(b + 4 + 4 * part) : 0u;
-    uint32_t h[2];
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const int q0 = static_cast<int8_t>((q4b >> (16 * j)) & 0xFF);
-      const int q1 = static_cast<int8_t>((q4b >> (16 * j + 8)) & 0xFF);
-      h[j] = static_cast<uint32_t>(__half_as_ushort(__int2half_rn(q0))) |
-             (static_cast<uint32_t>(__half_as_ushort(__int2half_rn(q1))) << 16);
-    }
-    emit_split<kQ4>(aplane, t, c, nb32, part, h[0], h[1], d16f, ssum, scale);
+    float2 q01, q23;
+    codes_of_word(q4b, q01, q23);
+    emit_split<kQ4>(aplane, t, c, nb32, part, q01, q23, d16f, ssum, scale);
   }
 }
 
