@@ -535,6 +535,11 @@ SPLIT_SHAPES = [
     ("q6_K", 3456, 3584, 300, 47),
     # 28 super-blocks per tile: the min term's region hand-off over a long tile
     ("q4_K", 896, 7168, 200, 48),
+    # 688 blocks per token: the quantization kernel keeps them in shared memory
+    ("q6_K", 130, 22016, 70, 49),
+    # 1280 blocks per token, past the shared-memory stash: two passes over X
+    ("q4_K", 64, 40960, 5, 50),
+    ("q6_K", 64, 40960, 5, 51),
 ]
 
 
