@@ -92,7 +92,7 @@ typedef struct mmq_weights_s *mmq_weights_t;
                               operand (every |sc| <= 64), and for q4_K when the split arm
                               runs 256-row weight tiles (problems with more 128 x 128
                               output tiles than SMs); else MMQ_ARM_F16 */
-#define MMQ_ARM_F16 1      /* operands from the registered fp16 operand plane (TMA copy) */
+#define MMQ_ARM_F16 1      /* operands from the registered fp16 operand plane (bulk copies) */
 #define MMQ_ARM_RAW 2      /* packed weight bytes streamed and unpacked to fp16 in shared
                               memory inside the GEMM ("47 · r44 — W_exp stride mismatch
                               root cause", §3.2: the in-kernel recombination); needs a
@@ -263,8 +263,14 @@ int mmq_gemm_f32_profiled(mmq_weights_t h, const float *X, int64_t nt, float *Y,
  *     MMQ_ERR_SCRATCH_LIMIT.  Scratch per token, with nt rounded up to a
  *     multiple of 128: id*2 + (id/32)*4 + 4 bytes, plus (id/256)*32 for q4_K;
  *     e.g. id = 3584 allows up to 2048 (q4_K) or 2176 (q6_K) tokens.
- *   - The first call on a device looks up the array's device address (once
- *     per device); make that first call before any stream capture.
+ *   - mmq_register_weights prepares what this entry point launches: it
+ *     looks up the array's device address on its device and loads the
+ *     GEMM's module and kernels there.  Without that, CUDA's lazy module
+ *     loading (the default since CUDA 12.2) would load them -- allocating
+ *     the array and the kernels' code -- inside the first call here.  So,
+ *     after a registration on the device, no call allocates; the first call
+ *     on a device still looks the address up in a host-side table, so make
+ *     it before any stream capture.
  *   - Every call shares the one array, which keeps the previous call's
  *     contents; each call rewrites or clears everything it reads.  Calls
  *     that can overlap on the GPU (different streams, no ordering) race on

@@ -22,6 +22,8 @@ from .oracle import (  # noqa: F401
     gemm,
     gemm_entries,
     gemm_entries_int,
+    gemm_mt,
+    host_threads,
     lib,
     q4k_quant,
     q4k_scale_min,

@@ -38,6 +38,7 @@
  * without -ffast-math.  Sums are accumulated in fp64.
  */
 #include <math.h>
+#include <pthread.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -423,4 +424,82 @@ int mmq_oracle_gemm(int type, const uint8_t *W, int64_t od, int64_t id, const ui
     free(xh);
     free(wr);
     return 0;
+}
+
+/* The same output as mmq_oracle_gemm, with the weight rows shared out over
+ * nthreads POSIX threads (contiguous row ranges).  Each output is the same
+ * fp64 sum in the same order as there, so Y is identical bit for bit; only
+ * the timing changes (the bench's CPU baseline runs on every host core). */
+struct or_gemm_job {
+    int type;
+    const uint8_t *W;
+    int64_t od, id, nt, o0, o1;
+    const double *xh;
+    double *Y;
+    int rc;
+};
+
+static void *or_gemm_rows(void *arg) {
+    struct or_gemm_job *j = (struct or_gemm_job *)arg;
+    double *wr = (double *)malloc(sizeof(double) * (size_t)j->id);
+    if (!wr) {
+        j->rc = -3;
+        return NULL;
+    }
+    for (int64_t o = j->o0; o < j->o1; ++o) {
+        mmq_oracle_dequant_weights(j->type, j->W, j->od, j->id, o, o + 1, wr);
+        for (int64_t t = 0; t < j->nt; ++t) {
+            const double *x = j->xh + t * j->id;
+            double acc = 0.0;
+            for (int64_t k = 0; k < j->id; ++k) acc += wr[k] * x[k];
+            j->Y[t * j->od + o] = acc;
+        }
+    }
+    free(wr);
+    j->rc = 0;
+    return NULL;
+}
+
+int mmq_oracle_gemm_mt(int type, const uint8_t *W, int64_t od, int64_t id, const uint8_t *Q,
+                       int64_t nt, double *Y, int nthreads) {
+    if (block_bytes(type) < 0 || id <= 0 || id % 256 != 0 || nt < 0 || od < 0) return -1;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 1024) nthreads = 1024;
+    if ((int64_t)nthreads > od && od > 0) nthreads = (int)od;
+    double *xh = (double *)malloc(sizeof(double) * (size_t)(nt > 0 ? nt : 1) * (size_t)id);
+    struct or_gemm_job *jobs = (struct or_gemm_job *)calloc((size_t)nthreads, sizeof(*jobs));
+    pthread_t *th = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    int *started = (int *)calloc((size_t)nthreads, sizeof(int));
+    if (!xh || !jobs || !th || !started) {
+        free(xh);
+        free(jobs);
+        free(th);
+        free(started);
+        return -3;
+    }
+    mmq_oracle_dequant_act(Q, nt, id, xh);
+    int rc = 0;
+    for (int i = 0; i < nthreads; ++i) {
+        jobs[i].type = type;
+        jobs[i].W = W;
+        jobs[i].od = od;
+        jobs[i].id = id;
+        jobs[i].nt = nt;
+        jobs[i].o0 = od * i / nthreads;
+        jobs[i].o1 = od * (i + 1) / nthreads;
+        jobs[i].xh = xh;
+        jobs[i].Y = Y;
+        jobs[i].rc = -3;
+        started[i] = pthread_create(&th[i], NULL, or_gemm_rows, &jobs[i]) == 0;
+        if (!started[i]) or_gemm_rows(&jobs[i]); /* no thread: run the range here */
+    }
+    for (int i = 0; i < nthreads; ++i) {
+        if (started[i]) pthread_join(th[i], NULL);
+        if (jobs[i].rc != 0) rc = jobs[i].rc;
+    }
+    free(xh);
+    free(jobs);
+    free(th);
+    free(started);
+    return rc;
 }

@@ -34,7 +34,7 @@ def build(force: bool = False) -> str:
             and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
         return _LIB
     tmp = _LIB + f".tmp{os.getpid()}"
-    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-pthread",
            "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB)
@@ -74,6 +74,9 @@ def lib() -> ctypes.CDLL:
                 fn.restype = ctypes.c_int
             L.mmq_oracle_gemm.argtypes = [ctypes.c_int, _ptr, _i64, _i64, _ptr, _i64, _ptr]
             L.mmq_oracle_gemm.restype = ctypes.c_int
+            L.mmq_oracle_gemm_mt.argtypes = [ctypes.c_int, _ptr, _i64, _i64, _ptr, _i64, _ptr,
+                                             ctypes.c_int]
+            L.mmq_oracle_gemm_mt.restype = ctypes.c_int
             L.mmq_oracle_chunk_partials.argtypes = [ctypes.c_int, _ptr, _i64, _i64, _ptr, _i64, _ptr]
             L.mmq_oracle_chunk_partials.restype = ctypes.c_int
             _lib = L
@@ -229,4 +232,28 @@ def gemm(qtype: int, W: np.ndarray, od: int, id_: int, Q: np.ndarray, nt: int) -
     rc = lib().mmq_oracle_gemm(qtype, _p(W), od, id_, _p(Q), nt, _p(Y))
     if rc != 0:
         raise ValueError(f"oracle gemm failed rc={rc}")
+    return Y
+
+
+def host_threads() -> int:
+    """Threads the host can run at once (the CPU baseline uses all of them)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+def gemm_mt(qtype: int, W: np.ndarray, od: int, id_: int, Q: np.ndarray, nt: int,
+            threads: int | None = None) -> np.ndarray:
+    """gemm() with the weight rows shared out over `threads` host threads
+    (default: all of them); the same values bit for bit."""
+    W = np.ascontiguousarray(W, dtype=np.uint8)
+    Q = np.ascontiguousarray(Q, dtype=np.uint8)
+    assert W.size == od * (id_ // 256) * _block_bytes(qtype)
+    assert Q.size == nt * (id_ // 32) * 40
+    Y = np.empty((nt, od), dtype=np.float64)
+    n = host_threads() if threads is None else int(threads)
+    rc = lib().mmq_oracle_gemm_mt(qtype, _p(W), od, id_, _p(Q), nt, _p(Y), n)
+    if rc != 0:
+        raise ValueError(f"oracle gemm_mt failed rc={rc}")
     return Y

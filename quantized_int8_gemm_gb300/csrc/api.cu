@@ -1,7 +1,6 @@
 // api.cu -- the extern "C" entry points of libmmq.so (declared in mmq.h):
-// argument validation, per-device state, registration bookkeeping, tensor
-// maps and launches.  No arithmetic of the method happens on the host.
-#include <cuda.h>
+// argument validation, per-device state, registration bookkeeping, scratch
+// and launches.  No arithmetic of the method happens on the host.
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -179,6 +178,10 @@ int mmq_register_weights(int type, const void *W, int64_t od, int64_t id, uint32
     if (e == cudaSuccess) e = mmq::launch_register_b0(h, static_cast<const uint8_t *>(W), s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   }
+  // load what mmq_gemm_noalloc will launch for this handle now, while
+  // allocating is allowed (lazy module loading would otherwise do it, and
+  // allocate, inside that call)
+  if (e == cudaSuccess) e = mmq::prepare_noalloc(h);
   if (e != cudaSuccess) rc = cuda_rc(e);
   if (rc != MMQ_OK) {
     free_planes(h);

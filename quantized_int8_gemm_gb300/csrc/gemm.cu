@@ -1722,6 +1722,30 @@ cudaError_t noalloc_scratch(int dev, void **out) {
 }
 
 namespace {
+template <bool kQ4, bool kSK, bool kRaw, bool kB0, bool kDump>
+cudaError_t prepare_variant(int dev);
+}  // namespace
+
+// Everything the whole-tile fp16-plane GEMM of a handle needs loaded on its
+// device: the module holding the fixed scratch array (its address looked up),
+// the activation prepass and the GEMM kernel variant.  With lazy module
+// loading these load on first use, and loading allocates device memory (the
+// array, the kernels' code); registration calls this, so a later
+// mmq_gemm_noalloc on the same handle loads nothing.
+cudaError_t prepare_noalloc(const mmq_weights_s *h) {
+  void *p = nullptr;
+  cudaError_t e = noalloc_scratch(h->device, &p);
+  if (e != cudaSuccess) return e;
+  cudaFuncAttributes fa;
+  const bool q4 = h->type == MMQ_Q4_K;
+  e = q4 ? cudaFuncGetAttributes(&fa, gemm_prepass_kernel<true>) : cudaFuncGetAttributes(&fa, gemm_prepass_kernel<false>);
+  if (e != cudaSuccess) return e;
+  if (q4) return prepare_variant<true, false, false, false, false>(h->device);
+  return h->b0plane ? prepare_variant<false, false, false, true, false>(h->device)
+                    : prepare_variant<false, false, false, false, false>(h->device);
+}
+
+namespace {
 
 // SM count of a device, read once.
 int num_sms(int dev) {
@@ -1788,11 +1812,7 @@ namespace {
 // per device, of the shared-memory opt-in and of the register count the
 // register split was planned for (a mismatch would stall setmaxnreg).
 template <bool kQ4, bool kSK, bool kRaw, bool kB0, bool kDump = false>
-cudaError_t launch_variant(int dev, int grid, cudaStream_t s, const uint8_t *aplane, const uint8_t *bplane,
-                           const uint8_t *rawplane, const uint8_t *b0plane, const uint8_t *bscale, const float *dap,
-                           const float *invp, int64_t nt, int64_t od, int64_t nb32, int n_tt, int n_ot,
-                           float *Y, WaitCtl w, float4 *ws, uint64_t *flags, bool pdl,
-                           float *dump = nullptr) {
+cudaError_t prepare_variant(int dev) {
   auto kern = mmq_gemm_kernel<kQ4, kSK, kRaw, kB0, kDump>;
   constexpr int smem = Smem<kQ4, kRaw, kB0>::kBytes;
   static std::atomic<int> ready[64];  // 0 unknown, 1 ready, 2 unusable
@@ -1805,7 +1825,18 @@ cudaError_t launch_variant(int dev, int grid, cudaStream_t s, const uint8_t *apl
     st = fa.numRegs == Shape<kRaw>::kRegsLaunch ? 1 : 2;
     ready[dev].store(st);
   }
-  if (st != 1) return cudaErrorInvalidKernelImage;
+  return st == 1 ? cudaSuccess : cudaErrorInvalidKernelImage;
+}
+
+template <bool kQ4, bool kSK, bool kRaw, bool kB0, bool kDump = false>
+cudaError_t launch_variant(int dev, int grid, cudaStream_t s, const uint8_t *aplane, const uint8_t *bplane,
+                           const uint8_t *rawplane, const uint8_t *b0plane, const uint8_t *bscale, const float *dap,
+                           const float *invp, int64_t nt, int64_t od, int64_t nb32, int n_tt, int n_ot,
+                           float *Y, WaitCtl w, float4 *ws, uint64_t *flags, bool pdl,
+                           float *dump = nullptr) {
+  auto kern = mmq_gemm_kernel<kQ4, kSK, kRaw, kB0, kDump>;
+  constexpr int smem = Smem<kQ4, kRaw, kB0>::kBytes;
+  if (const cudaError_t e = prepare_variant<kQ4, kSK, kRaw, kB0, kDump>(dev); e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(Shape<kRaw>::kThreads);

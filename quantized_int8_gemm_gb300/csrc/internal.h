@@ -1,6 +1,5 @@
 // internal.h -- declarations shared by the translation units of libmmq.so.
 #pragma once
-#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -88,5 +87,8 @@ cudaError_t launch_wait_selftest(DevStatus *st, unsigned epoch, uint64_t limit_n
 // Fixed scratch of mmq_gemm_noalloc (a static device array in gemm.cu).
 constexpr size_t kNoallocScratchBytes = size_t(16) << 20;
 cudaError_t noalloc_scratch(int dev, void **out);
+// Loads, on the handle's device, the scratch array's module and the kernels
+// mmq_gemm_noalloc launches for this handle (registration calls it).
+cudaError_t prepare_noalloc(const mmq_weights_s *h);
 
 }  // namespace mmq

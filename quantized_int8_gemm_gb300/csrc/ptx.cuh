@@ -1,8 +1,8 @@
-// ptx.cuh -- thin inline-PTX wrappers for sm_103a: mbarrier, TMA
-// (cp.async.bulk.tensor), tcgen05 (TMEM alloc, UMMA, commit, ld) and the
-// shared-memory / instruction descriptors UMMA consumes.
+// ptx.cuh -- thin inline-PTX wrappers for sm_103a: mbarrier, bulk-copy L2
+// prefetch, tcgen05 (TMEM alloc, UMMA, commit, ld) and the shared-memory /
+// instruction descriptors UMMA consumes.  (The operand copies themselves are
+// 1-D cp.async.bulk, issued where they are used.)
 #pragma once
-#include <cuda.h>
 #include <cstdint>
 
 namespace mmq {
@@ -107,19 +107,6 @@ __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wa
 // Prefetch `bytes` (a multiple of 16) at a 16-byte aligned global address into L2.
 __device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
-// ---------------------------------------------------------------- TMA
-__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *m) {
-  asm volatile("prefetch.tensormap [%0];" ::"l"(m) : "memory");
-}
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *m, uint32_t bar,
-                                            int32_t x, int32_t y) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-      "l"(m), "r"(bar), "r"(x), "r"(y)
-      : "memory");
 }
 
 // ---------------------------------------------------------------- tcgen05

@@ -647,3 +647,51 @@ def test_split_arm_wide_tiles(mmq, name, od):
     # every output written, and within fp32 summation of the exact-partials arm
     assert float((Y - Y16).abs().max()) <= 1e-5 * float(Y16.abs().max())
     w.release()
+
+
+# --------------------------------------------------------------------------
+# the FFN-down workload with the pre-expanded W_exp plane, at full size
+def test_ffn_down_workload_with_wexp_plane_through_the_gemm(mmq):
+    """q6_K 3584 x 18944, nt = 2630, registered with MMQ_REG_WEXP: the operand
+    plane is then rebuilt from the dense W_exp plane, so this is the consumer
+    gate of "47 · r44 — W_exp stride mismatch root cause" (§2.5) on the
+    workload's own shape -- the plane byte-exact, and the GEMM through it on
+    every arm that reads it against the oracle on sampled outputs and the
+    tile edges."""
+    cfg = gen.config_by_name("q6_K_ffn_down_3584x18944_nt2630")
+    W, X = gen.config_inputs(cfg)
+    w = mmq.mmq_register_weights("q6_K", torch.from_numpy(W).cuda(), cfg.od, cfg.id, mmq.MMQ_REG_WEXP)
+    assert np.array_equal(mmq.mmq_weights_wexp(w).cpu().numpy(), oracle.expand_q6k_dense(W, cfg.od, cfg.id))
+    Xd = torch.from_numpy(X).cuda()
+    ts, os_ = _sample_entries(cfg.nt, cfg.od, 800, cfg.seed + 11)
+    y_ref = oracle.gemm_entries(oracle.Q6_K, W, cfg.od, cfg.id, oracle.quantize_q8_0(X), cfg.nt, ts, os_)
+    for arm in (mmq.MMQ_ARM_AUTO, mmq.MMQ_ARM_SPLIT, mmq.MMQ_ARM_F16):
+        Y, used = mmq.mmq_gemm_f32(w, Xd, flags=arm, return_arm=True)
+        torch.cuda.synchronize()
+        assert mmq.mmq_last_device_error() == 0
+        Yn = Y.cpu().numpy()
+        assert np.isfinite(Yn).all()
+        err, bound = _within_tol(Yn[ts, os_], y_ref)
+        assert err <= bound, (mmq.ARM_NAMES[used], err, bound)
+    w.release()
+
+
+@pytest.mark.parametrize("name", ["q4_K_qproj_3584x3584_nt512", "q6_K_ffn_down_3584x18944_nt2630"])
+def test_raw_arm_workloads_sampled_against_oracle(mmq, name):
+    """The raw arm (packed weight bytes unpacked inside the GEMM) on the q-proj
+    and FFN-down workloads at full size, against the oracle directly (sampled
+    outputs and tile edges), not only against the fp16-plane arm."""
+    cfg = gen.config_by_name(name)
+    W, X = gen.config_inputs(cfg)
+    w = mmq.mmq_register_weights(cfg.qtype, torch.from_numpy(W).cuda(), cfg.od, cfg.id, mmq.MMQ_REG_RAW)
+    Y, used = mmq.mmq_gemm_f32(w, torch.from_numpy(X).cuda(), flags=mmq.MMQ_ARM_RAW, return_arm=True)
+    torch.cuda.synchronize()
+    assert mmq.mmq_last_device_error() == 0
+    assert used == mmq.MMQ_ARM_RAW
+    Yn = Y.cpu().numpy()
+    assert np.isfinite(Yn).all()
+    ts, os_ = _sample_entries(cfg.nt, cfg.od, 3000 if cfg.id <= 4096 else 800, cfg.seed + 13)
+    y_ref = oracle.gemm_entries(QT[cfg.qtype], W, cfg.od, cfg.id, oracle.quantize_q8_0(X), cfg.nt, ts, os_)
+    err, bound = _within_tol(Yn[ts, os_], y_ref)
+    assert err <= bound, (err, bound)
+    w.release()

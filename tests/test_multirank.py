@@ -61,3 +61,76 @@ def test_reference_arm_runs_on_rank_zero_only(capsys):
     args = types.SimpleNamespace(steps=3, warmup=3, gpus=2)
     assert bench.run_reference(args, gen.config_by_name("q6_K_tiny_256x512_nt16"), rank=1) is None
     assert capsys.readouterr().out == ""
+
+
+# --------------------------------------------------------------------------
+# column-parallel split of the GEMM over ranks (shard.py)
+def test_od_slices_cover_the_rows_in_tile_multiples():
+    from quantized_int8_gemm_gb300 import shard
+    for od in (1, 127, 128, 300, 3584, 18944, 1000):
+        for world in (1, 2, 3, 4, 8):
+            sl = shard.od_slices(od, world)
+            assert len(sl) == world
+            assert sl[0][0] == 0 and sl[-1][1] == od
+            for (a0, a1), (b0, b1) in zip(sl, sl[1:]):
+                assert a1 == b0                        # contiguous, no overlap
+            for o0, o1 in sl[:-1]:
+                assert o0 % 128 == 0 and (o1 - o0) % 128 == 0 or o1 == od
+            widths = [o1 - o0 for o0, o1 in sl]
+            units = [-(-w // 128) for w in widths]
+            assert max(units) - min(units) <= 1        # balanced to one tile
+    assert shard.od_slices(3584, 8) == [(0, 512), (512, 1024), (1024, 1536), (1536, 2048),
+                                        (2048, 2432), (2432, 2816), (2816, 3200), (3200, 3584)]
+
+
+def _shard_rank_main(rank, world, port, qtype, od, id_, nt, out):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import oracle
+    from quantized_int8_gemm_gb300 import shard
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        W = gen.weights(qtype, od, id_, 5)
+        Q = oracle.quantize_q8_0(gen.activations(nt, id_, 6))   # replicated activations
+        slices = shard.od_slices(od, world)
+        o0, o1 = slices[rank]
+        Ws = np.ascontiguousarray(shard.weight_rows(W, qtype, id_, o0, o1))
+        qt = oracle.Q4_K if qtype == "q4_K" else oracle.Q6_K
+        # the rank's own GEMM (here the oracle on its row slice: this test checks
+        # the partition and the gather, not the kernel)
+        y_loc = oracle.gemm(qt, Ws, o1 - o0, id_, Q, nt) if o1 > o0 else np.zeros((nt, 0))
+        y = shard.gather_columns(torch.from_numpy(y_loc), slices)
+        if rank == 0:
+            out.put(y.numpy())
+        dist.barrier()
+    finally:
+        dist.destroy_process_group()
+
+
+def test_column_parallel_gemm_reassembles_the_single_rank_result():
+    """Two gloo ranks, ragged od (300 rows: slices of 256 and 44): every rank
+    computes its row slice of W against the replicated activations, the
+    column slices are gathered, and the assembled Y equals the single-rank
+    result bit for bit (each output is the same sum either way)."""
+    import numpy as np
+
+    import oracle
+    qtype, od, id_, nt = "q4_K", 300, 512, 37
+    ctx = mp.get_context("spawn")
+    out = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_shard_rank_main, args=(r, 2, port, qtype, od, id_, nt, out))
+             for r in range(2)]
+    for p in procs:
+        p.start()
+    y = out.get(timeout=180)
+    for p in procs:
+        p.join(timeout=180)
+        assert p.exitcode == 0
+    W = gen.weights(qtype, od, id_, 5)
+    Q = oracle.quantize_q8_0(gen.activations(nt, id_, 6))
+    assert np.array_equal(y, oracle.gemm(oracle.Q4_K, W, od, id_, Q, nt))

@@ -538,3 +538,15 @@ def test_chunk_partials_brute_force_and_recombination(name, qtype, scales):
              - np.einsum("tc,tc,oc,oc->to", da, ssum, np.repeat(dmin, 8, axis=1), m))
     Y_ref = oracle.gemm(qtype, W, od, id_, Q, nt)
     assert np.allclose(Y, Y_ref, rtol=1e-12, atol=1e-12 * np.abs(Y_ref).max())
+
+
+def test_threaded_gemm_is_the_same_gemm():
+    """The CPU baseline's threaded oracle GEMM shares the weight rows out over
+    threads; every output must be the single-threaded value bit for bit, for
+    thread counts that do and do not divide od (and more threads than rows)."""
+    for qtype, qt, od, id_, nt in (("q4_K", oracle.Q4_K, 37, 512, 9), ("q6_K", oracle.Q6_K, 5, 256, 3)):
+        W = gen.weights(qtype, od, id_, 21)
+        Q = oracle.quantize_q8_0(gen.activations(nt, id_, 22, outlier_p=0.05, outlier_scale=20.0))
+        ref = oracle.gemm(qt, W, od, id_, Q, nt)
+        for threads in (1, 2, 3, 8, 64):
+            assert np.array_equal(oracle.gemm_mt(qt, W, od, id_, Q, nt, threads), ref), (qtype, threads)
