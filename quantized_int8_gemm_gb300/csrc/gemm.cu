@@ -58,6 +58,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "q8.cuh"
 #include "tiling.h"
 
 namespace mmq {
@@ -310,33 +311,14 @@ __global__ void __launch_bounds__(128) gemm_prepass_kernel(const uint8_t *__rest
 // min slots are bit-identical to the two-kernel path.  For q4_K the token's
 // scale exponent s_t needs every block first: a first pass computes it, the
 // second (reading X again, from L2) writes the planes.
-__device__ __forceinline__ void quant_codes8(float4 v, float &d, float &d16f, int (&q)[4], int &ssum) {
-  float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
-#pragma unroll
-  for (int m = 1; m < 8; m <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
-  d = amax / 127.0f;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) q[i] = 0;
-  if (amax != 0.0f) {
-    const float xs[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) q[i] = max(-127, min(127, static_cast<int>(roundf(xs[i] / d))));
-  }
-  ssum = q[0] + q[1] + q[2] + q[3];
-#pragma unroll
-  for (int m = 1; m < 8; m <<= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, m);
-  d16f = amax != 0.0f ? __half2float(__float2half_rn(d)) : 0.0f;
-}
-
-// the same, with the codes as two words of fp16 integers
-__device__ __forceinline__ void quant_block8(float4 v, float &d, float &d16f, uint32_t &h01,
-                                             uint32_t &h23, int &ssum) {
-  int q[4];
-  quant_codes8(v, d, d16f, q, ssum);
-  h01 = static_cast<uint32_t>(__half_as_ushort(__int2half_rn(q[0]))) |
-        (static_cast<uint32_t>(__half_as_ushort(__int2half_rn(q[1]))) << 16);
-  h23 = static_cast<uint32_t>(__half_as_ushort(__int2half_rn(q[2]))) |
-        (static_cast<uint32_t>(__half_as_ushort(__int2half_rn(q[3]))) << 16);
+// the q8_0 rule of quantize.cu (q8.cuh) on one lane's float4 of a block: the
+// block's d16 (as fp32), its code sum and the lane's codes as two half2 words
+__device__ __forceinline__ void quant_block8(float4 v, float &d16f, uint32_t &h01, uint32_t &h23, int &ssum) {
+  float q[4];
+  q8_lane(v, d16f, q);
+  ssum = static_cast<int>(q8_ssum(q));
+  h01 = q8_h2(q[0], q[1]);
+  h23 = q8_h2(q[2], q[3]);
 }
 
 // One 32-value block's fp16 operand words in the token's operand row; lane
@@ -407,10 +389,10 @@ __global__ void __launch_bounds__(32 * kQuantWarps) quantize_prepass_kernel(cons
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int64_t c = base + u * 4 + grp;
-      float d, d16f;
+      float d16f;
       uint32_t h01, h23;
       int ssum;
-      quant_block8(v[u], d, d16f, h01, h23, ssum);
+      quant_block8(v[u], d16f, h01, h23, ssum);
       if (c >= nb32) continue;
       emit_operand<kQ4>(aplane, t, c, nb32, part, h01, h23);
       if (!kQ4) {
@@ -457,10 +439,10 @@ __global__ void __launch_bounds__(32 * kQuantWarps) quantize_prepass_kernel(cons
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int64_t c = base + u * 4 + grp;
-        float d, d16f;
+        float d16f;
         uint32_t h01, h23;
         int ssum;
-        quant_block8(v[u], d, d16f, h01, h23, ssum);
+        quant_block8(v[u], d16f, h01, h23, ssum);
         if (c < nb32 && part == 0) emit_scales<true>(aplane, dap, t, c, nb32, d16f, ssum, scale);
       }
     }
@@ -525,7 +507,7 @@ __device__ __forceinline__ float split_range(float d16f, int ssum) {
   return kQ4 ? fmaxf(m, fabsf(d16f * static_cast<float>(ssum))) : m;
 }
 
-constexpr int kSplitStashBytesPerBlock = 40;  // 8 words of four int8 codes, d16, ssum
+constexpr int kSplitStashBytesPerBlock = 72;  // 32 fp16 codes, d16, ssum
 
 // the four int8 codes of one word as two fp32 pairs (low byte first)
 __device__ __forceinline__ void codes_of_word(uint32_t w, float2 &q01, float2 &q23) {
@@ -535,23 +517,40 @@ __device__ __forceinline__ void codes_of_word(uint32_t w, float2 &q01, float2 &q
                     static_cast<float>(static_cast<int8_t>(w >> 24)));
 }
 
-// From fp32 X: one CTA of eight warps per token, eight lanes per block; the
-// first pass quantizes (q8_0, as quantize.cu) and keeps each block in shared
-// memory (kStash) for the second, or the second quantizes again.
+// Eight consecutive codes (four half2 words, fp16 integers) times da_s ->
+// 16 bytes of the hi image and 16 of the lo image (split_pair per pair).
+__device__ __forceinline__ void split_chunk(uint4 codes, float da_s, uint4 &hi, uint4 &lo) {
+  const uint32_t w[4] = {codes.x, codes.y, codes.z, codes.w};
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    split_pair(__half22float2(*reinterpret_cast<const __half2 *>(&w[i])), da_s, h[i], l[i]);
+  hi = make_uint4(h[0], h[1], h[2], h[3]);
+  lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+// From fp32 X: one CTA of eight warps per token.  Pass one, eight lanes per
+// 32-value block: the q8_0 rule (q8.cuh); each block's codes (fp16), d16 and
+// code sum go to shared memory (kStash), and the token's scale exponent s_t
+// is reduced over its blocks.  Pass two, one thread per 8-value chunk: the
+// chunk's hi and lo words, one 16-byte store each, and (q4_K, first chunk of
+// a block) the block's min-term slots.  Without kStash (tokens too long for
+// shared memory) pass two quantizes X again, per block as in pass one.
 template <bool kQ4, bool kStash>
 __global__ void __launch_bounds__(32 * kQuantWarps, kStash ? 5 : 4) split_prepass_f32_kernel(const float *__restrict__ X,
                                                                    int64_t nt, int64_t nb32,
                                                                    uint8_t *__restrict__ aplane,
                                                                    float *__restrict__ invp) {
-  extern __shared__ uint32_t sstash[];  // [nb32][8] words of int8 codes, then [nb32] d16, [nb32] ssum
+  extern __shared__ uint4 sstash4[];  // [nb32][4] 16-byte code chunks, then [nb32] d16, [nb32] ssum
   griddep_launch_dependents();
   const int64_t t = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int part = lane & 7, grp = lane >> 3;
   const bool live = t < nt;  // rows nt .. nt_pad - 1 of the last tile: a zero activation row
   const float4 *xrow = reinterpret_cast<const float4 *>(X + (live ? t : 0) * nb32 * 32);
-  float *sd16 = reinterpret_cast<float *>(sstash + nb32 * 8);
-  int *sssum = reinterpret_cast<int *>(sd16 + nb32);
+  uint2 *scodes = reinterpret_cast<uint2 *>(sstash4);  // 8 bytes (four codes) per lane of a block
+  float *sd16 = reinterpret_cast<float *>(sstash4 + nb32 * 4);
+  float *sssum = sd16 + nb32;
   float gmax = 0.f;
   for (int64_t base = warp * 16; base < nb32; base += 16 * kQuantWarps) {
     float4 v[4];
@@ -563,14 +562,13 @@ __global__ void __launch_bounds__(32 * kQuantWarps, kStash ? 5 : 4) split_prepas
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int64_t c = base + u * 4 + grp;
-      float d, d16f;
-      int q[4], ssum;
-      quant_codes8(v[u], d, d16f, q, ssum);
+      float d16f, q[4];
+      q8_lane(v[u], d16f, q);
+      const float ssum = kQ4 ? q8_ssum(q) : 0.f;
       if (c >= nb32) continue;
-      gmax = fmaxf(gmax, split_range<kQ4>(d16f, ssum));
+      gmax = fmaxf(gmax, kQ4 ? fmaxf(d16f * 127.0f, fabsf(d16f * ssum)) : d16f * 127.0f);
       if (kStash) {
-        sstash[c * 8 + part] = (static_cast<uint32_t>(q[0]) & 0xFFu) | ((static_cast<uint32_t>(q[1]) & 0xFFu) << 8) |
-                               ((static_cast<uint32_t>(q[2]) & 0xFFu) << 16) | (static_cast<uint32_t>(q[3]) << 24);
+        scodes[c * 8 + part] = make_uint2(q8_h2(q[0], q[1]), q8_h2(q[2], q[3]));
         if (part == 0) {
           sd16[c] = d16f;
           sssum[c] = ssum;
@@ -588,11 +586,32 @@ __global__ void __launch_bounds__(32 * kQuantWarps, kStash ? 5 : 4) split_prepas
   const int s = split_scale_exp(gmax);
   const float scale = __uint_as_float(static_cast<uint32_t>(127 + s) << 23);
   if (tid == 0) invp[t] = __uint_as_float(static_cast<uint32_t>(127 - s) << 23);
+  const int64_t nsb = nb32 / 8;
+  const int r = static_cast<int>(t & (kTileM - 1));
+  const int64_t tile = t / kTileM;
   if (kStash) {
-    for (int64_t c = tid >> 3; c < nb32; c += 4 * kQuantWarps) {
-      float2 q01, q23;
-      codes_of_word(sstash[c * 8 + part], q01, q23);
-      emit_split<kQ4>(aplane, t, c, nb32, part, q01, q23, sd16[c], sssum[c], scale);
+    // chunk g: k = 8g .. 8g + 7, block c = g / 4; within its half super-block
+    // (sb, half) the chunk sits at K offset kk = 8 * (g % 16)
+    const uint32_t row_off = static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128);
+    for (int64_t g = tid; g < nb32 * 4; g += 32 * kQuantWarps) {
+      const int64_t c = g >> 2;
+      const int kk = static_cast<int>(g & 15) * 8;
+      uint8_t *blk = aplane + as_block(tile, c >> 3, static_cast<int>((c >> 2) & 1), nsb, kQ4);
+      const uint32_t off = static_cast<uint32_t>(kk >> 6) * kSplitQuarter + row_off +
+                           ((((kk & 63) >> 3) ^ (r & 7)) << 4);
+      const float d16f = sd16[c];
+      uint4 hi, lo;
+      split_chunk(sstash4[g], d16f * scale, hi, lo);
+      *reinterpret_cast<uint4 *>(blk + off) = hi;
+      *reinterpret_cast<uint4 *>(blk + kSplitLo + off) = lo;
+      if (kQ4 && (g & 3) == 0) {
+        const float gv = d16f * sssum[c] * scale;  // exact to fp32
+        const __half ghi = __float2half_rn(gv);
+        const __half glo = __float2half_rn(gv - __half2float(ghi));
+        uint8_t *mblk = aplane + as_block(tile, c >> 3, 1, nsb, true) + kSplitMin;
+        *reinterpret_cast<uint32_t *>(mblk + min_off(r, 2 * static_cast<int>(c & 7))) =
+            static_cast<uint32_t>(__half_as_ushort(ghi)) | (static_cast<uint32_t>(__half_as_ushort(glo)) << 16);
+      }
     }
   } else {
     for (int64_t base = warp * 16; base < nb32; base += 16 * kQuantWarps) {
@@ -605,12 +624,12 @@ __global__ void __launch_bounds__(32 * kQuantWarps, kStash ? 5 : 4) split_prepas
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int64_t c = base + u * 4 + grp;
-        float d, d16f;
-        int q[4], ssum;
-        quant_codes8(v[u], d, d16f, q, ssum);
+        float d16f, q[4];
+        q8_lane(v[u], d16f, q);
+        const float ssum = kQ4 ? q8_ssum(q) : 0.f;
         if (c < nb32)
-          emit_split<kQ4>(aplane, t, c, nb32, part, make_float2(static_cast<float>(q[0]), static_cast<float>(q[1])),
-                          make_float2(static_cast<float>(q[2]), static_cast<float>(q[3])), d16f, ssum, scale);
+          emit_split<kQ4>(aplane, t, c, nb32, part, make_float2(q[0], q[1]), make_float2(q[2], q[3]), d16f,
+                          static_cast<int>(ssum), scale);
       }
     }
   }

@@ -3,7 +3,8 @@
 // Block (t, c) of 32 values, at byte (t*nb32 + c)*40 (the pad40 plane of
 // "26 · r21 — Coalesced block-linear A staging", §2.1):
 //   d = amax/127 (fp32, IEEE division), q_i = roundf(x_i / d) (half away
-//   from zero), stored d16 = fp16_rn(d), bytes [2,4) = 0, ssum = sum q_i.
+//   from zero), stored d16 = fp16_rn(d), bytes [2,4) = 0, ssum = sum q_i
+//   (q8.cuh holds the rule, shared with the GEMM's quantizing prepasses).
 //
 // HBM-bound: 128 B read and 40 B written per block.  Eight lanes share a
 // block, each loading one float4 and storing one 4-byte qs word; lane 0 of
@@ -11,40 +12,27 @@
 #include <cuda_fp16.h>
 
 #include "internal.h"
+#include "q8.cuh"
 
 namespace mmq {
 namespace {
 
-// One 32-value block handled by 8 lanes (one float4 each).
+// One 32-value block handled by 8 lanes (one float4 each), the rule of q8.cuh.
 __device__ __forceinline__ void quantize_block(float4 v, int64_t blk, bool valid, int part,
                                                uint8_t *__restrict__ Q) {
-  float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
-#pragma unroll
-  for (int m = 1; m < 8; m <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
-  const float d = amax / 127.0f;
-  int q[4] = {0, 0, 0, 0};
-  if (amax != 0.0f) {
-    const float xs[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int qi = static_cast<int>(roundf(xs[i] / d));
-      q[i] = max(-127, min(127, qi));
-    }
-  }
-  int ssum = q[0] + q[1] + q[2] + q[3];
-#pragma unroll
-  for (int m = 1; m < 8; m <<= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, m);
+  float d16f, q[4];
+  q8_lane(v, d16f, q);
+  const float ssum = q8_ssum(q);
   if (!valid) return;
   uint8_t *b = Q + blk * MMQ_Q8_BLOCK_BYTES;
-  const uint32_t word = (static_cast<uint32_t>(q[0]) & 0xFFu) |
-                        ((static_cast<uint32_t>(q[1]) & 0xFFu) << 8) |
-                        ((static_cast<uint32_t>(q[2]) & 0xFFu) << 16) |
-                        ((static_cast<uint32_t>(q[3]) & 0xFFu) << 24);
+  const uint32_t word = (static_cast<uint32_t>(static_cast<int>(q[0])) & 0xFFu) |
+                        ((static_cast<uint32_t>(static_cast<int>(q[1])) & 0xFFu) << 8) |
+                        ((static_cast<uint32_t>(static_cast<int>(q[2])) & 0xFFu) << 16) |
+                        (static_cast<uint32_t>(static_cast<int>(q[3])) << 24);
   reinterpret_cast<uint32_t *>(b + MMQ_Q8_QS_OFF)[part] = word;
   if (part == 0) {
-    const uint32_t dbits = amax != 0.0f ? __half_as_ushort(__float2half_rn(d)) : 0u;
-    *reinterpret_cast<uint32_t *>(b + MMQ_Q8_D_OFF) = dbits;  // d16 | zero pad
-    *reinterpret_cast<int32_t *>(b + MMQ_Q8_SSUM_OFF) = ssum;
+    *reinterpret_cast<uint32_t *>(b + MMQ_Q8_D_OFF) = __half_as_ushort(__float2half_rn(d16f));  // d16 | zero pad
+    *reinterpret_cast<int32_t *>(b + MMQ_Q8_SSUM_OFF) = static_cast<int>(ssum);
   }
 }
 
