@@ -91,7 +91,8 @@ typedef struct mmq_weights_s *mmq_weights_t;
 #define MMQ_ARM_AUTO 0     /* library choice: MMQ_ARM_SPLIT for q6_K with a one-plane
                               operand (every |sc| <= 64), and for q4_K when the split arm
                               runs 256-row weight tiles (problems with more 128 x 128
-                              output tiles than SMs); else MMQ_ARM_F16 */
+                              output tiles than SMs) or pieces of tiles (problems with at
+                              most half as many tiles as SMs); else MMQ_ARM_F16 */
 #define MMQ_ARM_F16 1      /* operands from the registered fp16 operand plane (bulk copies) */
 #define MMQ_ARM_RAW 2      /* packed weight bytes streamed and unpacked to fp16 in shared
                               memory inside the GEMM ("47 · r44 — W_exp stride mismatch
@@ -105,7 +106,10 @@ typedef struct mmq_weights_s *mmq_weights_t;
                               apply once per super-block: every product exact, fp32
                               summation (results within the GEMM tolerance, not
                               bit-identical to F16); whole tiles of 128 or 256 weight
-                              rows per CTA */
+                              rows per CTA, or -- with at most half as many 128 x 128
+                              tiles as SMs -- each tile's super-blocks cut into pieces
+                              over several CTAs whose partial sums are added in a fixed
+                              order (repeat calls bit-identical) */
 
 /*
  * mmq_quantize_act -- q8_0 quantization of activations.
@@ -208,7 +212,8 @@ int mmq_weights_info(mmq_weights_t h, int *type, int64_t *od, int64_t *id,
  * a multiple of 128 (nt_pad*id*2 bytes for MMQ_ARM_F16 and MMQ_ARM_RAW, plus
  * nt_pad*(id/32)*8 of per-block scales; nt_pad*id*4 of hi + lo images for
  * MMQ_ARM_SPLIT; about 1/16 more for q4_K's min images), and for a stream-K
- * launch of the fp16-plane arm one 64 KB partial tile per CTA -- stream-ordered from a
+ * launch of the fp16-plane arm one 64 KB partial tile per CTA (for the split
+ * arm's pieces one 64 KB partial per piece and a counter per tile) -- stream-ordered from a
  * library-private memory pool and frees it stream-ordered; while `stream` is
  * being captured into a CUDA graph the scratch becomes a graph memory node
  * (cudaMallocAsync), so the call can be captured and replayed.

@@ -247,7 +247,8 @@ static int gemm_impl(mmq_weights_t h, const void *Q, const float *X, int64_t nt,
   if (flags != MMQ_ARM_AUTO && flags != MMQ_ARM_F16 && flags != MMQ_ARM_RAW && flags != MMQ_ARM_SPLIT)
     return MMQ_ERR_UNSUPPORTED;
   if (flags == MMQ_ARM_RAW && (!h->rawplane || h->b0plane)) return MMQ_ERR_UNSUPPORTED;
-  // library choice: the split arm for one-plane q6_K, and for q4_K where it runs 256-row tiles;
+  // library choice: the split arm for one-plane q6_K, and for q4_K where it runs 256-row tiles
+  // or pieces of tiles;
   // else the fp16-plane arm (measured fastest on the q-proj and FFN workloads of each kind; a
   // two-plane q6_K operand doubles the split arm's tensor work but hides in the other's hand-off)
   const bool raw = flags == MMQ_ARM_RAW;

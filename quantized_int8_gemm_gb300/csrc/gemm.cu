@@ -53,6 +53,7 @@
 // and UMMAs, frees TMEM and returns.
 #include <cuda_fp16.h>
 
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 
@@ -540,9 +541,12 @@ template <bool kQ4, bool kStash>
 __global__ void __launch_bounds__(32 * kQuantWarps, kStash ? 5 : 4) split_prepass_f32_kernel(const float *__restrict__ X,
                                                                    int64_t nt, int64_t nb32,
                                                                    uint8_t *__restrict__ aplane,
-                                                                   float *__restrict__ invp) {
+                                                                   float *__restrict__ invp,
+                                                                   int *__restrict__ cnt, int ncnt) {
   extern __shared__ uint4 sstash4[];  // [nb32][4] 16-byte code chunks, then [nb32] d16, [nb32] ssum
   griddep_launch_dependents();
+  if (blockIdx.x == 0)  // the GEMM's per-tile piece counters start at zero
+    for (int i = threadIdx.x; i < ncnt; i += blockDim.x) cnt[i] = 0;
   const int64_t t = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int part = lane & 7, grp = lane >> 3;
@@ -639,8 +643,11 @@ __global__ void __launch_bounds__(32 * kQuantWarps, kStash ? 5 : 4) split_prepas
 template <bool kQ4>
 __global__ void __launch_bounds__(128) split_prepass_q_kernel(const uint8_t *__restrict__ Q, int64_t nt,
                                                               int64_t nb32, uint8_t *__restrict__ aplane,
-                                                              float *__restrict__ invp) {
+                                                              float *__restrict__ invp, int *__restrict__ cnt,
+                                                              int ncnt) {
   griddep_launch_dependents();
+  if (blockIdx.x == 0)  // the GEMM's per-tile piece counters start at zero
+    for (int i = threadIdx.x; i < ncnt; i += blockDim.x) cnt[i] = 0;
   const int64_t t = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const bool live = t < nt;  // rows nt .. nt_pad - 1 of the last tile: a zero activation row
@@ -1390,13 +1397,23 @@ __device__ __forceinline__ void fold_region(uint32_t ta, const float4 *s4, float
   }
 }
 
-template <bool kQ4, bool kWide, bool kB0>
+// kKP (few tiles, 128-row one-plane tiles only): the super-blocks of every
+// tile are cut into n_kp contiguous pieces, one CTA each.  A piece stores its
+// scaled partial sums of the token rows below nt to its 64 KB of `part`; the
+// last CTA of a tile to finish (a counter per tile, zeroed by the prepass)
+// adds the tile's pieces in piece order and stores Y, so the sum is the same
+// whichever CTA finishes last.  Activation K-blocks are copied only up to the
+// tile's last token row (rounded up to 8): rows beyond it feed output rows
+// that are never stored.
+template <bool kQ4, bool kWide, bool kB0, bool kKP = false>
 __global__ void __launch_bounds__(SplitShape::kThreads, 1)
     mmq_gemm_split_kernel(const uint8_t *__restrict__ aplane, const uint8_t *__restrict__ bplane,
                           const uint8_t *__restrict__ bscale, const float *__restrict__ invp, int64_t nt,
                           int64_t od, int64_t nb32, int n_tt, int n_ot, float *__restrict__ Y, WaitCtl wctl,
-                          const uint8_t *__restrict__ b0plane) {
+                          const uint8_t *__restrict__ b0plane, int n_kp, float *__restrict__ part,
+                          int *__restrict__ cnt) {
   static_assert(!kB0 || !kQ4, "the B0 plane is q6_K's");
+  static_assert(!kKP || (!kWide && !kB0), "pieces of 128-row one-plane tiles");
   using L = SplitSmem<kQ4, kWide, kB0>;
   using S = SplitShape;
   constexpr int STAGES = L::kStages, NR = L::kRegions, NW = L::kN / 128;
@@ -1411,6 +1428,12 @@ __global__ void __launch_bounds__(SplitShape::kThreads, 1)
   const int n_tiles = n_tt * n_og;
   // weight tile w of group og (the last group of an odd n_ot repeats its tile)
   auto wtile = [&](int og, int w) { return min(og * NW + w, n_ot - 1); };
+  // units of work: whole tiles, or (kKP) pieces (tile, k) of super-blocks
+  const int kp = kKP ? n_kp : 1;
+  const int n_units = n_tiles * kp;
+  auto unit_tile = [&](int u) { return kKP ? u / kp : u; };
+  auto unit_sb0 = [&](int u) -> int64_t { return kKP ? nsb * (u % kp) / kp : 0; };
+  auto unit_sb1 = [&](int u) -> int64_t { return kKP ? nsb * (u % kp + 1) / kp : nsb; };
 
   const uint32_t bar = base + L::kBar;
   auto full = [&](int s) { return bar + 8u * s; };
@@ -1472,9 +1495,16 @@ __global__ void __launch_bounds__(SplitShape::kThreads, 1)
     griddep_wait();  // the activation blocks come from the kernel before this one
     uint32_t ks = 0, ns = 0, issued = 0, s_issued = 0, m_issued = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      const int tile = unit_tile(u);
       const int tt = tile % n_tt, og = tile / n_tt;
-      for (int64_t sb = 0; sb < nsb && ok; ++sb, ++ns) {
+      // kKP: bytes of each activation K-block's rows that are copied (rows up
+      // to the tile's last token, rounded up to 8); otherwise all 128
+      const int64_t rows_left = nt - static_cast<int64_t>(tt) * kTileM;
+      const uint32_t arow =
+          kKP ? static_cast<uint32_t>(((rows_left < kTileM ? rows_left : kTileM) + 7) & ~7) * 128u
+              : static_cast<uint32_t>(kSplitLo);
+      for (int64_t sb = unit_sb0(u); sb < unit_sb1(u) && ok; ++sb, ++ns) {
         const int e = static_cast<int>(ns % SRING);
         ok = __all_sync(0xffffffffu, mbar_wait(sempty(e), ((ns / SRING) & 1) ^ 1, wctl));
         if (!ok) break;
@@ -1508,9 +1538,13 @@ __global__ void __launch_bounds__(SplitShape::kThreads, 1)
           const bool mins = kQ4 && !SH && qq == 3;
           const uint8_t *ablk = aplane + as_block(tt, sb, half, nsb, kQ4);
           if (lane == 0) {
-            mbar_arrive_expect_tx(full(s), kSplitQuarter + NW * L::kBK * (kB0 ? 2 : 1) +
-                                               (mins ? L::kMinA + L::kMinB : 0));
-            bulk_load(a_smem(s), ablk + kb * kSplitQuarter, kSplitQuarter, full(s));
+            mbar_arrive_expect_tx(full(s), 2 * arow + NW * L::kBK * (kB0 ? 2 : 1) + (mins ? L::kMinA + L::kMinB : 0));
+            if (kKP) {  // the hi and the lo K-block's first rows
+              bulk_load(a_smem(s), ablk + kb * kSplitQuarter, arow, full(s));
+              bulk_load(a_smem(s) + kSplitLo, ablk + kb * kSplitQuarter + kSplitLo, arow, full(s));
+            } else {
+              bulk_load(a_smem(s), ablk + kb * kSplitQuarter, kSplitQuarter, full(s));
+            }
             if (mins) bulk_load(a_smem(s) + kSplitQuarter, ablk + kSplitMin, kMinBytes, full(s));
           } else if (lane == 1) {
             for (int w = 0; w < NW; ++w) {
@@ -1571,8 +1605,8 @@ __global__ void __launch_bounds__(SplitShape::kThreads, 1)
       }
       __syncwarp();
     };
-    for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-      for (int64_t sb = 0; sb < nsb && ok; ++sb, ++nr) {
+    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      for (int64_t sb = unit_sb0(u); sb < unit_sb1(u) && ok; ++sb, ++nr) {
         const int r = static_cast<int>(nr % NR);
         if constexpr (SH) {
           while (ok && pmin + NR <= nr) issue_min(pmin++);  // the region's last min term goes first
@@ -1645,7 +1679,8 @@ __global__ void __launch_bounds__(SplitShape::kThreads, 1)
     uint32_t nr = 0, ns = 0;
     bool ok = true;
     griddep_wait();  // 2^-s comes from the kernel before this one
-    for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      const int tile = unit_tile(u);
       const int tt = tile % n_tt, og = tile / n_tt;
       const int64_t t = static_cast<int64_t>(tt) * kTileM + row;
       // this warp's columns: weight tile og*NW + chalf (kWide), else half chalf of tile og
@@ -1654,7 +1689,7 @@ __global__ void __launch_bounds__(SplitShape::kThreads, 1)
       float2 y[CW / 2];
 #pragma unroll
       for (int i = 0; i < CW / 2; ++i) y[i] = make_float2(0.f, 0.f);
-      for (int64_t sb = 0; sb < nsb && ok; ++sb, ++nr, ++ns) {
+      for (int64_t sb = unit_sb0(u); sb < unit_sb1(u) && ok; ++sb, ++nr, ++ns) {
         const int r = static_cast<int>(nr % NR), e = static_cast<int>(ns % SRING);
         ok = __all_sync(0xffffffffu, mbar_wait(rfull(r), (nr / NR) & 1, wctl));
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(sfull(e), (ns / SRING) & 1, wctl));
@@ -1687,6 +1722,53 @@ __global__ void __launch_bounds__(SplitShape::kThreads, 1)
         }
       }
       if (!ok) break;
+      if constexpr (kKP) {
+       if (kp > 1) {
+        __shared__ int s_last;  // whether this CTA finished its tile's last piece
+        // this piece's partial sums (times 2^-s_t, exact), then the tile's
+        // count; the last of its pieces adds them all in piece order.  Layout
+        // per (piece, tile): [column half][float4 i of the row's 64 columns][row],
+        // so a warp's 32 rows are 512 contiguous bytes
+        const int piece = u % kp;
+        auto at = [&](int pc) {
+          return reinterpret_cast<float4 *>(part) + ((static_cast<int64_t>(pc) * n_tiles + tile) * 2 + chalf) * 16 * kTileM + row;
+        };
+        const float inv = t < nt ? __ldg(invp + t) : 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) y[i] = __fmul2_rn(y[i], make_float2(inv, inv));
+        if (t < nt) {
+          float4 *dst = at(piece);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) __stcg(dst + i * kTileM, make_float4(y[2 * i].x, y[2 * i].y, y[2 * i + 1].x, y[2 * i + 1].y));
+        }
+        __threadfence();
+        epi_bar();
+        if (threadIdx.x == 0) s_last = atomicAdd(cnt + tile, 1) == kp - 1;
+        epi_bar();
+        if (s_last && t < nt) {
+          __threadfence();
+          float2 acc[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) acc[i] = make_float2(0.f, 0.f);
+          for (int pc = 0; pc < kp; ++pc) {
+            if (pc == piece) {  // this CTA's own piece, still in registers
+#pragma unroll
+              for (int i = 0; i < 32; ++i) acc[i] = __fadd2_rn(acc[i], y[i]);
+              continue;
+            }
+            const float4 *src = at(pc);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float4 v = __ldcg(src + i * kTileM);
+              acc[2 * i] = __fadd2_rn(acc[2 * i], make_float2(v.x, v.y));
+              acc[2 * i + 1] = __fadd2_rn(acc[2 * i + 1], make_float2(v.z, v.w));
+            }
+          }
+          store_y_row<0>(Y, t, od, o0, acc, 1.0f);
+        }
+        continue;
+       }
+      }
       if (t < nt && (!kWide || og * NW + chalf < n_ot)) {  // (a repeated last tile is not stored)
         const float inv = __ldg(invp + t);
         store_y_row<0>(Y, t, od, o0, y, inv);
@@ -1957,9 +2039,10 @@ namespace {
 // latency-bound.)
 struct SplitPlan {
   bool q4, wide;
-  int64_t n_tt, nt_pad, nsb;
+  int kp;  // pieces per tile (1: whole tiles)
+  int64_t n_tt, nt_pad, nsb, rows;  // rows: activation rows the prepass writes
   int n_ot, n_tiles, grid;
-  size_t inv_off, bytes;
+  size_t inv_off, part_off, cnt_off, bytes;
 };
 
 SplitPlan plan_split(const mmq_weights_s *h, int64_t nt) {
@@ -1982,8 +2065,29 @@ SplitPlan plan_split(const mmq_weights_s *h, int64_t nt) {
       p.grid = static_cast<int>(tiles < sms ? tiles : sms);
     }
   }
-  p.inv_off = (static_cast<size_t>(p.n_tt * p.nsb) * as_pair_bytes(p.q4) + 255) / 256 * 256;
-  p.bytes = p.inv_off + static_cast<size_t>(p.nt_pad) * 4;
+  p.kp = 1;
+  p.rows = p.nt_pad;
+  // Few 128-row tiles: pieces of super-blocks over the SMs, when the busiest
+  // CTA then does fewer super-blocks (tensor-bound at ~2600 clk each with the
+  // activation rows trimmed to the tokens) plus ~1500 clk of partial sums
+  const int64_t tiles128 = p.n_tt * p.n_ot;
+  if (!h->b0plane && p.nsb >= 2 && 2 * tiles128 <= sms) {
+    const int64_t kp = std::min<int64_t>(p.nsb, sms / tiles128);
+    const int64_t est = (p.nsb + kp - 1) / kp * 2600 + 1500;
+    if (est < best * p.nsb) {  // (best: the whole-tile plan's clk per super-block)
+      p.wide = false;
+      p.kp = static_cast<int>(kp);
+      p.n_tiles = static_cast<int>(tiles128);
+      p.grid = static_cast<int>(tiles128 * kp);
+      // the last tile is copied only up to its last token row, rounded up to 8
+      p.rows = (p.n_tt - 1) * kTileM + ((nt - (p.n_tt - 1) * kTileM + 7) & ~int64_t(7));
+    }
+  }
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  p.inv_off = up(static_cast<size_t>(p.n_tt * p.nsb) * as_pair_bytes(p.q4));
+  p.part_off = up(p.inv_off + static_cast<size_t>(p.nt_pad) * 4);
+  p.cnt_off = p.part_off + (p.kp > 1 ? up(static_cast<size_t>(p.kp) * p.n_tiles * kTileM * kTileN * 4) : 0);
+  p.bytes = p.cnt_off + (p.kp > 1 ? up(static_cast<size_t>(p.n_tiles) * 4) : 0);
   return p;
 }
 
@@ -1991,7 +2095,10 @@ SplitPlan plan_split(const mmq_weights_s *h, int64_t nt) {
 
 size_t gemm_split_scratch_bytes(const mmq_weights_s *h, int64_t nt) { return plan_split(h, nt).bytes; }
 
-bool gemm_split_wide(const mmq_weights_s *h, int64_t nt) { return plan_split(h, nt).wide; }
+bool gemm_split_wide(const mmq_weights_s *h, int64_t nt) {
+  const SplitPlan p = plan_split(h, nt);
+  return p.wide || p.kp > 1;
+}
 
 cudaError_t launch_gemm_split(const mmq_weights_s *h, const uint8_t *Q, const float *X, int64_t nt, float *Y,
                               void *scratch, DevStatus *st, unsigned epoch, uint64_t limit_ns,
@@ -2003,25 +2110,29 @@ cudaError_t launch_gemm_split(const mmq_weights_s *h, const uint8_t *Q, const fl
   uint8_t *base8 = static_cast<uint8_t *>(scratch);
   uint8_t *aplane = base8;
   float *invp = reinterpret_cast<float *>(base8 + p.inv_off);
+  float *part = p.kp > 1 ? reinterpret_cast<float *>(base8 + p.part_off) : nullptr;
+  int *cnt = p.kp > 1 ? reinterpret_cast<int *>(base8 + p.cnt_off) : nullptr;
+  const int ncnt = p.kp > 1 ? p.n_tiles : 0;
   const int dev = h->device;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   cudaError_t e = cudaSuccess;
-  // one CTA per row of the padded token tiles (padding rows: a zero activation row)
-  const unsigned pgrid = static_cast<unsigned>(nt_pad);
+  // one CTA per row of the padded token tiles (padding rows: a zero activation
+  // row), or, with pieces, up to the last token row the GEMM copies
+  const unsigned pgrid = static_cast<unsigned>(p.rows);
   if (X) {
     const size_t stash = static_cast<size_t>(nb32) * kSplitStashBytesPerBlock;
     const bool fits = stash <= static_cast<size_t>(kStashMaxBytes);
     if (q4) {
-      if (fits) split_prepass_f32_kernel<true, true><<<pgrid, 32 * kQuantWarps, stash, s>>>(X, nt, nb32, aplane, invp);
-      else split_prepass_f32_kernel<true, false><<<pgrid, 32 * kQuantWarps, 0, s>>>(X, nt, nb32, aplane, invp);
+      if (fits) split_prepass_f32_kernel<true, true><<<pgrid, 32 * kQuantWarps, stash, s>>>(X, nt, nb32, aplane, invp, cnt, ncnt);
+      else split_prepass_f32_kernel<true, false><<<pgrid, 32 * kQuantWarps, 0, s>>>(X, nt, nb32, aplane, invp, cnt, ncnt);
     } else {
-      if (fits) split_prepass_f32_kernel<false, true><<<pgrid, 32 * kQuantWarps, stash, s>>>(X, nt, nb32, aplane, invp);
-      else split_prepass_f32_kernel<false, false><<<pgrid, 32 * kQuantWarps, 0, s>>>(X, nt, nb32, aplane, invp);
+      if (fits) split_prepass_f32_kernel<false, true><<<pgrid, 32 * kQuantWarps, stash, s>>>(X, nt, nb32, aplane, invp, cnt, ncnt);
+      else split_prepass_f32_kernel<false, false><<<pgrid, 32 * kQuantWarps, 0, s>>>(X, nt, nb32, aplane, invp, cnt, ncnt);
     }
   } else if (q4) {
-    split_prepass_q_kernel<true><<<pgrid, 128, 0, s>>>(Q, nt, nb32, aplane, invp);
+    split_prepass_q_kernel<true><<<pgrid, 128, 0, s>>>(Q, nt, nb32, aplane, invp, cnt, ncnt);
   } else {
-    split_prepass_q_kernel<false><<<pgrid, 128, 0, s>>>(Q, nt, nb32, aplane, invp);
+    split_prepass_q_kernel<false><<<pgrid, 128, 0, s>>>(Q, nt, nb32, aplane, invp, cnt, ncnt);
   }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
@@ -2031,7 +2142,7 @@ cudaError_t launch_gemm_split(const mmq_weights_s *h, const uint8_t *Q, const fl
   const uint8_t *bs = bp + b_scale_region(n_ot, nsb, q4);
   const int grid = p.grid;
   auto go = [&](auto kern, int smem, int variant) -> cudaError_t {
-    static std::atomic<int> ready[6][64];  // per kernel variant: 0 unknown, 1 ready, 2 unusable
+    static std::atomic<int> ready[8][64];  // per kernel variant: 0 unknown, 1 ready, 2 unusable
     std::atomic<int> &rd = ready[variant][dev];
     int stt = rd.load();
     if (stt == 0) {
@@ -2055,9 +2166,12 @@ cudaError_t launch_gemm_split(const mmq_weights_s *h, const uint8_t *Q, const fl
     cfg.numAttrs = ev0 ? 0 : 1;
     return cudaLaunchKernelEx(&cfg, kern, static_cast<const uint8_t *>(aplane), bp, bs,
                               static_cast<const float *>(invp), nt, h->od, nb32, static_cast<int>(n_tt), n_ot, Y, w,
-                              static_cast<const uint8_t *>(h->b0plane));
+                              static_cast<const uint8_t *>(h->b0plane), p.kp, part, cnt);
   };
-  if (q4)
+  if (p.kp > 1)
+    e = q4 ? go(mmq_gemm_split_kernel<true, false, false, true>, SplitSmem<true, false>::kBytes, 6)
+           : go(mmq_gemm_split_kernel<false, false, false, true>, SplitSmem<false, false>::kBytes, 7);
+  else if (q4)
     e = wide ? go(mmq_gemm_split_kernel<true, true, false>, SplitSmem<true, true>::kBytes, 3)
              : go(mmq_gemm_split_kernel<true, false, false>, SplitSmem<true, false>::kBytes, 0);
   else if (h->b0plane)

@@ -695,3 +695,56 @@ def test_raw_arm_workloads_sampled_against_oracle(mmq, name):
     err, bound = _within_tol(Yn[ts, os_], y_ref)
     assert err <= bound, (err, bound)
     w.release()
+
+
+# --------------------------------------------------------------------------
+# few tiles (small nt): the split arm cuts each tile's super-blocks into pieces
+@pytest.mark.parametrize("name", ["q4_K", "q6_K"])
+@pytest.mark.parametrize("nt", [1, 16, 64, 100, 128, 129, 200, 256])
+def test_small_nt_pieces_against_oracle(mmq, name, nt):
+    """q-proj weights (3584 x 3584) at token counts whose 128-row tiles fill
+    at most half the SMs: every tile's super-blocks are shared out as pieces
+    over CTAs, the activation copies stop at the last token row, and the
+    last piece of a tile adds all pieces in order.  Full element-by-element
+    compare with the oracle, on the library's arm and the split arm; repeat
+    calls bit-identical (the order of the pieces' sum is fixed)."""
+    od = id_ = 3584
+    W = gen.weights(name, od, id_, seed=700 + nt)
+    X = gen.activations(nt, id_, seed=701 + nt, outlier_p=0.01, outlier_scale=20.0)
+    w = mmq.mmq_register_weights(name, torch.from_numpy(W).cuda(), od, id_)
+    Xd = torch.from_numpy(X).cuda()
+    Y_ref = oracle.gemm_mt(QT[name], W, od, id_, oracle.quantize_q8_0(X), nt)
+    for arm in (mmq.MMQ_ARM_AUTO, mmq.MMQ_ARM_SPLIT):
+        Y, used = mmq.mmq_gemm_f32(w, Xd, flags=arm, return_arm=True)
+        Y2 = mmq.mmq_gemm_f32(w, Xd, flags=arm)
+        torch.cuda.synchronize()
+        assert mmq.mmq_last_device_error() == 0
+        assert used == mmq.MMQ_ARM_SPLIT
+        assert torch.equal(Y, Y2)
+        err, bound = _within_tol(Y.cpu().numpy(), Y_ref)
+        assert err <= bound, (arm, err, bound)
+    Y16 = mmq.mmq_gemm_f32(w, Xd, flags=mmq.MMQ_ARM_F16)
+    assert float((Y - Y16).abs().max()) <= 1e-5 * float(Y16.abs().max())
+    w.release()
+
+
+@pytest.mark.parametrize("name,od,id_,nt", [("q6_K", 3584, 18944, 16), ("q4_K", 1000, 2048, 50),
+                                            ("q6_K", 130, 512, 7)])
+def test_small_nt_pieces_other_shapes(mmq, name, od, id_, nt):
+    """Pieces on the FFN-down shape (74 super-blocks per tile), a ragged od
+    (8 tiles, one super-block per piece) and a two-tile weight; from pad40
+    blocks and from fp32 X, against the oracle."""
+    W = gen.weights(name, od, id_, seed=710 + nt)
+    X = gen.activations(nt, id_, seed=711 + nt, outlier_p=0.01, outlier_scale=20.0)
+    w = mmq.mmq_register_weights(name, torch.from_numpy(W).cuda(), od, id_)
+    Xd = torch.from_numpy(X).cuda()
+    Q = mmq.mmq_quantize_act(Xd)
+    Yf = mmq.mmq_gemm_f32(w, Xd, flags=mmq.MMQ_ARM_SPLIT)
+    Yq = mmq.mmq_gemm(w, Q, nt, flags=mmq.MMQ_ARM_SPLIT)
+    torch.cuda.synchronize()
+    assert mmq.mmq_last_device_error() == 0
+    assert torch.equal(Yf, Yq)
+    Y_ref = oracle.gemm_mt(QT[name], W, od, id_, oracle.quantize_q8_0(X), nt)
+    err, bound = _within_tol(Yf.cpu().numpy(), Y_ref)
+    assert err <= bound, (err, bound)
+    w.release()
