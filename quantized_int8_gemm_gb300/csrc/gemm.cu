@@ -1397,10 +1397,13 @@ __device__ __forceinline__ void fold_region(uint32_t ta, const float4 *s4, float
   }
 }
 
-// kKP (few tiles, 128-row one-plane tiles only): the super-blocks of every
-// tile are cut into n_kp contiguous pieces, one CTA each.  A piece stores its
-// scaled partial sums of the token rows below nt to its 64 KB of `part`; the
-// last CTA of a tile to finish (a counter per tile, zeroed by the prepass)
+// kKP (one-plane tiles): tiles n_full .. n_tiles-1 -- all of them when the
+// tiles fill at most half the SMs, else those of the last, partly filled wave
+// -- have their super-blocks cut into n_kp contiguous pieces, one unit of
+// work each, after the n_full whole tiles; a CTA takes units blockIdx.x,
+// blockIdx.x + gridDim.x, ...  A piece stores its scaled partial sums of the
+// token rows below nt to its slot of `part` (64 KB per 128 columns); the last
+// CTA of a tile to finish (a counter per pieced tile, zeroed by the prepass)
 // adds the tile's pieces in piece order and stores Y, so the sum is the same
 // whichever CTA finishes last.  Activation K-blocks are copied only up to the
 // tile's last token row (rounded up to 8): rows beyond it feed output rows
@@ -1410,10 +1413,10 @@ __global__ void __launch_bounds__(SplitShape::kThreads, 1)
     mmq_gemm_split_kernel(const uint8_t *__restrict__ aplane, const uint8_t *__restrict__ bplane,
                           const uint8_t *__restrict__ bscale, const float *__restrict__ invp, int64_t nt,
                           int64_t od, int64_t nb32, int n_tt, int n_ot, float *__restrict__ Y, WaitCtl wctl,
-                          const uint8_t *__restrict__ b0plane, int n_kp, float *__restrict__ part,
+                          const uint8_t *__restrict__ b0plane, int n_kp, int n_full, float *__restrict__ part,
                           int *__restrict__ cnt) {
   static_assert(!kB0 || !kQ4, "the B0 plane is q6_K's");
-  static_assert(!kKP || (!kWide && !kB0), "pieces of 128-row one-plane tiles");
+  static_assert(!kKP || !kB0, "pieces of one-plane tiles");
   using L = SplitSmem<kQ4, kWide, kB0>;
   using S = SplitShape;
   constexpr int STAGES = L::kStages, NR = L::kRegions, NW = L::kN / 128;
@@ -1428,12 +1431,14 @@ __global__ void __launch_bounds__(SplitShape::kThreads, 1)
   const int n_tiles = n_tt * n_og;
   // weight tile w of group og (the last group of an odd n_ot repeats its tile)
   auto wtile = [&](int og, int w) { return min(og * NW + w, n_ot - 1); };
-  // units of work: whole tiles, or (kKP) pieces (tile, k) of super-blocks
+  // units of work: whole tiles, then (kKP) pieces (tile, k) of super-blocks
   const int kp = kKP ? n_kp : 1;
-  const int n_units = n_tiles * kp;
-  auto unit_tile = [&](int u) { return kKP ? u / kp : u; };
-  auto unit_sb0 = [&](int u) -> int64_t { return kKP ? nsb * (u % kp) / kp : 0; };
-  auto unit_sb1 = [&](int u) -> int64_t { return kKP ? nsb * (u % kp + 1) / kp : nsb; };
+  const int nfull = kKP ? n_full : n_tiles;
+  const int n_units = nfull + (n_tiles - nfull) * kp;
+  auto unit_tile = [&](int u) { return kKP && u >= nfull ? nfull + (u - nfull) / kp : u; };
+  auto unit_piece = [&](int u) { return kKP && u >= nfull ? (u - nfull) % kp : -1; };
+  auto unit_sb0 = [&](int u) -> int64_t { return kKP && u >= nfull ? nsb * unit_piece(u) / kp : 0; };
+  auto unit_sb1 = [&](int u) -> int64_t { return kKP && u >= nfull ? nsb * (unit_piece(u) + 1) / kp : nsb; };
 
   const uint32_t bar = base + L::kBar;
   auto full = [&](int s) { return bar + 8u * s; };
@@ -1723,48 +1728,46 @@ __global__ void __launch_bounds__(SplitShape::kThreads, 1)
       }
       if (!ok) break;
       if constexpr (kKP) {
-       if (kp > 1) {
+       if (u >= nfull) {
         __shared__ int s_last;  // whether this CTA finished its tile's last piece
         // this piece's partial sums (times 2^-s_t, exact), then the tile's
-        // count; the last of its pieces adds them all in piece order.  Layout
-        // per (piece, tile): [column half][float4 i of the row's 64 columns][row],
-        // so a warp's 32 rows are 512 contiguous bytes
-        const int piece = u % kp;
+        // count; the last of its pieces adds them all, in piece order, from
+        // `part`.  Layout per (piece, pieced tile): [column half][float4 i of
+        // the warp's CW columns][row], so a warp's 32 rows are 512 contiguous bytes
+        const int piece = unit_piece(u), pt = tile - nfull, n_pieced = n_tiles - nfull;
         auto at = [&](int pc) {
-          return reinterpret_cast<float4 *>(part) + ((static_cast<int64_t>(pc) * n_tiles + tile) * 2 + chalf) * 16 * kTileM + row;
+          return reinterpret_cast<float4 *>(part) +
+                 ((static_cast<int64_t>(pc) * n_pieced + pt) * 2 + chalf) * (CW / 4) * kTileM + row;
         };
-        const float inv = t < nt ? __ldg(invp + t) : 0.f;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) y[i] = __fmul2_rn(y[i], make_float2(inv, inv));
         if (t < nt) {
+          const float inv = __ldg(invp + t);
           float4 *dst = at(piece);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) __stcg(dst + i * kTileM, make_float4(y[2 * i].x, y[2 * i].y, y[2 * i + 1].x, y[2 * i + 1].y));
+          for (int i = 0; i < CW / 4; ++i) {
+            const float2 a = __fmul2_rn(y[2 * i], make_float2(inv, inv));
+            const float2 b = __fmul2_rn(y[2 * i + 1], make_float2(inv, inv));
+            __stcg(dst + i * kTileM, make_float4(a.x, a.y, b.x, b.y));
+          }
         }
         __threadfence();
         epi_bar();
-        if (threadIdx.x == 0) s_last = atomicAdd(cnt + tile, 1) == kp - 1;
+        if (threadIdx.x == 0) s_last = atomicAdd(cnt + pt, 1) == kp - 1;
         epi_bar();
-        if (s_last && t < nt) {
+        if (s_last && t < nt && (!kWide || og * NW + chalf < n_ot)) {
           __threadfence();
-          float2 acc[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) acc[i] = make_float2(0.f, 0.f);
+          for (int i = 0; i < CW / 2; ++i) y[i] = make_float2(0.f, 0.f);
           for (int pc = 0; pc < kp; ++pc) {
-            if (pc == piece) {  // this CTA's own piece, still in registers
-#pragma unroll
-              for (int i = 0; i < 32; ++i) acc[i] = __fadd2_rn(acc[i], y[i]);
-              continue;
-            }
             const float4 *src = at(pc);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
+            for (int i = 0; i < CW / 4; ++i) {
               const float4 v = __ldcg(src + i * kTileM);
-              acc[2 * i] = __fadd2_rn(acc[2 * i], make_float2(v.x, v.y));
-              acc[2 * i + 1] = __fadd2_rn(acc[2 * i + 1], make_float2(v.z, v.w));
+              y[2 * i] = __fadd2_rn(y[2 * i], make_float2(v.x, v.y));
+              y[2 * i + 1] = __fadd2_rn(y[2 * i + 1], make_float2(v.z, v.w));
             }
           }
-          store_y_row<0>(Y, t, od, o0, acc, 1.0f);
+          store_y_row<0>(Y, t, od, o0, y, 1.0f);
+          if constexpr (CW > 64) store_y_row<32>(Y, t, od, o0 + 64, y, 1.0f);
         }
         continue;
        }
@@ -2039,7 +2042,8 @@ namespace {
 // latency-bound.)
 struct SplitPlan {
   bool q4, wide;
-  int kp;  // pieces per tile (1: whole tiles)
+  int kp;      // pieces per pieced tile (1: whole tiles only)
+  int n_full;  // tiles done whole, before the pieced ones
   int64_t n_tt, nt_pad, nsb, rows;  // rows: activation rows the prepass writes
   int n_ot, n_tiles, grid;
   size_t inv_off, part_off, cnt_off, bytes;
@@ -2066,28 +2070,48 @@ SplitPlan plan_split(const mmq_weights_s *h, int64_t nt) {
     }
   }
   p.kp = 1;
+  p.n_full = p.n_tiles;
   p.rows = p.nt_pad;
-  // Few 128-row tiles: pieces of super-blocks over the SMs, when the busiest
-  // CTA then does fewer super-blocks (tensor-bound at ~2600 clk each with the
-  // activation rows trimmed to the tokens) plus ~1500 clk of partial sums
-  const int64_t tiles128 = p.n_tt * p.n_ot;
-  if (!h->b0plane && p.nsb >= 2 && 2 * tiles128 <= sms) {
-    const int64_t kp = std::min<int64_t>(p.nsb, sms / tiles128);
-    const int64_t est = (p.nsb + kp - 1) / kp * 2600 + 1500;
-    if (est < best * p.nsb) {  // (best: the whole-tile plan's clk per super-block)
-      p.wide = false;
-      p.kp = static_cast<int>(kp);
-      p.n_tiles = static_cast<int>(tiles128);
-      p.grid = static_cast<int>(tiles128 * kp);
-      // the last tile is copied only up to its last token row, rounded up to 8
-      p.rows = (p.n_tt - 1) * kTileM + ((nt - (p.n_tt - 1) * kTileM + 7) & ~int64_t(7));
+  if (!h->b0plane && p.nsb >= 2) {
+    // Few 128-row tiles: every tile's super-blocks in pieces over the SMs,
+    // when the busiest CTA then does fewer super-blocks (tensor-bound at ~2600
+    // clk each with the activation rows trimmed to the tokens) plus ~1500 clk
+    // of partial sums
+    const int64_t tiles128 = p.n_tt * p.n_ot;
+    if (2 * tiles128 <= sms) {
+      const int64_t kp = std::min<int64_t>(p.nsb, sms / tiles128);
+      const int64_t est = (p.nsb + kp - 1) / kp * 2600 + 1500;
+      if (est < best * p.nsb) {  // (best: the whole-tile plan's clk per super-block)
+        p.wide = false;
+        p.kp = static_cast<int>(kp);
+        p.n_tiles = static_cast<int>(tiles128);
+        p.n_full = 0;
+        p.grid = static_cast<int>(tiles128 * kp);
+        // the last tile is copied only up to its last token row, rounded up to 8
+        p.rows = (p.n_tt - 1) * kTileM + ((nt - (p.n_tt - 1) * kTileM + 7) & ~int64_t(7));
+      }
+    } else {
+      // Several waves of whole tiles whose last wave leaves SMs idle: the
+      // tiles of that wave in pieces over every CTA instead, when that saves
+      // more than ~3000 clk of partial sums on the busiest CTA.  Not for q4_K
+      // with 256-row tiles: that variant's epilogue (192 registers, the min
+      // term sharing the accumulator regions) spills with the piece code and
+      // measured 12 % slower on the FFN-up workload (476 against 424 us).
+      const int64_t grid = p.grid, waves = (p.n_tiles + grid - 1) / grid;
+      const int64_t rest = p.n_tiles - (waves - 1) * grid;
+      const int64_t kp = std::min<int64_t>(p.nsb, rest > 0 ? grid / rest : 0);
+      if (!(p.q4 && p.wide) && waves >= 2 && kp >= 2 && (p.nsb - (p.nsb + kp - 1) / kp) * (best / waves) > 3000) {
+        p.kp = static_cast<int>(kp);
+        p.n_full = static_cast<int>((waves - 1) * grid);
+      }
     }
   }
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
   p.inv_off = up(static_cast<size_t>(p.n_tt * p.nsb) * as_pair_bytes(p.q4));
   p.part_off = up(p.inv_off + static_cast<size_t>(p.nt_pad) * 4);
-  p.cnt_off = p.part_off + (p.kp > 1 ? up(static_cast<size_t>(p.kp) * p.n_tiles * kTileM * kTileN * 4) : 0);
-  p.bytes = p.cnt_off + (p.kp > 1 ? up(static_cast<size_t>(p.n_tiles) * 4) : 0);
+  const size_t pieced = static_cast<size_t>(p.n_tiles - p.n_full);
+  p.cnt_off = p.part_off + (p.kp > 1 ? up(p.kp * pieced * kTileM * kTileN * 4 * (p.wide ? 2 : 1)) : 0);
+  p.bytes = p.cnt_off + (p.kp > 1 ? up(pieced * 4) : 0);
   return p;
 }
 
@@ -2112,7 +2136,7 @@ cudaError_t launch_gemm_split(const mmq_weights_s *h, const uint8_t *Q, const fl
   float *invp = reinterpret_cast<float *>(base8 + p.inv_off);
   float *part = p.kp > 1 ? reinterpret_cast<float *>(base8 + p.part_off) : nullptr;
   int *cnt = p.kp > 1 ? reinterpret_cast<int *>(base8 + p.cnt_off) : nullptr;
-  const int ncnt = p.kp > 1 ? p.n_tiles : 0;
+  const int ncnt = p.kp > 1 ? p.n_tiles - p.n_full : 0;
   const int dev = h->device;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   cudaError_t e = cudaSuccess;
@@ -2142,7 +2166,7 @@ cudaError_t launch_gemm_split(const mmq_weights_s *h, const uint8_t *Q, const fl
   const uint8_t *bs = bp + b_scale_region(n_ot, nsb, q4);
   const int grid = p.grid;
   auto go = [&](auto kern, int smem, int variant) -> cudaError_t {
-    static std::atomic<int> ready[8][64];  // per kernel variant: 0 unknown, 1 ready, 2 unusable
+    static std::atomic<int> ready[10][64];  // per kernel variant: 0 unknown, 1 ready, 2 unusable
     std::atomic<int> &rd = ready[variant][dev];
     int stt = rd.load();
     if (stt == 0) {
@@ -2166,9 +2190,11 @@ cudaError_t launch_gemm_split(const mmq_weights_s *h, const uint8_t *Q, const fl
     cfg.numAttrs = ev0 ? 0 : 1;
     return cudaLaunchKernelEx(&cfg, kern, static_cast<const uint8_t *>(aplane), bp, bs,
                               static_cast<const float *>(invp), nt, h->od, nb32, static_cast<int>(n_tt), n_ot, Y, w,
-                              static_cast<const uint8_t *>(h->b0plane), p.kp, part, cnt);
+                              static_cast<const uint8_t *>(h->b0plane), p.kp, p.n_full, part, cnt);
   };
-  if (p.kp > 1)
+  if (p.kp > 1 && wide)  // (q6_K only: the plan keeps q4_K's 256-row tiles whole)
+    e = go(mmq_gemm_split_kernel<false, true, false, true>, SplitSmem<false, true>::kBytes, 9);
+  else if (p.kp > 1)
     e = q4 ? go(mmq_gemm_split_kernel<true, false, false, true>, SplitSmem<true, false>::kBytes, 6)
            : go(mmq_gemm_split_kernel<false, false, false, true>, SplitSmem<false, false>::kBytes, 7);
   else if (q4)

@@ -748,3 +748,32 @@ def test_small_nt_pieces_other_shapes(mmq, name, od, id_, nt):
     err, bound = _within_tol(Yf.cpu().numpy(), Y_ref)
     assert err <= bound, (err, bound)
     w.release()
+
+
+@pytest.mark.parametrize("name,od,id_,nt", [("q6_K", 2048, 3584, 2630), ("q6_K", 3584, 3584, 2048),
+                                            ("q4_K", 2048, 3584, 2630)])
+def test_last_wave_in_pieces(mmq, name, od, id_, nt):
+    """Several waves of 256-row q6_K tiles whose last wave would leave SMs idle
+    (168 and 224 tiles on the GPU's SMs): those tiles run as pieces over every
+    CTA after the whole tiles (q4_K's 256-row tiles stay whole: the same shape
+    as a control).  Sampled outputs against the oracle, tile edges included;
+    repeat calls bit-identical."""
+    W = gen.weights(name, od, id_, seed=720 + od)
+    X = gen.activations(nt, id_, seed=721 + od, outlier_p=0.01, outlier_scale=20.0)
+    w = mmq.mmq_register_weights(name, torch.from_numpy(W).cuda(), od, id_)
+    Xd = torch.from_numpy(X).cuda()
+    Y = mmq.mmq_gemm_f32(w, Xd, flags=mmq.MMQ_ARM_SPLIT)
+    Y2 = mmq.mmq_gemm_f32(w, Xd, flags=mmq.MMQ_ARM_SPLIT)
+    torch.cuda.synchronize()
+    assert mmq.mmq_last_device_error() == 0
+    assert torch.equal(Y, Y2)
+    Yn = Y.cpu().numpy()
+    assert np.isfinite(Yn).all()
+    ts, os_ = _sample_entries(nt, od, 3000, od + nt)
+    # the last rows of the output (the tiles of the last wave)
+    ts = np.concatenate([ts, np.full(64, nt - 1), np.arange(nt - 64, nt)])
+    os_ = np.concatenate([os_, np.arange(od - 64, od), np.full(64, od - 1)])
+    y_ref = oracle.gemm_entries(QT[name], W, od, id_, oracle.quantize_q8_0(X), nt, ts, os_)
+    err, bound = _within_tol(Yn[ts, os_], y_ref)
+    assert err <= bound, (err, bound)
+    w.release()
