@@ -800,6 +800,9 @@ def main(argv=None):
                     help="register with MMQ_REG_WEXP: the operand plane is built from the dense W_exp "
                          "plane (the workload is then named <workload>_wexp)")
     ap.add_argument("--no-also", action="store_true", help="skip the other q-proj workload")
+    ap.add_argument("--nt", type=int, default=None,
+                    help="run the workload's shape and generators at this many tokens (the name's _nt suffix "
+                         "follows)")
     ap.add_argument("--no-timings", action="store_true",
                     help="skip the separate quantize_act / gemm / fused timings")
     args = ap.parse_args(argv)
@@ -807,6 +810,11 @@ def main(argv=None):
         ap.error("--warmup must be >= 3")
     from synth import gen
     cfg = gen.config_by_name(args.workload)
+    if args.nt is not None:  # the workload's weights and generators at another token count
+        import dataclasses
+        if args.nt <= 0:
+            ap.error("--nt must be positive")
+        cfg = dataclasses.replace(cfg, nt=args.nt, name=re.sub(r"_nt\d+$", f"_nt{args.nt}", cfg.name))
     rank, world = _env_int("RANK", 0), _env_int("WORLD_SIZE", 1)
     if args.impl == "reference":
         run_reference(args, cfg, rank)

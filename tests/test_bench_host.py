@@ -43,3 +43,12 @@ def test_code_hash_ignores_comments(tmp_path):
     assert bench._code_sha1(str(a)) == bench._code_sha1(str(b))
     b.write_text('int f() { return 2; }\n const char *s = "//x";\n')
     assert bench._code_sha1(str(a)) != bench._code_sha1(str(b))
+
+
+def test_nt_override_renames_the_workload(monkeypatch):
+    """--nt keeps the workload's shape and generators and renames its _nt suffix."""
+    got = {}
+    monkeypatch.setattr(bench, "run_reference", lambda args, cfg, rank: got.setdefault("cfg", cfg))
+    bench.main(["--impl", "reference", "--workload", "q6_K_qproj_3584x3584_nt512", "--nt", "16"])
+    cfg = got["cfg"]
+    assert (cfg.name, cfg.nt, cfg.od, cfg.id, cfg.qtype) == ("q6_K_qproj_3584x3584_nt16", 16, 3584, 3584, "q6_K")
