@@ -680,6 +680,58 @@ def _e2e(args, wl, stream, world, dev, ops, d2h_bytes):
             "launch": "the E steps as one CUDA graph" if ge is not None else "eager"}
 
 
+def run_engines():
+    """One JSON line: the rates of the exact-integer-capable engines -- the
+    library's own probe loops (tcgen05 kind::f16 per SM, mma.sync s8 and f16)
+    and, as library references, torch._int_mm (int8) and torch fp16 matmul at
+    8192^3, best of 10 each."""
+    import torch
+
+    import quantized_int8_gemm_gb300 as mmq
+    from quantized_int8_gemm_gb300 import build as mbuild
+    mbuild.build()
+    torch.cuda.set_device(0)
+    rates = mmq.mmq_probe_engine_rates()
+    dev = torch.device("cuda")
+    props = torch.cuda.get_device_properties(dev)
+    n = 8192
+
+    def best_ms(fn):
+        fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(10):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return min(ts)
+
+    a8 = torch.randint(-127, 128, (n, n), dtype=torch.int8, device=dev)
+    b8 = torch.randint(-127, 128, (n, n), dtype=torch.int8, device=dev)
+    int_mm = 2 * n ** 3 / (best_ms(lambda: torch._int_mm(a8, b8)) * 1e-3) / 1e12
+    a16, b16 = a8.half(), b8.half()
+    f16 = 2 * n ** 3 / (best_ms(lambda: torch.matmul(a16, b16)) * 1e-3) / 1e12
+    clocks = _clock_snapshot()
+    out = {"engines": rates, "torch_int_mm_8192_tops": int_mm, "torch_fp16_matmul_8192_tflops": f16,
+           "sms": props.multi_processor_count, "gpu": props.name, "sm_clock_mhz_after": clocks}
+    m = rates["umma_f16_mac_per_clk_per_sm"]["N128"]
+    if clocks:
+        out["umma_f16_tflops_at_that_clock"] = 2 * m * props.multi_processor_count * clocks * 1e6 / 1e12
+    print(json.dumps(out), flush=True)
+
+
+def _clock_snapshot():
+    try:
+        r = subprocess.run(["nvidia-smi", "--query-gpu=clocks.sm", "--format=csv,noheader,nounits", "-i", "0"],
+                           capture_output=True, text=True, timeout=10)
+        return float(r.stdout.strip().splitlines()[0])
+    except (OSError, ValueError, IndexError, subprocess.SubprocessError):
+        return None
+
+
 # the other q-proj workload, timed beside the default one in the same run
 ALSO_WORKLOADS = {DEFAULT_WORKLOAD: ["q6_K_qproj_3584x3584_nt512"]}
 
@@ -800,6 +852,9 @@ def main(argv=None):
                     help="register with MMQ_REG_WEXP: the operand plane is built from the dense W_exp "
                          "plane (the workload is then named <workload>_wexp)")
     ap.add_argument("--no-also", action="store_true", help="skip the other q-proj workload")
+    ap.add_argument("--engines", action="store_true",
+                    help="print the tensor engines' rates (the library's probe, torch._int_mm and fp16 matmul) "
+                         "instead of a bench line")
     ap.add_argument("--nt", type=int, default=None,
                     help="run the workload's shape and generators at this many tokens (the name's _nt suffix "
                          "follows)")
@@ -816,6 +871,9 @@ def main(argv=None):
             ap.error("--nt must be positive")
         cfg = dataclasses.replace(cfg, nt=args.nt, name=re.sub(r"_nt\d+$", f"_nt{args.nt}", cfg.name))
     rank, world = _env_int("RANK", 0), _env_int("WORLD_SIZE", 1)
+    if args.engines:
+        run_engines()
+        return
     if args.impl == "reference":
         run_reference(args, cfg, rank)
     else:

@@ -317,6 +317,21 @@ void mmq_set_wait_timeout_ns(uint64_t ns);
  * mmq_last_device_error() -- MMQ_ERR_DEVICE_TIMEOUT when the bound works. */
 int mmq_selftest_wait_timeout(uint64_t timeout_ns, mmq_stream_t stream);
 
+/*
+ * mmq_probe_engine_rates -- measurement hook, not part of the method: the
+ * rates of the exact-integer-capable tensor engines on the current device,
+ * the numbers behind the choice of tcgen05 kind::f16 for the integer
+ * contraction and of the fp16/bf16 peak as the roofline's denominator (the
+ * log pages run int8 IMMA; sm_103a has no tcgen05 kind::i8).  Writes
+ *   out[0..2]  tcgen05.mma kind::f16, M = 128, K = 16, N = 64 / 128 / 256:
+ *              MACs per clock per SM (one issuing warp per SM, back to back)
+ *   out[3]     mma.sync m16n8k32 s8 -> s32 over the whole GPU, TOPS (2 ops per MAC)
+ *   out[4]     mma.sync m16n8k16 f16 -> f32 over the whole GPU, TFLOP/s
+ * Synchronizes `stream`; takes well under a second.  Errors: MMQ_ERR_ARG,
+ * MMQ_ERR_NO_DEVICE, MMQ_ERR_CUDA, MMQ_ERR_DEVICE_TIMEOUT.
+ */
+int mmq_probe_engine_rates(double *out, mmq_stream_t stream);
+
 /* Static text for a status code. */
 const char *mmq_strerror(int code);
 

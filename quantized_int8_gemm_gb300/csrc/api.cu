@@ -391,6 +391,17 @@ int mmq_last_device_error(void) {
   return w.status ? MMQ_ERR_DEVICE_TIMEOUT : MMQ_OK;
 }
 
+int mmq_probe_engine_rates(double *out, mmq_stream_t stream) {
+  if (!out) return MMQ_ERR_ARG;
+  int dev;
+  DeviceState *d;
+  if (int rc = device_state(&dev, &d)) return rc;
+  cudaError_t e = mmq::launch_engine_probes(d->words, next_epoch(), g_limit_ns.load(),
+                                            reinterpret_cast<cudaStream_t>(stream), out);
+  if (e != cudaSuccess) return cuda_rc(e);
+  return mmq_last_device_error();
+}
+
 int mmq_selftest_wait_timeout(uint64_t timeout_ns, mmq_stream_t stream) {
   int dev;
   DeviceState *d;

@@ -84,6 +84,9 @@ cudaError_t launch_gemm_split(const mmq_weights_s *h, const uint8_t *Q, const fl
 cudaError_t launch_wait_selftest(DevStatus *st, unsigned epoch, uint64_t limit_ns,
                                  cudaStream_t s);
 
+// Engine-rate microbenchmarks (probe.cu); out[0..4] as mmq_probe_engine_rates.
+cudaError_t launch_engine_probes(DevStatus *st, unsigned epoch, uint64_t limit_ns, cudaStream_t s, double *out);
+
 // Fixed scratch of mmq_gemm_noalloc (a static device array in gemm.cu).
 constexpr size_t kNoallocScratchBytes = size_t(16) << 20;
 cudaError_t noalloc_scratch(int dev, void **out);

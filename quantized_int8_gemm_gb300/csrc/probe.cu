@@ -1,0 +1,191 @@
+// probe.cu -- microbenchmarks of the GB300's exact-integer-capable engines,
+// the measurements behind the choice of tensor-core kind and of the roofline
+// peak (mmq_probe_engine_rates in mmq.h).  Not part of the GEMM.
+//
+//   umma_rate_kernel<N>  one CTA per SM issues back-to-back tcgen05.mma
+//                        kind::f16 (M = 128, N, K = 16) from one warp into one
+//                        TMEM accumulator, operands (zeros) in shared memory;
+//                        the issuing thread's clock64 over the loop and the
+//                        final commit gives clk per UMMA
+//   mma_sync_s8_kernel   warp-level mma.sync m16n8k32 s8 -> s32, eight
+//                        independent accumulators per warp
+//   mma_sync_f16_kernel  warp-level mma.sync m16n8k16 f16 -> f32, likewise
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace mmq {
+namespace {
+
+constexpr int kUmmaIters = 4096;
+
+template <int N>
+__global__ void __launch_bounds__(128, 1) umma_rate_kernel(WaitCtl wctl, long long *clk_per_cta) {
+  __shared__ __align__(1024) uint8_t ops[2 * 16384];  // A and B: one 128-row, 64-K K-block each
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t tslot;
+  for (int i = threadIdx.x; i < 2 * 16384 / 16; i += blockDim.x) reinterpret_cast<uint4 *>(ops)[i] = make_uint4(0, 0, 0, 0);
+  const uint32_t b = smem_addr(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);
+    fence_mbar_init();
+  }
+  if (threadIdx.x < 32) {
+    tmem_alloc(smem_addr(&tslot), N < 32 ? 32 : N);
+    tmem_relinquish();
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the zeroed operands, for the tensor core
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *reinterpret_cast<volatile uint32_t *>(&tslot);
+  if (threadIdx.x < 32) {
+    uint32_t elected;
+    asm volatile("{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}" : "=r"(elected));
+    constexpr uint32_t idesc = idesc_f16_f32(128, N);
+    const uint64_t ad = sdesc_kmajor_sw128(smem_addr(ops)), bd = sdesc_kmajor_sw128(smem_addr(ops + 16384));
+    long long t0 = 0;
+    if (elected) {
+      t0 = clock64();
+      for (int i = 0; i < kUmmaIters; ++i) umma_f16(tbase, ad + 2 * (i & 3), bd + 2 * (i & 3), idesc, i ? 1u : 0u);
+      umma_commit(b);
+    }
+    __syncwarp();
+    const bool ok = mbar_wait(b, 0, wctl, false);
+    if (elected) clk_per_cta[blockIdx.x] = ok ? clock64() - t0 : -1;
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    tc_fence_after();
+    tmem_dealloc(tbase, N < 32 ? 32 : N);
+  }
+}
+
+constexpr int kMmaIters = 4096;
+
+__global__ void __launch_bounds__(256) mma_sync_s8_kernel(int *out) {
+  uint32_t a[4], bb[2];
+  int c[8][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) a[i] = 0x01010101u * (threadIdx.x & 3);
+  bb[0] = 0x01020304u;
+  bb[1] = 0x02030405u;
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) c[j][i] = 0;
+  for (int it = 0; it < kMmaIters; ++it) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      asm volatile(
+          "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+          "{%0, %1, %2, %3};"
+          : "+r"(c[j][0]), "+r"(c[j][1]), "+r"(c[j][2]), "+r"(c[j][3])
+          : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(bb[0]), "r"(bb[1]));
+  }
+  int s = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) s += c[j][0] + c[j][1] + c[j][2] + c[j][3];
+  if (s == 0x7fffffff) out[0] = s;  // keep the loop
+}
+
+__global__ void __launch_bounds__(256) mma_sync_f16_kernel(float *out) {
+  uint32_t a[4], bb[2];
+  float c[8][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) a[i] = 0x3c003c00u;  // 1.0 fp16 pairs
+  bb[0] = bb[1] = 0x00000000u;
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) c[j][i] = 0.f;
+  for (int it = 0; it < kMmaIters; ++it) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      asm volatile(
+          "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+          "{%0, %1, %2, %3};"
+          : "+f"(c[j][0]), "+f"(c[j][1]), "+f"(c[j][2]), "+f"(c[j][3])
+          : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(bb[0]), "r"(bb[1]));
+  }
+  float s = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) s += c[j][0] + c[j][1] + c[j][2] + c[j][3];
+  if (s == 1234.5f) out[0] = s;  // keep the loop
+}
+
+template <typename F>
+cudaError_t time_ms(cudaStream_t s, F launch, float *ms) {
+  cudaEvent_t e0, e1;
+  cudaError_t e = cudaEventCreate(&e0);
+  if (e != cudaSuccess) return e;
+  if ((e = cudaEventCreate(&e1)) != cudaSuccess) {
+    cudaEventDestroy(e0);
+    return e;
+  }
+  launch();  // warm-up
+  e = cudaEventRecord(e0, s);
+  launch();
+  if (e == cudaSuccess) e = cudaEventRecord(e1, s);
+  if (e == cudaSuccess) e = cudaEventSynchronize(e1);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaEventElapsedTime(ms, e0, e1);
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  return e;
+}
+
+template <int N>
+cudaError_t umma_rate(int sms, WaitCtl w, long long *clk, cudaStream_t s, double *mac_per_clk) {
+  umma_rate_kernel<N><<<sms, 128, 0, s>>>(w, clk);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  long long *h = new long long[sms];
+  e = cudaMemcpy(h, clk, sizeof(long long) * sms, cudaMemcpyDeviceToHost);
+  double sum = 0;
+  int n = 0;
+  for (int i = 0; e == cudaSuccess && i < sms; ++i)
+    if (h[i] > 0) {
+      sum += static_cast<double>(h[i]);
+      ++n;
+    }
+  delete[] h;
+  if (e != cudaSuccess) return e;
+  *mac_per_clk = n ? 128.0 * N * 16 * kUmmaIters / (sum / n) : 0.0;
+  return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_engine_probes(DevStatus *st, unsigned epoch, uint64_t limit_ns, cudaStream_t s, double *out) {
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  WaitCtl w{&st->status, &st->abort_epoch, epoch, limit_ns};
+  long long *clk = nullptr;
+  if ((e = cudaMalloc(&clk, sizeof(long long) * sms)) != cudaSuccess) return e;
+  e = umma_rate<64>(sms, w, clk, s, &out[0]);
+  if (e == cudaSuccess) e = umma_rate<128>(sms, w, clk, s, &out[1]);
+  if (e == cudaSuccess) e = umma_rate<256>(sms, w, clk, s, &out[2]);
+  cudaFree(clk);
+  if (e != cudaSuccess) return e;
+  int *sink = nullptr;
+  if ((e = cudaMalloc(&sink, 16)) != cudaSuccess) return e;
+  const unsigned grid = static_cast<unsigned>(sms) * 4;
+  const double mmas = static_cast<double>(grid) * 8 /* warps */ * kMmaIters * 8;
+  float ms = 0.f;
+  e = time_ms(s, [&] { mma_sync_s8_kernel<<<grid, 256, 0, s>>>(sink); }, &ms);
+  if (e == cudaSuccess) out[3] = mmas * 2.0 * 16 * 8 * 32 / (ms * 1e-3) / 1e12;
+  if (e == cudaSuccess) e = time_ms(s, [&] { mma_sync_f16_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<float *>(sink)); }, &ms);
+  if (e == cudaSuccess) out[4] = mmas * 2.0 * 16 * 8 * 16 / (ms * 1e-3) / 1e12;
+  cudaFree(sink);
+  return e;
+}
+
+}  // namespace mmq

@@ -49,7 +49,7 @@ EXPORTS = [
     "mmq_weights_info", "mmq_gemm", "mmq_gemm_f32", "mmq_gemm_profiled", "mmq_gemm_f32_profiled",
     "mmq_gemm_noalloc", "mmq_debug_chunk_partials", "mmq_dequantize_weights",
     "mmq_last_device_error", "mmq_set_wait_timeout_ns",
-    "mmq_selftest_wait_timeout", "mmq_strerror",
+    "mmq_selftest_wait_timeout", "mmq_strerror", "mmq_probe_engine_rates",
 ]
 
 _lock = threading.Lock()
@@ -91,6 +91,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         L.mmq_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
         L.mmq_set_wait_timeout_ns.restype = None
         L.mmq_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
+        L.mmq_probe_engine_rates.argtypes = [vp, vp]
         L.mmq_strerror.argtypes = [i32]
         L.mmq_strerror.restype = ctypes.c_char_p
         for n in EXPORTS:
@@ -292,3 +293,15 @@ def mmq_selftest_wait_timeout(timeout_ns: int, stream=None) -> int:
 
 def mmq_strerror(code: int) -> str:
     return strerror(code)
+
+
+def mmq_probe_engine_rates(stream=None) -> dict:
+    """Rates of the tensor engines on the current device (a measurement hook):
+    tcgen05 kind::f16 MACs per clock per SM at N = 64, 128, 256, and the
+    whole-GPU mma.sync s8 TOPS and f16 TFLOP/s."""
+    out = (ctypes.c_double * 5)()
+    rc = load().mmq_probe_engine_rates(ctypes.cast(out, ctypes.c_void_p), _stream(stream))
+    if rc != MMQ_OK:
+        raise MMQError(rc, "mmq_probe_engine_rates")
+    return {"umma_f16_mac_per_clk_per_sm": {"N64": out[0], "N128": out[1], "N256": out[2]},
+            "mma_sync_s8_tops": out[3], "mma_sync_f16_tflops": out[4]}
