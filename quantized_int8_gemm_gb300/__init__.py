@@ -26,6 +26,7 @@ from .mmq import (  # noqa: F401
     mmq_debug_chunk_partials,
     mmq_gemm_profiled,
     mmq_last_device_error,
+    mmq_probe_engine_rates,
     mmq_quantize_act,
     mmq_register_weights,
     mmq_selftest_wait_timeout,
