@@ -22,12 +22,23 @@ namespace {
 
 constexpr int kUmmaIters = 4096;
 
+// Operands in dynamic shared memory, 1024-byte aligned: A = one 64-K K-block
+// of 128 rows (16 KB), B = one of N rows (N * 128 B, read whole by every
+// UMMA).  The launch asks for kUmmaSmem bytes so that one CTA runs per SM.
+template <int N>
+__host__ __device__ constexpr int umma_ops_bytes() { return 16384 + N * 128; }
+constexpr int kUmmaSmem = 120 * 1024;
+static_assert(umma_ops_bytes<256>() + 1024 <= kUmmaSmem, "operands fit the request");
+
 template <int N>
 __global__ void __launch_bounds__(128, 1) umma_rate_kernel(WaitCtl wctl, long long *clk_per_cta) {
-  __shared__ __align__(1024) uint8_t ops[2 * 16384];  // A and B: one 128-row, 64-K K-block each
+  extern __shared__ uint8_t dyn[];
   __shared__ __align__(8) uint64_t bar;
   __shared__ uint32_t tslot;
-  for (int i = threadIdx.x; i < 2 * 16384 / 16; i += blockDim.x) reinterpret_cast<uint4 *>(ops)[i] = make_uint4(0, 0, 0, 0);
+  const uint32_t raw = smem_addr(dyn);
+  uint8_t *ops = dyn + (((raw + 1023u) & ~1023u) - raw);
+  for (int i = threadIdx.x; i < umma_ops_bytes<N>() / 16; i += blockDim.x)
+    reinterpret_cast<uint4 *>(ops)[i] = make_uint4(0, 0, 0, 0);
   const uint32_t b = smem_addr(&bar);
   if (threadIdx.x == 0) {
     mbar_init(b, 1);
@@ -141,8 +152,10 @@ cudaError_t time_ms(cudaStream_t s, F launch, float *ms) {
 
 template <int N>
 cudaError_t umma_rate(int sms, WaitCtl w, long long *clk, cudaStream_t s, double *mac_per_clk) {
-  umma_rate_kernel<N><<<sms, 128, 0, s>>>(w, clk);
-  cudaError_t e = cudaStreamSynchronize(s);
+  cudaError_t e = cudaFuncSetAttribute(umma_rate_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize, kUmmaSmem);
+  if (e != cudaSuccess) return e;
+  umma_rate_kernel<N><<<sms, 128, kUmmaSmem, s>>>(w, clk);
+  e = cudaStreamSynchronize(s);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   long long *h = new long long[sms];
