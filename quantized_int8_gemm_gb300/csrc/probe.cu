@@ -109,7 +109,9 @@ __global__ void __launch_bounds__(256) mma_sync_f16_kernel(float *out) {
   float c[8][4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) a[i] = 0x3c003c00u;  // 1.0 fp16 pairs
-  bb[0] = bb[1] = 0x00000000u;
+  // nonzero B: a zero operand made the loop report more than the tensor peak
+  bb[0] = 0x3c003c00u;
+  bb[1] = 0x3c00bc00u;
 #pragma unroll
   for (int j = 0; j < 8; ++j)
 #pragma unroll

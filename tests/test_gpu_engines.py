@@ -18,6 +18,8 @@ def test_engine_rates():
     assert 3600 <= umma["N256"] <= 4200, umma
     assert 0 < umma["N64"] < umma["N128"], umma
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    # even at 2.1 GHz the whole GPU's fp16 UMMA rate is > 10x the int8 mma.sync rate measured here
-    assert r["mma_sync_s8_tops"] > 0 and 10 * r["mma_sync_s8_tops"] < 2 * umma["N128"] * sms * 1.0e9 / 1e12, r
-    assert r["mma_sync_f16_tflops"] > 0, r
+    # even at a 1.5 GHz SM clock the whole GPU's fp16 UMMA rate is > 10x the int8 mma.sync rate measured here
+    umma_tflops_at_1p5ghz = 2 * umma["N128"] * sms * 1.5e9 / 1e12
+    assert 0 < 10 * r["mma_sync_s8_tops"] < umma_tflops_at_1p5ghz, r
+    # the warp-level f16 MMA stays below the fp16 UMMA as well
+    assert 0 < r["mma_sync_f16_tflops"] < umma_tflops_at_1p5ghz * 2070 / 1500, r
