@@ -79,12 +79,11 @@ __global__ void __launch_bounds__(128, 1) umma_rate_kernel(WaitCtl wctl, long lo
 constexpr int kMmaIters = 4096;
 
 __global__ void __launch_bounds__(256) mma_sync_s8_kernel(int *out) {
-  uint32_t a[4], bb[2];
+  // operand registers that differ per thread (constant operands let the
+  // f16 loop report more than the tensor peak)
+  const uint32_t x = threadIdx.x;
+  const uint32_t a[4] = {x, x * 3u, x * 5u, x * 7u}, bb[2] = {x * 11u, x * 13u};
   int c[8][4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) a[i] = 0x01010101u * (threadIdx.x & 3);
-  bb[0] = 0x01020304u;
-  bb[1] = 0x02030405u;
 #pragma unroll
   for (int j = 0; j < 8; ++j)
 #pragma unroll
@@ -105,13 +104,9 @@ __global__ void __launch_bounds__(256) mma_sync_s8_kernel(int *out) {
 }
 
 __global__ void __launch_bounds__(256) mma_sync_f16_kernel(float *out) {
-  uint32_t a[4], bb[2];
+  const uint32_t x = threadIdx.x;  // per-thread operand registers, as above
+  const uint32_t a[4] = {x, x * 3u, x * 5u, x * 7u}, bb[2] = {x * 11u, x * 13u};
   float c[8][4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) a[i] = 0x3c003c00u;  // 1.0 fp16 pairs
-  // nonzero B: a zero operand made the loop report more than the tensor peak
-  bb[0] = 0x3c003c00u;
-  bb[1] = 0x3c00bc00u;
 #pragma unroll
   for (int j = 0; j < 8; ++j)
 #pragma unroll
