@@ -452,7 +452,8 @@ def _measure(args, wl, stream, world, dev, main=True):
     if mmq.mmq_last_device_error() != 0:
         raise RuntimeError("device wait expired during warm-up")
     arm_name = mmq.ARM_NAMES.get(arm, str(arm))
-    kernel_name = "mmq_gemm_split_kernel" if arm == mmq.MMQ_ARM_SPLIT else "mmq_gemm_kernel"
+    kernel_name = {mmq.MMQ_ARM_SPLIT: "mmq_gemm_split_kernel",
+                   mmq.MMQ_ARM_PAIR: "mmq_gemm_pair_kernel"}.get(arm, "mmq_gemm_kernel")
 
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(K)]

@@ -88,11 +88,14 @@ typedef struct mmq_weights_s *mmq_weights_t;
 #define MMQ_REG_RAW 0x2u   /* also keep the packed bytes, regrouped, for MMQ_ARM_RAW */
 
 /* ---- GEMM arms (flags of mmq_gemm select one; arm_used reports it) ----- */
-#define MMQ_ARM_AUTO 0     /* library choice: MMQ_ARM_SPLIT for q6_K with a one-plane
-                              operand (every |sc| <= 64), and for q4_K when the split arm
-                              runs 256-row weight tiles (problems with more 128 x 128
-                              output tiles than SMs) or pieces of tiles (problems with at
-                              most half as many tiles as SMs); else MMQ_ARM_F16 */
+#define MMQ_ARM_AUTO 0     /* library choice: MMQ_ARM_PAIR above 128 tokens for one-plane
+                              operands (q4_K, and q6_K with every |sc| <= 64), except
+                              q6_K problems whose 256-row split tiles fill two or more
+                              waves of SMs to 85 %; otherwise MMQ_ARM_SPLIT for one-plane
+                              q6_K, and for q4_K when the split arm runs 256-row weight
+                              tiles (problems with more 128 x 128 output tiles than SMs)
+                              or pieces of tiles (problems with at most half as many tiles
+                              as SMs); else MMQ_ARM_F16 */
 #define MMQ_ARM_F16 1      /* operands from the registered fp16 operand plane (bulk copies) */
 #define MMQ_ARM_RAW 2      /* packed weight bytes streamed and unpacked to fp16 in shared
                               memory inside the GEMM ("47 · r44 — W_exp stride mismatch
@@ -110,6 +113,14 @@ typedef struct mmq_weights_s *mmq_weights_t;
                               tiles as SMs -- each tile's super-blocks cut into pieces
                               over several CTAs whose partial sums are added in a fixed
                               order (repeat calls bit-identical) */
+#define MMQ_ARM_PAIR 4     /* MMQ_ARM_SPLIT's operands and arithmetic on pairs of SMs: 2-CTA
+                              clusters run cta_group::2 UMMAs of 256 weight rows x 128 (or
+                              112) tokens, each SM staging its own 128 weight rows and half
+                              of the token rows, so a 64-K stage of the operand ring holds a
+                              third less and takes two bulk copies; whole tiles; results
+                              within fp32 summation of MMQ_ARM_SPLIT's (the tensor core sums
+                              the transposed tile in its own order); handles whose operand
+                              is one plane (otherwise MMQ_ERR_UNSUPPORTED) */
 
 /*
  * mmq_quantize_act -- q8_0 quantization of activations.

@@ -7,6 +7,7 @@ from .mmq import (  # noqa: F401
     ARM_NAMES,
     MMQ_ARM_AUTO,
     MMQ_ARM_F16,
+    MMQ_ARM_PAIR,
     MMQ_ARM_RAW,
     MMQ_ARM_SPLIT,
     MMQ_OUT_F16,

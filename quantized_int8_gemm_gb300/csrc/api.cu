@@ -244,18 +244,21 @@ static int gemm_impl(mmq_weights_t h, const void *Q, const float *X, int64_t nt,
                      mmq_stream_t stream, uint32_t flags, int *arm_used, cudaEvent_t ev0,
                      cudaEvent_t ev1) {
   if (!h || nt < 0 || nt > kMaxTokens) return MMQ_ERR_ARG;
-  if (flags != MMQ_ARM_AUTO && flags != MMQ_ARM_F16 && flags != MMQ_ARM_RAW && flags != MMQ_ARM_SPLIT)
+  if (flags != MMQ_ARM_AUTO && flags != MMQ_ARM_F16 && flags != MMQ_ARM_RAW && flags != MMQ_ARM_SPLIT &&
+      flags != MMQ_ARM_PAIR)
     return MMQ_ERR_UNSUPPORTED;
   if (flags == MMQ_ARM_RAW && (!h->rawplane || h->b0plane)) return MMQ_ERR_UNSUPPORTED;
-  // library choice: the split arm for one-plane q6_K, and for q4_K where it runs 256-row tiles
-  // or pieces of tiles;
-  // else the fp16-plane arm (measured fastest on the q-proj and FFN workloads of each kind; a
+  if (flags == MMQ_ARM_PAIR && h->b0plane) return MMQ_ERR_UNSUPPORTED;
+  // library choice: the pair arm above 128 tokens (one-plane operands; not for q6_K whose
+  // 256-row split tiles fill two or more waves); else the split arm for one-plane q6_K, and
+  // for q4_K where it runs 256-row tiles or pieces of tiles; else the fp16-plane arm (a
   // two-plane q6_K operand doubles the split arm's tensor work but hides in the other's hand-off)
   const bool raw = flags == MMQ_ARM_RAW;
-  const bool split = flags == MMQ_ARM_SPLIT ||
+  const bool pair = flags == MMQ_ARM_PAIR || (flags == MMQ_ARM_AUTO && mmq::gemm_pair_preferred(h, nt));
+  const bool split = pair || flags == MMQ_ARM_SPLIT ||
                      (flags == MMQ_ARM_AUTO && ((h->type == MMQ_Q6_K && !h->b0plane) ||
                                                 (h->type == MMQ_Q4_K && mmq::gemm_split_wide(h, nt))));
-  if (arm_used) *arm_used = raw ? MMQ_ARM_RAW : split ? MMQ_ARM_SPLIT : MMQ_ARM_F16;
+  if (arm_used) *arm_used = raw ? MMQ_ARM_RAW : pair ? MMQ_ARM_PAIR : split ? MMQ_ARM_SPLIT : MMQ_ARM_F16;
   if (nt == 0) return MMQ_OK;
   const void *A = X ? static_cast<const void *>(X) : Q;
   if (!A || !Y) return MMQ_ERR_ARG;
@@ -272,7 +275,8 @@ static int gemm_impl(mmq_weights_t h, const void *Q, const float *X, int64_t nt,
   cudaError_t e = cudaStreamIsCapturing(s, &cap);
   if (e != cudaSuccess) return cuda_rc(e);
   const bool capturing = cap == cudaStreamCaptureStatusActive;
-  const size_t bytes = split ? mmq::gemm_split_scratch_bytes(h, nt) : mmq::gemm_scratch_bytes(h, nt, true, raw);
+  const size_t bytes =
+      split ? mmq::gemm_split_scratch_bytes(h, nt, pair) : mmq::gemm_scratch_bytes(h, nt, true, raw);
   void *scratch = nullptr;
   e = capturing ? cudaMallocAsync(&scratch, bytes, s)
                 : cudaMallocFromPoolAsync(&scratch, bytes, d->pool, s);
@@ -281,7 +285,7 @@ static int gemm_impl(mmq_weights_t h, const void *Q, const float *X, int64_t nt,
   const unsigned ev_flags = capturing ? cudaEventRecordExternal : cudaEventRecordDefault;
   if (split)
     e = mmq::launch_gemm_split(h, static_cast<const uint8_t *>(Q), X, nt, Y, scratch, d->words, next_epoch(),
-                               g_limit_ns.load(), s, ev0, ev1, ev_flags);
+                               g_limit_ns.load(), s, ev0, ev1, ev_flags, pair);
   else
     e = mmq::launch_gemm(h, static_cast<const uint8_t *>(Q), X, nt, Y, scratch, true, raw,
                          d->words, next_epoch(), g_limit_ns.load(), s, ev0, ev1, ev_flags);

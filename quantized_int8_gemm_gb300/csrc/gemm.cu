@@ -477,26 +477,31 @@ __device__ __forceinline__ void split_pair(float2 q, float da_s, uint32_t &hi, u
 
 // Lane `part` of block c's eight: its 4 values into the hi and lo images, and
 // (part 0, q4_K) the block's min-term slots.
-template <bool kQ4>
+// kPair: the pair arm's block layout (tiling.h) with token tiles of tp rows,
+// else the split arm's.
+template <bool kQ4, bool kPair>
 __device__ __forceinline__ void emit_split(uint8_t *__restrict__ aplane, int64_t t, int64_t c, int64_t nb32,
                                            int part, float2 q01, float2 q23, float d16f, int ssum,
-                                           float scale) {
+                                           float scale, int tp) {
   const int64_t nsb = nb32 / 8;
-  const int r = static_cast<int>(t & (kTileM - 1));
-  uint8_t *blk = aplane + as_block(t / kTileM, c >> 3, static_cast<int>((c >> 2) & 1), nsb, kQ4);
-  const uint32_t off = split_off(r, static_cast<int>(c & 3) * 32 + 4 * part);
+  const int64_t tile = kPair ? t / tp : t / kTileM;
+  const int r = static_cast<int>(kPair ? t % tp : t & (kTileM - 1)), h = tp / 2;
+  const int half = static_cast<int>((c >> 2) & 1), k = static_cast<int>(c & 3) * 32 + 4 * part;
+  uint8_t *blk = aplane + (kPair ? pair_block(tile, c >> 3, half, nsb, kQ4, h) : as_block(tile, c >> 3, half, nsb, kQ4));
+  const uint32_t off = kPair ? pair_off(r, k, kQ4, half, h) : split_off(r, k);
   const float da_s = d16f * scale;
   uint32_t hi0, lo0, hi1, lo1;
   split_pair(q01, da_s, hi0, lo0);
   split_pair(q23, da_s, hi1, lo1);
   *reinterpret_cast<uint2 *>(blk + off) = make_uint2(hi0, hi1);
-  *reinterpret_cast<uint2 *>(blk + kSplitLo + off) = make_uint2(lo0, lo1);
+  *reinterpret_cast<uint2 *>(blk + (kPair ? pair_kb_bytes(h) : kSplitLo) + off) = make_uint2(lo0, lo1);
   if (kQ4 && part == 0) {
     const float g = d16f * static_cast<float>(ssum) * scale;  // exact to fp32
     const __half hi = __float2half_rn(g);
     const __half lo = __float2half_rn(g - __half2float(hi));
-    uint8_t *mblk = aplane + as_block(t / kTileM, c >> 3, 1, nsb, true) + kSplitMin;
-    *reinterpret_cast<uint32_t *>(mblk + min_off(r, 2 * static_cast<int>(c & 7))) =
+    uint8_t *mblk = aplane + (kPair ? pair_block(tile, c >> 3, 1, nsb, true, h) : as_block(tile, c >> 3, 1, nsb, true));
+    const int j = 2 * static_cast<int>(c & 7);
+    *reinterpret_cast<uint32_t *>(mblk + (kPair ? pair_min_off(r, j, h) : kSplitMin + min_off(r, j))) =
         static_cast<uint32_t>(__half_as_ushort(hi)) | (static_cast<uint32_t>(__half_as_ushort(lo)) << 16);
   }
 }
@@ -537,12 +542,13 @@ __device__ __forceinline__ void split_chunk(uint4 codes, float da_s, uint4 &hi, 
 // chunk's hi and lo words, one 16-byte store each, and (q4_K, first chunk of
 // a block) the block's min-term slots.  Without kStash (tokens too long for
 // shared memory) pass two quantizes X again, per block as in pass one.
-template <bool kQ4, bool kStash>
+// kPair: the pair arm's block layout, token tiles of tp rows.
+template <bool kQ4, bool kStash, bool kPair = false>
 __global__ void __launch_bounds__(32 * kQuantWarps, kStash ? 5 : 4) split_prepass_f32_kernel(const float *__restrict__ X,
                                                                    int64_t nt, int64_t nb32,
                                                                    uint8_t *__restrict__ aplane,
                                                                    float *__restrict__ invp,
-                                                                   int *__restrict__ cnt, int ncnt) {
+                                                                   int *__restrict__ cnt, int ncnt, int tp) {
   extern __shared__ uint4 sstash4[];  // [nb32][4] 16-byte code chunks, then [nb32] d16, [nb32] ssum
   griddep_launch_dependents();
   if (blockIdx.x == 0)  // the GEMM's per-tile piece counters start at zero
@@ -591,8 +597,8 @@ __global__ void __launch_bounds__(32 * kQuantWarps, kStash ? 5 : 4) split_prepas
   const float scale = __uint_as_float(static_cast<uint32_t>(127 + s) << 23);
   if (tid == 0) invp[t] = __uint_as_float(static_cast<uint32_t>(127 - s) << 23);
   const int64_t nsb = nb32 / 8;
-  const int r = static_cast<int>(t & (kTileM - 1));
-  const int64_t tile = t / kTileM;
+  const int r = static_cast<int>(kPair ? t % tp : t & (kTileM - 1)), h = tp / 2;
+  const int64_t tile = kPair ? t / tp : t / kTileM;
   if (kStash) {
     // chunk g: k = 8g .. 8g + 7, block c = g / 4; within its half super-block
     // (sb, half) the chunk sits at K offset kk = 8 * (g % 16)
@@ -600,20 +606,23 @@ __global__ void __launch_bounds__(32 * kQuantWarps, kStash ? 5 : 4) split_prepas
     for (int64_t g = tid; g < nb32 * 4; g += 32 * kQuantWarps) {
       const int64_t c = g >> 2;
       const int kk = static_cast<int>(g & 15) * 8;
-      uint8_t *blk = aplane + as_block(tile, c >> 3, static_cast<int>((c >> 2) & 1), nsb, kQ4);
-      const uint32_t off = static_cast<uint32_t>(kk >> 6) * kSplitQuarter + row_off +
-                           ((((kk & 63) >> 3) ^ (r & 7)) << 4);
+      const int half = static_cast<int>((c >> 2) & 1);
+      uint8_t *blk = aplane + (kPair ? pair_block(tile, c >> 3, half, nsb, kQ4, h) : as_block(tile, c >> 3, half, nsb, kQ4));
+      const uint32_t off = kPair ? pair_off(r, kk, kQ4, half, h)
+                                 : static_cast<uint32_t>(kk >> 6) * kSplitQuarter + row_off +
+                                       ((((kk & 63) >> 3) ^ (r & 7)) << 4);
       const float d16f = sd16[c];
       uint4 hi, lo;
       split_chunk(sstash4[g], d16f * scale, hi, lo);
       *reinterpret_cast<uint4 *>(blk + off) = hi;
-      *reinterpret_cast<uint4 *>(blk + kSplitLo + off) = lo;
+      *reinterpret_cast<uint4 *>(blk + (kPair ? pair_kb_bytes(h) : kSplitLo) + off) = lo;
       if (kQ4 && (g & 3) == 0) {
         const float gv = d16f * sssum[c] * scale;  // exact to fp32
         const __half ghi = __float2half_rn(gv);
         const __half glo = __float2half_rn(gv - __half2float(ghi));
-        uint8_t *mblk = aplane + as_block(tile, c >> 3, 1, nsb, true) + kSplitMin;
-        *reinterpret_cast<uint32_t *>(mblk + min_off(r, 2 * static_cast<int>(c & 7))) =
+        uint8_t *mblk = aplane + (kPair ? pair_block(tile, c >> 3, 1, nsb, true, h) : as_block(tile, c >> 3, 1, nsb, true));
+        const int j = 2 * static_cast<int>(c & 7);
+        *reinterpret_cast<uint32_t *>(mblk + (kPair ? pair_min_off(r, j, h) : kSplitMin + min_off(r, j))) =
             static_cast<uint32_t>(__half_as_ushort(ghi)) | (static_cast<uint32_t>(__half_as_ushort(glo)) << 16);
       }
     }
@@ -632,19 +641,20 @@ __global__ void __launch_bounds__(32 * kQuantWarps, kStash ? 5 : 4) split_prepas
         q8_lane(v[u], d16f, q);
         const float ssum = kQ4 ? q8_ssum(q) : 0.f;
         if (c < nb32)
-          emit_split<kQ4>(aplane, t, c, nb32, part, make_float2(q[0], q[1]), make_float2(q[2], q[3]), d16f,
-                          static_cast<int>(ssum), scale);
+          emit_split<kQ4, kPair>(aplane, t, c, nb32, part, make_float2(q[0], q[1]), make_float2(q[2], q[3]), d16f,
+                                 static_cast<int>(ssum), scale, tp);
       }
     }
   }
 }
 
-// From pad40 q8_0 blocks: one CTA of 128 threads per token.
-template <bool kQ4>
+// From pad40 q8_0 blocks: one CTA of 128 threads per token.  kPair: the pair
+// arm's block layout.
+template <bool kQ4, bool kPair = false>
 __global__ void __launch_bounds__(128) split_prepass_q_kernel(const uint8_t *__restrict__ Q, int64_t nt,
                                                               int64_t nb32, uint8_t *__restrict__ aplane,
                                                               float *__restrict__ invp, int *__restrict__ cnt,
-                                                              int ncnt) {
+                                                              int ncnt, int tp) {
   griddep_launch_dependents();
   if (blockIdx.x == 0)  // the GEMM's per-tile piece counters start at zero
     for (int i = threadIdx.x; i < ncnt; i += blockDim.x) cnt[i] = 0;
@@ -675,7 +685,7 @@ __global__ void __launch_bounds__(128) split_prepass_q_kernel(const uint8_t *__r
     const uint32_t q4b = live ? *reinterpret_cast<const uint32_t *>(b + 4 + 4 * part) : 0u;
     float2 q01, q23;
     codes_of_word(q4b, q01, q23);
-    emit_split<kQ4>(aplane, t, c, nb32, part, q01, q23, d16f, ssum, scale);
+    emit_split<kQ4, kPair>(aplane, t, c, nb32, part, q01, q23, d16f, ssum, scale, tp);
   }
 }
 
@@ -1788,6 +1798,317 @@ __global__ void __launch_bounds__(SplitShape::kThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------- the pair arm's GEMM
+// The split arm's operands and arithmetic on pairs of SMs.  A 2-CTA cluster
+// computes output tiles of 256 weight rows x 128 tokens with cta_group::2
+// UMMAs of M = 256, N = 128: the weights are the A operand (each CTA stages
+// its own weight tile's 128 rows) and the hi and lo activation images the B
+// operand (each CTA stages half of the tile's tp = 128 or 112 token rows, from
+// the pair layout of tiling.h).  A 64-K stage takes two bulk copies per CTA,
+// its weight K-block and its activation rows (hi and lo side by side in the
+// pair layout), so six stages are in flight: measured, three or four copies
+// per 64-K stage fall behind the tensor pipe while two keep pace with it, and
+// three 128-K stages leave the ring waiting on the copies' round trip.  Per
+// output the
+// exact products and the epilogue's fp32 operations are those of the 128-row
+// split kernel, with the tile transposed -- TMEM lane = weight row, column =
+// token, so the scales d and dmin are one value per thread; the tensor core's
+// summation order inside a super-block may differ.
+//
+// Roles (both CTAs): warps 0-7 epilogue of the CTA's own 128 weight rows,
+// warp 8 producer (its own stage halves and scale blocks).  Warp 9: in the
+// even CTA the UMMA issuer; in the odd CTA a relay that, once a stage of its
+// own has landed, arrives on the even CTA's barrier for that stage, which so
+// waits for both halves.  The issuer's commits arrive on both CTAs' barriers
+// (stage free, accumulator ready); both epilogues arrive on the even CTA's
+// accumulator-free barrier.  The q4_K min term: per super-block one K = 16
+// pair UMMA of the weight min images (A) against the activation min images
+// (B), into a region of its own, issued with the super-block's last stage:
+// the activation min image comes in that stage's activation copy (it follows
+// the lo K-block in the pair layout), the weight one into a two-entry ring
+// that the same stage fills (a commit covers every earlier UMMA, so an entry
+// is free again two super-blocks later).
+struct PairShape {
+  static constexpr int kThreads = 384;
+  static constexpr int kRegsLaunch = 168;
+  static constexpr int kRegsEpi = 208;
+  static constexpr int kRegsCtl = 88;
+  static_assert(256 * kRegsEpi + (kThreads - 256) * kRegsCtl == kThreads * kRegsLaunch,
+                "the register split must add up to what the launch holds");
+};
+template <bool kQ4>
+struct PairSmem {
+  static constexpr int kW = kTileN * 64 * 2;                  // weight K-block: 128 rows x 64 K, 16384
+  static constexpr int kAB = 2 * pair_kb_bytes(64) + (kQ4 ? 64 * 32 : 0);  // up to 64 token rows: hi, lo, min
+  static constexpr int kStage = kW + (kAB + 1023) / 1024 * 1024;
+  static constexpr int kStages = 6;
+  static constexpr int kMR = kQ4 ? 2 : 0;                     // weight min-image ring (q4_K)
+  static constexpr int kMinRing = kStages * kStage;
+  static constexpr int kScale = scale_block_bytes(kQ4);
+  static constexpr int kScaleRing = kMinRing + kMR * kMinBytes;
+  static constexpr int kRegions = kQ4 ? 2 : 4;  // accumulators of 128 columns (q4_K: then as many min regions)
+  static constexpr int kBar = kScaleRing + SRING * kScale;
+  // full, empty per stage; rfull, rempty per region; sfull, sempty per scale entry; done
+  static constexpr int kNumBars = 2 * kStages + 2 * kRegions + 2 * SRING + 1;
+  static constexpr int kSlot = kBar + kNumBars * 8;
+  static constexpr int kBytes = kSlot + 16 + 1024;
+  static_assert(kStage % 1024 == 0 && kMinBytes % 1024 == 0, "stage buffers keep 1 KB alignment");
+  static_assert(kBytes <= 227 * 1024, "shared memory budget");
+  static_assert(kRegions * 128 * (kQ4 ? 2 : 1) <= TMEM_COLS, "TMEM columns");
+};
+
+template <bool kQ4>
+__global__ void __launch_bounds__(PairShape::kThreads, 1)
+    mmq_gemm_pair_kernel(const uint8_t *__restrict__ aplane, const uint8_t *__restrict__ bplane,
+                         const uint8_t *__restrict__ bscale, const float *__restrict__ invp, int64_t nt,
+                         int64_t od, int64_t nb32, int n_tt, int n_ot, float *__restrict__ Y, WaitCtl wctl,
+                         int tp) {
+  using L = PairSmem<kQ4>;
+  constexpr int STAGES = L::kStages, NR = L::kRegions;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t *smem = smem_raw + (base - raw);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();  // 0: issues the UMMAs; 1: its peer
+  const int pair = static_cast<int>(blockIdx.x >> 1), n_pairs = static_cast<int>(gridDim.x >> 1);
+  const int64_t nsb = nb32 / 8;
+  const int h = tp / 2;             // token rows each CTA stages (a multiple of 8, at most 64)
+  const int n_wp = (n_ot + 1) / 2;  // pairs of weight tiles
+  const int n_units = n_tt * n_wp;  // token tiles fastest
+  // this CTA's weight tile of pair wp (an odd n_ot's last pair repeats its tile, not stored)
+  auto wtile = [&](int wp) { return min(2 * wp + static_cast<int>(rank), n_ot - 1); };
+
+  const uint32_t bar = base + L::kBar;
+  auto full = [&](int s) { return bar + 8u * s; };
+  auto empty = [&](int s) { return bar + 8u * (STAGES + s); };
+  auto rfull = [&](int r) { return bar + 8u * (2 * STAGES + r); };
+  auto rempty = [&](int r) { return bar + 8u * (2 * STAGES + NR + r); };
+  auto sfull = [&](int e) { return bar + 8u * (2 * STAGES + 2 * NR + e); };
+  auto sempty = [&](int e) { return bar + 8u * (2 * STAGES + 2 * NR + SRING + e); };
+  const uint32_t done = bar + 8u * (L::kNumBars - 1);
+  auto w_smem = [&](int s) { return base + s * L::kStage; };
+  auto a_smem = [&](int s) { return base + s * L::kStage + L::kW; };
+  auto m_smem = [&](int m) { return base + L::kMinRing + m * kMinBytes; };
+  auto s_smem = [&](int e) { return base + L::kScaleRing + e * L::kScale; };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full(s), rank == 0 ? 2 : 1);  // the even CTA's: its own copies and the peer's relay
+      mbar_init(empty(s), 1);
+    }
+    for (int r = 0; r < NR; ++r) {
+      mbar_init(rfull(r), 1);
+      mbar_init(rempty(r), 2 * EPI_WARPS);  // (the even CTA's is the one used: both epilogues)
+    }
+    for (int e = 0; e < SRING; ++e) {
+      mbar_init(sfull(e), 1);
+      mbar_init(sempty(e), EPI_WARPS);
+    }
+    mbar_init(done, 1);
+    fence_mbar_init();
+  }
+  if (warp == ISSUER_WARP) {
+    tmem_alloc_pair(base + L::kSlot, TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync();  // both CTAs' barriers are initialised before either arrives on the other's
+  tc_fence_after();
+  const uint32_t tbase = *reinterpret_cast<volatile uint32_t *>(smem + L::kSlot);
+  if (warp >= PRODUCER_WARP) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(PairShape::kRegsCtl));
+    if (warp == PRODUCER_WARP) {
+      // ------------------------------------------------------------ producer
+      griddep_wait();  // the activation blocks come from the kernel before this one
+      uint32_t ks = 0, ns = 0, issued = 0, s_issued = 0;
+      bool ok = true;
+      for (int u = pair; u < n_units && ok; u += n_pairs) {
+        const int tt = u % n_tt, w = wtile(u / n_tt);
+        for (int64_t sb = 0; sb < nsb && ok; ++sb, ++ns) {
+          const int e = static_cast<int>(ns % SRING);
+          ok = __all_sync(0xffffffffu, mbar_wait(sempty(e), ((ns / SRING) & 1) ^ 1, wctl));
+          if (!ok) break;
+          for (int qq = 0; qq < 4; ++qq, ++ks) {  // 64-K quarters of the super-block
+            const int s = static_cast<int>(ks % STAGES);
+            ok = __all_sync(0xffffffffu, mbar_wait(empty(s), ((ks / STAGES) & 1) ^ 1, wctl));
+            if (!ok) break;
+            if (lane == 0) {
+              const int half = qq >> 1, kb = qq & 1;
+              const bool mins = kQ4 && qq == 3;
+              // this CTA's rows of the hi and the lo K-block (and, last quarter, the min image after them)
+              const uint32_t ab = 2 * pair_kb_bytes(h) + (mins ? h * 32 : 0);
+              mbar_arrive_expect_tx(full(s), L::kW + ab + (mins ? kMinBytes : 0));
+              bulk_load(w_smem(s), bplane + b_block(w, sb, half, nsb, kQ4) + kb * L::kW, L::kW, full(s));
+              bulk_load(a_smem(s),
+                        aplane + pair_block(tt, sb, half, nsb, kQ4, h) + rank * pair_rank_bytes(kQ4, half, h) +
+                            kb * 2 * pair_kb_bytes(h),
+                        ab, full(s));
+              if (mins)
+                bulk_load(m_smem(static_cast<int>(ns % (kQ4 ? L::kMR : 1))),
+                          bplane + b_block(w, sb, 1, nsb, kQ4) + kBMin, kMinBytes, full(s));
+            }
+            __syncwarp();
+            issued = ks + 1;
+            if (qq == 0) {  // the super-block's scales, after its first stage's operands
+              if (lane == 1) {
+                mbar_arrive_expect_tx(sfull(e), L::kScale);
+                bulk_load(s_smem(e), bscale + b_scale_block(w, sb, nsb, kQ4), L::kScale, sfull(e));
+              }
+              __syncwarp();
+              s_issued = ns + 1;
+            }
+          }
+        }
+      }
+      if (!ok) {  // drain this CTA's copies still in flight
+        for (uint32_t k = issued > STAGES ? issued - STAGES : 0; k < issued; ++k)
+          mbar_wait(full(k % STAGES), (k / STAGES) & 1, wctl, false);
+        for (uint32_t k = s_issued > SRING ? s_issued - SRING : 0; k < s_issued; ++k)
+          mbar_wait(sfull(k % SRING), (k / SRING) & 1, wctl, false);
+      }
+    } else if (warp == ISSUER_WARP && rank == 1) {
+      // ------------------------------------------------------------ relay (odd CTA)
+      uint32_t ks = 0;
+      bool ok = true;
+      for (int u = pair; u < n_units && ok; u += n_pairs) {
+        for (int64_t q = 0; q < 4 * nsb && ok; ++q, ++ks) {
+          const int s = static_cast<int>(ks % STAGES);
+          ok = __all_sync(0xffffffffu, mbar_wait(full(s), (ks / STAGES) & 1, wctl));
+          if (ok && lane == 0) mbar_arrive_cluster(mapa_shared(full(s), 0));
+          __syncwarp();
+        }
+      }
+      mbar_wait(done, 0, wctl, false);  // the even CTA's last UMMA has read this CTA's stages
+    } else if (warp == ISSUER_WARP) {
+      // ------------------------------------------------------------ UMMA issuer (even CTA)
+      uint32_t elected;
+      asm volatile("{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+                   : "=r"(elected));
+      const uint32_t idesc = idesc_f16_f32(256, tp);
+      constexpr uint64_t kStageDesc = L::kStage >> 4;
+      const uint64_t w0 = sdesc_kmajor_sw128(w_smem(0)), h0 = sdesc_kmajor_sw128(a_smem(0));
+      const uint64_t l0 = sdesc_kmajor_sw128(a_smem(0) + pair_kb_bytes(h));
+      const uint64_t am0 = sdesc_kmajor_sw32(a_smem(0) + 2 * pair_kb_bytes(h));
+      const uint64_t wm0 = sdesc_kmajor_sw32(m_smem(0));
+      uint32_t ks = 0, nr = 0;
+      bool ok = true;
+      for (int u = pair; u < n_units && ok; u += n_pairs) {
+        for (int64_t sb = 0; sb < nsb && ok; ++sb, ++nr) {
+          const int r = static_cast<int>(nr % NR);
+          ok = __all_sync(0xffffffffu, mbar_wait(rempty(r), ((nr / NR) & 1) ^ 1, wctl));
+          if (!ok) break;
+          const uint32_t dacc = tbase + r * 128, dmin = tbase + (NR + r) * 128;
+          for (int qq = 0; qq < 4 && ok; ++qq, ++ks) {
+            const int s = static_cast<int>(ks % STAGES);
+            ok = __all_sync(0xffffffffu, mbar_wait(full(s), (ks / STAGES) & 1, wctl));
+            if (!ok) break;
+            tc_fence_after();
+            if (elected) {
+              const uint64_t so = s * kStageDesc;
+#pragma unroll
+              for (int lc = 0; lc < 2; ++lc) {  // 32-K chunks: 64 B into the swizzled rows
+                const uint64_t off = so + lc * (64 >> 4);
+                umma_pair_f16(dacc, w0 + off, h0 + off, idesc, (qq | lc) ? 1u : 0u);
+                umma_pair_f16(dacc, w0 + off + 2, h0 + off + 2, idesc, 1u);
+                umma_pair_f16(dacc, w0 + off, l0 + off, idesc, 1u);
+                umma_pair_f16(dacc, w0 + off + 2, l0 + off + 2, idesc, 1u);
+              }
+              if (kQ4 && qq == 3)
+                umma_pair_f16(dmin, wm0 + static_cast<uint64_t>(nr % 2) * (kMinBytes >> 4), am0 + so, idesc, 0u);
+              umma_pair_commit(empty(s));
+              if (qq == 3) umma_pair_commit(rfull(r));
+            }
+            __syncwarp();
+          }
+        }
+      }
+      if (elected) umma_pair_commit(done);
+      __syncwarp();
+      mbar_wait(done, 0, wctl, false);
+    }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(PairShape::kRegsEpi));
+    // ------------------------------------------------------------ epilogue
+    // warp w: TMEM lanes (weight rows) 32*(w%4).., columns 64*(w/4) .. +63 (those below tp are tokens)
+    const int quad = warp & 3, chalf = warp >> 2;
+    const int row = quad * 32 + lane;
+    const uint32_t taddr = tbase + (static_cast<uint32_t>(quad * 32) << 16) + chalf * 64;
+    uint32_t nr = 0, ns = 0;
+    bool ok = true;
+    griddep_wait();  // 2^-s comes from the kernel before this one
+    for (int u = pair; u < n_units && ok; u += n_pairs) {
+      const int tt = u % n_tt, wp = u / n_tt, w = wtile(wp);
+      float2 y[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) y[i] = make_float2(0.f, 0.f);
+      for (int64_t sb = 0; sb < nsb && ok; ++sb, ++nr, ++ns) {
+        const int r = static_cast<int>(nr % NR), e = static_cast<int>(ns % SRING);
+        ok = __all_sync(0xffffffffu, mbar_wait(rfull(r), (nr / NR) & 1, wctl));
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(sfull(e), (ns / SRING) & 1, wctl));
+        if (!ok) break;
+        tc_fence_after();
+        const float *sc = reinterpret_cast<const float *>(smem + (s_smem(e) - base));
+        const float d = sc[row];
+        const float2 d2 = make_float2(d, d);
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+          uint32_t t0[32];
+          tmem_ld_32x32b_x32(taddr + r * 128 + g * 32, t0);
+          tmem_wait_ld(t0);
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            y[g * 16 + i] = __ffma2_rn(d2, make_float2(__uint_as_float(t0[2 * i]), __uint_as_float(t0[2 * i + 1])),
+                                       y[g * 16 + i]);
+        }
+        if constexpr (kQ4) {
+          const float nm = -sc[kScaleBytes / 4 + row];  // -dmin of this row
+          const float2 m2 = make_float2(nm, nm);
+#pragma unroll
+          for (int g = 0; g < 2; ++g) {
+            uint32_t t0[32];
+            tmem_ld_32x32b_x32(taddr + (NR + r) * 128 + g * 32, t0);
+            tmem_wait_ld(t0);
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              y[g * 16 + i] = __ffma2_rn(m2, make_float2(__uint_as_float(t0[2 * i]), __uint_as_float(t0[2 * i + 1])),
+                                         y[g * 16 + i]);
+          }
+        }
+        // the regions go back to the issuer, the scale entry to the producer
+        tc_fence_before();
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive_cluster(mapa_shared(rempty(r), 0));
+          mbar_arrive(sempty(e));
+        }
+      }
+      if (!ok) break;
+      const int64_t o = static_cast<int64_t>(w) * kTileN + row;
+      if (2 * wp + static_cast<int>(rank) < n_ot && o < od) {
+        // columns chalf*64 + c below tp are tokens tt*tp + chalf*64 + c
+        const int64_t t0 = static_cast<int64_t>(tt) * tp + chalf * 64;
+        const int64_t tend = min(nt, static_cast<int64_t>(tt) * tp + tp);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int64_t t = t0 + 2 * i;
+          if (t < tend) Y[t * od + o] = __fmul_rn(y[i].x, __ldg(invp + t));
+          if (t + 1 < tend) Y[(t + 1) * od + o] = __fmul_rn(y[i].y, __ldg(invp + t + 1));
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  cluster_sync();  // neither CTA leaves while the other may still use its barriers, stages or TMEM
+  if (warp == ISSUER_WARP) {
+    tc_fence_after();
+    tmem_dealloc_pair(tbase, TMEM_COLS);
+  }
+}
+
 // One CTA that waits on a barrier nothing arrives at: checks that a bounded
 // wait returns and reports instead of hanging.
 __global__ void wait_selftest_kernel(WaitCtl wctl) {
@@ -2044,12 +2365,47 @@ struct SplitPlan {
   bool q4, wide;
   int kp;      // pieces per pieced tile (1: whole tiles only)
   int n_full;  // tiles done whole, before the pieced ones
+  int tp;      // tokens per tile (the pair arm: 128 or 112; else 128)
   int64_t n_tt, nt_pad, nsb, rows;  // rows: activation rows the prepass writes
   int n_ot, n_tiles, grid;
   size_t inv_off, part_off, cnt_off, bytes;
 };
 
-SplitPlan plan_split(const mmq_weights_s *h, int64_t nt) {
+// How many SM pairs the device holds at once for the pair kernel (one CTA per
+// SM; how many pairs a device offers depends on how its SMs group), asked once
+// per device; -1 if the kernel is unusable (its register count is not the
+// one its register split was planned for).
+template <bool kQ4>
+int pair_capacity(int dev) {
+  static std::atomic<int> cached[64];  // 0 unknown
+  int pairs = cached[dev].load();
+  if (pairs != 0) return pairs;
+  auto kern = mmq_gemm_pair_kernel<kQ4>;
+  constexpr int smem = PairSmem<kQ4>::kBytes;
+  cudaFuncAttributes fa;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+      cudaFuncGetAttributes(&fa, kern) != cudaSuccess || fa.numRegs != PairShape::kRegsLaunch) {
+    pairs = -1;
+  } else {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * static_cast<unsigned>(num_sms(dev) / 2));
+    cfg.blockDim = dim3(PairShape::kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    pairs = cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n > 0 ? n : -1;
+  }
+  cached[dev].store(pairs);
+  return pairs;
+}
+
+SplitPlan plan_split(const mmq_weights_s *h, int64_t nt, bool pair) {
   SplitPlan p{};
   p.q4 = h->type == MMQ_Q4_K;
   p.n_tt = (nt + kTileM - 1) / kTileM;
@@ -2072,7 +2428,30 @@ SplitPlan plan_split(const mmq_weights_s *h, int64_t nt) {
   p.kp = 1;
   p.n_full = p.n_tiles;
   p.rows = p.nt_pad;
-  if (!h->b0plane && p.nsb >= 2) {
+  p.tp = kTileM;
+  if (pair) {
+    // the pair arm: whole tiles of 256 weight rows x tp tokens, one SM pair
+    // each; tp = 112 when it leaves fewer SM pairs idle in the busiest wave
+    // (the q-proj shapes: 70 tiles over 140 SMs instead of 56 over 112)
+    const int cap = p.q4 ? pair_capacity<true>(h->device) : pair_capacity<false>(h->device);
+    const int64_t pairs = cap > 0 ? cap : 1, n_wp = (p.n_ot + 1) / 2;
+    int64_t best_est = -1;
+    for (int tp : {128, 112}) {
+      const int64_t units = (nt + tp - 1) / tp * n_wp;
+      const int64_t est = (units + pairs - 1) / pairs * tp;
+      if (best_est < 0 || est < best_est) {
+        best_est = est;
+        p.tp = tp;
+      }
+    }
+    p.wide = false;
+    p.n_tt = (nt + p.tp - 1) / p.tp;
+    p.nt_pad = p.n_tt * p.tp;
+    p.rows = p.nt_pad;
+    p.n_tiles = static_cast<int>(p.n_tt * n_wp);
+    p.n_full = p.n_tiles;
+    p.grid = static_cast<int>(2 * std::min<int64_t>(p.n_tiles, pairs));
+  } else if (!h->b0plane && p.nsb >= 2) {
     // Few 128-row tiles: every tile's super-blocks in pieces over the SMs,
     // when the busiest CTA then does fewer super-blocks (tensor-bound at ~2600
     // clk each with the activation rows trimmed to the tokens) plus ~1500 clk
@@ -2107,7 +2486,8 @@ SplitPlan plan_split(const mmq_weights_s *h, int64_t nt) {
     }
   }
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
-  p.inv_off = up(static_cast<size_t>(p.n_tt * p.nsb) * as_pair_bytes(p.q4));
+  const size_t per_sb = pair ? pair_sb_bytes(p.q4, p.tp / 2) : as_pair_bytes(p.q4);
+  p.inv_off = up(static_cast<size_t>(p.n_tt * p.nsb) * per_sb);
   p.part_off = up(p.inv_off + static_cast<size_t>(p.nt_pad) * 4);
   const size_t pieced = static_cast<size_t>(p.n_tiles - p.n_full);
   p.cnt_off = p.part_off + (p.kp > 1 ? up(p.kp * pieced * kTileM * kTileN * 4 * (p.wide ? 2 : 1)) : 0);
@@ -2117,17 +2497,88 @@ SplitPlan plan_split(const mmq_weights_s *h, int64_t nt) {
 
 }  // namespace
 
-size_t gemm_split_scratch_bytes(const mmq_weights_s *h, int64_t nt) { return plan_split(h, nt).bytes; }
+size_t gemm_split_scratch_bytes(const mmq_weights_s *h, int64_t nt, bool pair) {
+  return plan_split(h, nt, pair).bytes;
+}
 
 bool gemm_split_wide(const mmq_weights_s *h, int64_t nt) {
-  const SplitPlan p = plan_split(h, nt);
+  const SplitPlan p = plan_split(h, nt, false);
   return p.wide || p.kp > 1;
 }
 
+// The library's choice of the pair arm (measured on the GB300, fused calls on
+// the 3584 x 3584 weights at 16 .. 2048 tokens and the two FFN workloads):
+// faster than every other arm above 128 tokens for both weight types (the
+// one near-tie, within 1.5 %, at 768 tokens, where a second wave of tiles is
+// mostly empty), slower than the split arm's pieces up to 128 tokens; for
+// q6_K the split arm's 256-row tiles stay ahead (by 4 % on the FFN-down
+// workload) when they fill at least two waves to 85 % or more.
+bool gemm_pair_preferred(const mmq_weights_s *h, int64_t nt) {
+  if (h->b0plane || nt <= kTileM) return false;
+  const bool q4 = h->type == MMQ_Q4_K;
+  if ((q4 ? pair_capacity<true>(h->device) : pair_capacity<false>(h->device)) < 0) return false;
+  if (!q4) {
+    const SplitPlan p = plan_split(h, nt, false);
+    if (p.wide) {
+      const int64_t sms = num_sms(h->device), waves = (p.n_tiles + sms - 1) / sms;
+      if (waves >= 2 && 100 * static_cast<int64_t>(p.n_tiles) >= 85 * waves * sms) return false;
+    }
+  }
+  return true;
+}
+
+namespace {
+
+// The split and pair arms' activation prepass: from fp32 X (the token's codes
+// kept in shared memory when they fit) or from pad40 blocks Q.
+template <bool kQ4, bool kPair>
+void split_prepass(const uint8_t *Q, const float *X, int64_t nt, int64_t nb32, uint8_t *aplane, float *invp, int *cnt,
+                   int ncnt, unsigned pgrid, int tp, cudaStream_t s) {
+  if (X) {
+    const size_t stash = static_cast<size_t>(nb32) * kSplitStashBytesPerBlock;
+    if (stash <= static_cast<size_t>(kStashMaxBytes))
+      split_prepass_f32_kernel<kQ4, true, kPair><<<pgrid, 32 * kQuantWarps, stash, s>>>(X, nt, nb32, aplane, invp,
+                                                                                         cnt, ncnt, tp);
+    else
+      split_prepass_f32_kernel<kQ4, false, kPair><<<pgrid, 32 * kQuantWarps, 0, s>>>(X, nt, nb32, aplane, invp,
+                                                                                      cnt, ncnt, tp);
+  } else {
+    split_prepass_q_kernel<kQ4, kPair><<<pgrid, 128, 0, s>>>(Q, nt, nb32, aplane, invp, cnt, ncnt, tp);
+  }
+}
+
+// The pair arm's kernel: launched as 2-CTA clusters, `grid` CTAs (pairs of
+// CTAs, at most as many pairs as the device holds at once).
+template <bool kQ4>
+cudaError_t launch_pair(int dev, int grid, cudaStream_t s, bool pdl, const uint8_t *aplane, const uint8_t *bp,
+                        const uint8_t *bs, const float *invp, int64_t nt, int64_t od, int64_t nb32, int n_tt,
+                        int n_ot, float *Y, WaitCtl w, int tp) {
+  if (pair_capacity<kQ4>(dev) < 0) return cudaErrorInvalidKernelImage;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(PairShape::kThreads);
+  cfg.dynamicSmemBytes = PairSmem<kQ4>::kBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, mmq_gemm_pair_kernel<kQ4>, aplane, bp, bs, invp, nt, od, nb32, n_tt, n_ot, Y, w,
+                            tp);
+}
+
+}  // namespace
+
 cudaError_t launch_gemm_split(const mmq_weights_s *h, const uint8_t *Q, const float *X, int64_t nt, float *Y,
                               void *scratch, DevStatus *st, unsigned epoch, uint64_t limit_ns,
-                              cudaStream_t s, cudaEvent_t ev0, cudaEvent_t ev1, unsigned ev_flags) {
-  const SplitPlan p = plan_split(h, nt);
+                              cudaStream_t s, cudaEvent_t ev0, cudaEvent_t ev1, unsigned ev_flags, bool pair) {
+  if (pair && h->b0plane) return cudaErrorInvalidValue;
+  const SplitPlan p = plan_split(h, nt, pair);
   const bool q4 = p.q4, wide = p.wide;
   const int64_t n_tt = p.n_tt, nt_pad = p.nt_pad, nsb = p.nsb, nb32 = h->nb32;
   const int n_ot = p.n_ot;
@@ -2143,27 +2594,27 @@ cudaError_t launch_gemm_split(const mmq_weights_s *h, const uint8_t *Q, const fl
   // one CTA per row of the padded token tiles (padding rows: a zero activation
   // row), or, with pieces, up to the last token row the GEMM copies
   const unsigned pgrid = static_cast<unsigned>(p.rows);
-  if (X) {
-    const size_t stash = static_cast<size_t>(nb32) * kSplitStashBytesPerBlock;
-    const bool fits = stash <= static_cast<size_t>(kStashMaxBytes);
-    if (q4) {
-      if (fits) split_prepass_f32_kernel<true, true><<<pgrid, 32 * kQuantWarps, stash, s>>>(X, nt, nb32, aplane, invp, cnt, ncnt);
-      else split_prepass_f32_kernel<true, false><<<pgrid, 32 * kQuantWarps, 0, s>>>(X, nt, nb32, aplane, invp, cnt, ncnt);
-    } else {
-      if (fits) split_prepass_f32_kernel<false, true><<<pgrid, 32 * kQuantWarps, stash, s>>>(X, nt, nb32, aplane, invp, cnt, ncnt);
-      else split_prepass_f32_kernel<false, false><<<pgrid, 32 * kQuantWarps, 0, s>>>(X, nt, nb32, aplane, invp, cnt, ncnt);
-    }
-  } else if (q4) {
-    split_prepass_q_kernel<true><<<pgrid, 128, 0, s>>>(Q, nt, nb32, aplane, invp, cnt, ncnt);
-  } else {
-    split_prepass_q_kernel<false><<<pgrid, 128, 0, s>>>(Q, nt, nb32, aplane, invp, cnt, ncnt);
-  }
+  if (q4)
+    pair ? split_prepass<true, true>(Q, X, nt, nb32, aplane, invp, cnt, ncnt, pgrid, p.tp, s)
+         : split_prepass<true, false>(Q, X, nt, nb32, aplane, invp, cnt, ncnt, pgrid, kTileM, s);
+  else
+    pair ? split_prepass<false, true>(Q, X, nt, nb32, aplane, invp, cnt, ncnt, pgrid, p.tp, s)
+         : split_prepass<false, false>(Q, X, nt, nb32, aplane, invp, cnt, ncnt, pgrid, kTileM, s);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   WaitCtl w{&st->status, &st->abort_epoch, epoch, limit_ns};
   if (ev0 && (e = cudaEventRecordWithFlags(ev0, s, ev_flags)) != cudaSuccess) return e;
   const uint8_t *bp = static_cast<const uint8_t *>(h->bplane);
   const uint8_t *bs = bp + b_scale_region(n_ot, nsb, q4);
+  if (pair) {
+    e = q4 ? launch_pair<true>(dev, p.grid, s, ev0 == nullptr, aplane, bp, bs, invp, nt, h->od, nb32,
+                               static_cast<int>(n_tt), n_ot, Y, w, p.tp)
+           : launch_pair<false>(dev, p.grid, s, ev0 == nullptr, aplane, bp, bs, invp, nt, h->od, nb32,
+                                static_cast<int>(n_tt), n_ot, Y, w, p.tp);
+    if (e != cudaSuccess) return e;
+    if ((e = cudaGetLastError()) == cudaSuccess && ev1) e = cudaEventRecordWithFlags(ev1, s, ev_flags);
+    return e;
+  }
   const int grid = p.grid;
   auto go = [&](auto kern, int smem, int variant) -> cudaError_t {
     static std::atomic<int> ready[10][64];  // per kernel variant: 0 unknown, 1 ready, 2 unusable

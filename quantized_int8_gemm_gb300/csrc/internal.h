@@ -73,13 +73,17 @@ cudaError_t launch_gemm(const mmq_weights_s *h, const uint8_t *Q, const float *X
                         cudaEvent_t ev1, unsigned ev_flags, float *dump = nullptr);
 
 // Split arm (activation scale folded into A as an exact fp16 hi + lo pair):
-// scratch bytes, and the prepass + GEMM launch (whole tiles).
-size_t gemm_split_scratch_bytes(const mmq_weights_s *h, int64_t nt);
-// whether the split arm would run 256-row weight tiles for this many tokens
+// scratch bytes, and the prepass + GEMM launch.  pair: the same operands and
+// arithmetic on 2-CTA clusters (cta_group::2 UMMAs of 256 weight rows by 128
+// tokens; one-plane handles only).
+size_t gemm_split_scratch_bytes(const mmq_weights_s *h, int64_t nt, bool pair);
+// whether the split arm would run 256-row weight tiles or pieces of tiles for this many tokens
 bool gemm_split_wide(const mmq_weights_s *h, int64_t nt);
+// whether MMQ_ARM_AUTO takes the pair arm for this many tokens
+bool gemm_pair_preferred(const mmq_weights_s *h, int64_t nt);
 cudaError_t launch_gemm_split(const mmq_weights_s *h, const uint8_t *Q, const float *X, int64_t nt, float *Y,
                               void *scratch, DevStatus *st, unsigned epoch, uint64_t limit_ns,
-                              cudaStream_t s, cudaEvent_t ev0, cudaEvent_t ev1, unsigned ev_flags);
+                              cudaStream_t s, cudaEvent_t ev0, cudaEvent_t ev1, unsigned ev_flags, bool pair);
 
 cudaError_t launch_wait_selftest(DevStatus *st, unsigned epoch, uint64_t limit_ns,
                                  cudaStream_t s);

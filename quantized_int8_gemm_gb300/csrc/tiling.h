@@ -107,6 +107,39 @@ __host__ __device__ constexpr uint32_t split_off(int row, int k) {
   return static_cast<uint32_t>((k >> 6) * kSplitQuarter) + operand_off(row, k & 63);
 }
 
+// ---------------------------------------------------------------- pair arm
+// The pair arm's activation plane: token tiles of TP = 2H rows (H a multiple
+// of 8, at most 64), one block per (token tile, super-block, half) holding the
+// hi and lo images grouped by the H-row half of the tile that one CTA of an SM
+// pair stages, so that a CTA's share of a half super-block is one contiguous
+// copy:
+//   [rows 0..H-1:  hi kb0][lo kb0][hi kb1][lo kb1][odd, q4_K: A min]
+//   [rows H..2H-1: the same]
+// (an H-row K-block: H rows x 128 B with the 128-byte swizzle, H * 128 bytes;
+// the min image H rows x 16 slots with the 32-byte swizzle, H * 32 bytes).
+// With H = 64 a block holds the split arm's bytes, regrouped.
+__host__ __device__ constexpr int pair_kb_bytes(int h) { return h * 128; }
+__host__ __device__ constexpr int pair_rank_bytes(bool q4, int half, int h) {
+  return 4 * pair_kb_bytes(h) + (q4 && half ? h * 32 : 0);
+}
+// bytes of one (token tile, super-block): its even and its odd block
+__host__ __device__ constexpr int pair_sb_bytes(bool q4, int h) {
+  return 2 * pair_rank_bytes(q4, 0, h) + 2 * pair_rank_bytes(q4, 1, h);
+}
+__host__ __device__ constexpr uint64_t pair_block(int64_t tile, int64_t sb, int half, int64_t nsb, bool q4, int h) {
+  return static_cast<uint64_t>((tile * nsb + sb) * pair_sb_bytes(q4, h) + (half ? 2 * pair_rank_bytes(q4, 0, h) : 0));
+}
+// byte offset of the hi element (row, k), row in [0, 2h), k in [0, 128), inside
+// a pair block; its lo element is pair_kb_bytes(h) further
+__host__ __device__ constexpr uint32_t pair_off(int row, int k, bool q4, int half, int h) {
+  return static_cast<uint32_t>((row / h) * pair_rank_bytes(q4, half, h) + (k >> 6) * 2 * pair_kb_bytes(h)) +
+         operand_off(row % h, k & 63);
+}
+// byte offset of min-term slot j of row r inside an odd pair block (q4_K)
+__host__ __device__ constexpr uint32_t pair_min_off(int row, int j, int h) {
+  return static_cast<uint32_t>((row / h) * pair_rank_bytes(true, 1, h) + 4 * pair_kb_bytes(h)) + min_off(row % h, j);
+}
+
 // ---------------------------------------------------------------- raw plane
 // The raw arm streams the packed weight bytes and unpacks them in the GEMM.
 // Per (weight tile, super-block, half) one raw block holds the bytes of that

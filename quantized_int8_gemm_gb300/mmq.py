@@ -37,9 +37,11 @@ MMQ_ARM_AUTO = 0
 MMQ_ARM_F16 = 1
 MMQ_ARM_RAW = 2
 MMQ_ARM_SPLIT = 3
+MMQ_ARM_PAIR = 4
 MMQ_OUT_F16 = 1
 MMQ_OUT_F32 = 2
-ARM_NAMES = {MMQ_ARM_F16: "f16_plane", MMQ_ARM_RAW: "raw_unpack", MMQ_ARM_SPLIT: "split_scale"}
+ARM_NAMES = {MMQ_ARM_F16: "f16_plane", MMQ_ARM_RAW: "raw_unpack", MMQ_ARM_SPLIT: "split_scale",
+             MMQ_ARM_PAIR: "split_scale_sm_pairs"}
 
 Q8_BLOCK_BYTES = 40
 BLOCK_BYTES = {MMQ_Q4_K: 144, MMQ_Q6_K: 210}
