@@ -57,6 +57,8 @@ if ROOT not in sys.path:
 METRIC = "int8 TOPS and GEMM tokens/s at 1 GB300; % of roofline (q4_K/q6_K x q8_0)"
 UNIT = "TOPS"  # 2*nt*od*id integer multiply-adds counted as 2 ops, per second, / 1e12
 DEFAULT_WORKLOAD = "q4_K_qproj_3584x3584_nt512"
+# the GEMM arm every call of the run asks for (--arm; 0: the library's choice)
+ARM = [0]
 # The pages' own q4_K q-proj kernel (nt=512, od=id=3584): 555 us after the
 # split-phase A staging step, i.e. 2*512*3584*3584 / 555e-6 = 23.7 TOPS, on an
 # unnamed GPU ("25 · r20: Split-phase A staging", §5).  Context only.
@@ -387,7 +389,7 @@ class _Workload:
         seed = cfg.seed + (1000 * rank if rank_seed else 0)
         self.W_host = gen.weights(cfg.qtype, cfg.od, cfg.id, seed, q6_scales=args.q6_scales)
         W_dev = torch.from_numpy(shard.weight_rows(self.W_host, cfg.qtype, cfg.id, self.o0, self.o1)).to(dev)
-        self.flags = mmq.MMQ_REG_WEXP if args.reg_wexp else 0
+        self.flags = (mmq.MMQ_REG_WEXP if args.reg_wexp else 0) | (mmq.MMQ_REG_RAW if args.arm == "raw" else 0)
         torch.cuda.synchronize()
         t = time.perf_counter()
         w0 = mmq.mmq_register_weights(cfg.qtype, W_dev, self.od, cfg.id, self.flags)
@@ -429,25 +431,25 @@ def _measure(args, wl, stream, world, dev, main=True):
         j = i % n_sets
         if fused:  # X -> operand plane -> Y: two kernels
             if ev is None:
-                mmq.mmq_gemm_f32(ws[j], Xs[j], Ys[j])
+                mmq.mmq_gemm_f32(ws[j], Xs[j], Ys[j], flags=ARM[0])
             else:
-                mmq.mmq_gemm_f32_profiled(ws[j], Xs[j], Ys[j], ev[0], ev[1])
+                mmq.mmq_gemm_f32_profiled(ws[j], Xs[j], Ys[j], ev[0], ev[1], flags=ARM[0])
             return
         mmq.mmq_quantize_act(Xs[j], Qs[j])  # X -> pad40 Q -> operand plane -> Y: three kernels
         if ev is None:
-            mmq.mmq_gemm(ws[j], Qs[j], nt, Ys[j])
+            mmq.mmq_gemm(ws[j], Qs[j], nt, Ys[j], flags=ARM[0])
         else:
-            mmq.mmq_gemm_profiled(ws[j], Qs[j], nt, Ys[j], ev[0], ev[1])
+            mmq.mmq_gemm_profiled(ws[j], Qs[j], nt, Ys[j], ev[0], ev[1], flags=ARM[0])
 
     K, Wu = args.steps, args.warmup
     with torch.cuda.stream(stream):
         for i in range(Wu):
             step(i)
         if fused:  # one more untimed call that reports the arm the library picked
-            arm = mmq.mmq_gemm_f32(ws[0], Xs[0], Ys[0], return_arm=True)[1]
+            arm = mmq.mmq_gemm_f32(ws[0], Xs[0], Ys[0], flags=ARM[0], return_arm=True)[1]
         else:
             mmq.mmq_quantize_act(Xs[0], Qs[0])
-            arm = mmq.mmq_gemm(ws[0], Qs[0], nt, Ys[0], return_arm=True)[1]
+            arm = mmq.mmq_gemm(ws[0], Qs[0], nt, Ys[0], flags=ARM[0], return_arm=True)[1]
     stream.synchronize()
     if mmq.mmq_last_device_error() != 0:
         raise RuntimeError("device wait expired during warm-up")
@@ -570,9 +572,9 @@ def _separate_timings(wl, stream, peaks, reps=200):
         res[f"quantize_act_{mode}_us"] = _graph_time_us(
             stream, [lambda j=pick(i): mmq.mmq_quantize_act(wl.Xs[j], wl.Qs[j]) for i in range(reps)])
         res[f"gemm_{mode}_us"] = _graph_time_us(
-            stream, [lambda j=pick(i): mmq.mmq_gemm(wl.ws[j], wl.Qs[j], nt, wl.Ys[j]) for i in range(reps)])
+            stream, [lambda j=pick(i): mmq.mmq_gemm(wl.ws[j], wl.Qs[j], nt, wl.Ys[j], flags=ARM[0]) for i in range(reps)])
         res[f"fused_{mode}_us"] = _graph_time_us(
-            stream, [lambda j=pick(i): mmq.mmq_gemm_f32(wl.ws[j], wl.Xs[j], wl.Ys[j]) for i in range(reps)])
+            stream, [lambda j=pick(i): mmq.mmq_gemm_f32(wl.ws[j], wl.Xs[j], wl.Ys[j], flags=ARM[0]) for i in range(reps)])
     if mmq.mmq_last_device_error() != 0:
         raise RuntimeError("device wait expired in the separate timings")
     qbytes = nt * id_ * 4 + nt * (id_ // 32) * 40  # read X, write the pad40 blocks: 168 B per block
@@ -622,10 +624,10 @@ def _e2e(args, wl, stream, world, dev, ops, d2h_bytes):
             if started[j]:
                 stream.wait_event(done_o[j])  # set j's Y is free once read back
             if fused:
-                mmq.mmq_gemm_f32(ws[j], Xs[j], Ys[j])
+                mmq.mmq_gemm_f32(ws[j], Xs[j], Ys[j], flags=ARM[0])
             else:
                 mmq.mmq_quantize_act(Xs[j], Qs[j])
-                mmq.mmq_gemm(ws[j], Qs[j], nt, Ys[j])
+                mmq.mmq_gemm(ws[j], Qs[j], nt, Ys[j], flags=ARM[0])
             done_c[j].record()
         with torch.cuda.stream(s_out):
             s_out.wait_event(done_c[j])
@@ -853,6 +855,8 @@ def main(argv=None):
                     help="register with MMQ_REG_WEXP: the operand plane is built from the dense W_exp "
                          "plane (the workload is then named <workload>_wexp)")
     ap.add_argument("--no-also", action="store_true", help="skip the other q-proj workload")
+    ap.add_argument("--arm", choices=("auto", "f16", "raw", "split", "pair"), default="auto",
+                    help="force one GEMM arm (default: the library's choice)")
     ap.add_argument("--engines", action="store_true",
                     help="print the tensor engines' rates (the library's probe, torch._int_mm and fp16 matmul) "
                          "instead of a bench line")
@@ -864,6 +868,7 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    ARM[0] = {"auto": 0, "f16": 1, "raw": 2, "split": 3, "pair": 4}[args.arm]
     from synth import gen
     cfg = gen.config_by_name(args.workload)
     if args.nt is not None:  # the workload's weights and generators at another token count

@@ -52,3 +52,14 @@ def test_nt_override_renames_the_workload(monkeypatch):
     bench.main(["--impl", "reference", "--workload", "q6_K_qproj_3584x3584_nt512", "--nt", "16"])
     cfg = got["cfg"]
     assert (cfg.name, cfg.nt, cfg.od, cfg.id, cfg.qtype) == ("q6_K_qproj_3584x3584_nt16", 16, 3584, 3584, "q6_K")
+
+
+def test_arm_option_sets_the_flags_every_call_passes(monkeypatch):
+    """--arm forces one GEMM arm for the run (the C ABI's MMQ_ARM_* values)."""
+    monkeypatch.setattr(bench, "run_reference", lambda args, cfg, rank: None)
+    try:
+        for name, flag in (("pair", 4), ("split", 3), ("f16", 1), ("auto", 0)):
+            bench.main(["--impl", "reference", "--arm", name])
+            assert bench.ARM[0] == flag
+    finally:
+        bench.ARM[0] = 0
