@@ -72,6 +72,7 @@ constexpr int SRING = 4;          // per-super-block scale ring entries
 constexpr int RRING = 4;          // raw arm: raw weight block ring entries
 constexpr int EPI_WARPS = 8;      // warpgroups 0 and 1
 constexpr int PRODUCER_WARP = 8;  // warpgroup 2: producer, two UMMA issuers, one idle warp
+constexpr int PRODUCER2_WARP = 10;  // the pair arm's second producer
 constexpr int ISSUER_WARP = 9;    // issuers 9 and 10; issuer i owns TMEM slots 2i and 2i+1
 constexpr int ISSUERS = 2;
 constexpr int CONVERTER_WARP = 12;  // raw arm: warpgroup 3 unpacks the weight blocks
@@ -1816,10 +1817,10 @@ __global__ void __launch_bounds__(SplitShape::kThreads, 1)
 // summation order inside a super-block may differ.
 //
 // Roles (both CTAs): warps 0-7 epilogue of the CTA's own 128 weight rows,
-// warp 8 producer (its own stage halves and scale blocks).  Warp 9: in the
-// even CTA the UMMA issuer; in the odd CTA a relay that, once a stage of its
-// own has landed, arrives on the even CTA's barrier for that stage, which so
-// waits for both halves.  The issuer's commits arrive on both CTAs' barriers
+// warps 8 and 10 producers (the CTA's own stages, even and odd, and its
+// scale blocks).  Warp 9: in the even CTA the UMMA issuer; in the odd CTA a
+// relay that, once a stage of its own has landed, arrives on the even CTA's
+// barrier for that stage, which so waits for both halves.  The issuer's commits arrive on both CTAs' barriers
 // (stage free, accumulator ready); both epilogues arrive on the even CTA's
 // accumulator-free barrier.  The q4_K min term: per super-block one K = 16
 // pair UMMA of the weight min images (A) against the activation min images
@@ -1919,8 +1920,11 @@ __global__ void __launch_bounds__(PairShape::kThreads, 1)
   const uint32_t tbase = *reinterpret_cast<volatile uint32_t *>(smem + L::kSlot);
   if (warp >= PRODUCER_WARP) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(PairShape::kRegsCtl));
-    if (warp == PRODUCER_WARP) {
-      // ------------------------------------------------------------ producer
+    if (warp == PRODUCER_WARP || warp == PRODUCER2_WARP) {
+      // ------------------------------------------------------------ producers
+      // two warps, the even and the odd stages (the scale blocks with the
+      // even ones); one warp's per-stage code spilled in the q4_K variant
+      const int p = warp == PRODUCER_WARP ? 0 : 1;
       griddep_wait();  // the activation blocks come from the kernel before this one
       uint32_t ks = 0, ns = 0, issued = 0, s_issued = 0;
       bool ok = true;
@@ -1928,9 +1932,10 @@ __global__ void __launch_bounds__(PairShape::kThreads, 1)
         const int tt = u % n_tt, w = wtile(u / n_tt);
         for (int64_t sb = 0; sb < nsb && ok; ++sb, ++ns) {
           const int e = static_cast<int>(ns % SRING);
-          ok = __all_sync(0xffffffffu, mbar_wait(sempty(e), ((ns / SRING) & 1) ^ 1, wctl));
+          if (p == 0) ok = __all_sync(0xffffffffu, mbar_wait(sempty(e), ((ns / SRING) & 1) ^ 1, wctl));
           if (!ok) break;
           for (int qq = 0; qq < 4; ++qq, ++ks) {  // 64-K quarters of the super-block
+            if (static_cast<int>(ks & 1) != p) continue;
             const int s = static_cast<int>(ks % STAGES);
             ok = __all_sync(0xffffffffu, mbar_wait(empty(s), ((ks / STAGES) & 1) ^ 1, wctl));
             if (!ok) break;
@@ -1951,7 +1956,7 @@ __global__ void __launch_bounds__(PairShape::kThreads, 1)
             }
             __syncwarp();
             issued = ks + 1;
-            if (qq == 0) {  // the super-block's scales, after its first stage's operands
+            if (qq == 0) {  // (producer 0) the super-block's scales, after its first stage's operands
               if (lane == 1) {
                 mbar_arrive_expect_tx(sfull(e), L::kScale);
                 bulk_load(s_smem(e), bscale + b_scale_block(w, sb, nsb, kQ4), L::kScale, sfull(e));
@@ -1962,9 +1967,9 @@ __global__ void __launch_bounds__(PairShape::kThreads, 1)
           }
         }
       }
-      if (!ok) {  // drain this CTA's copies still in flight
+      if (!ok) {  // drain this warp's copies still in flight
         for (uint32_t k = issued > STAGES ? issued - STAGES : 0; k < issued; ++k)
-          mbar_wait(full(k % STAGES), (k / STAGES) & 1, wctl, false);
+          if (static_cast<int>(k & 1) == p) mbar_wait(full(k % STAGES), (k / STAGES) & 1, wctl, false);
         for (uint32_t k = s_issued > SRING ? s_issued - SRING : 0; k < s_issued; ++k)
           mbar_wait(sfull(k % SRING), (k / SRING) & 1, wctl, false);
       }
