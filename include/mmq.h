@@ -338,6 +338,11 @@ int mmq_selftest_wait_timeout(uint64_t timeout_ns, mmq_stream_t stream);
  *              MACs per clock per SM (one issuing warp per SM, back to back)
  *   out[3]     mma.sync m16n8k32 s8 -> s32 over the whole GPU, TOPS (2 ops per MAC)
  *   out[4]     mma.sync m16n8k16 f16 -> f32 over the whole GPU, TFLOP/s
+ *   out[5..6]  as out[0..2], N = 96 / 112
+ *   out[7..11] tcgen05.mma.cta_group::2 kind::f16 on 2-CTA clusters, M = 256,
+ *              K = 16, N = 64 / 96 / 112 / 128 / 256: MACs per clock per SM
+ *              of the pair (the pair arm's UMMA shape)
+ * (12 doubles.)
  * Synchronizes `stream`; takes well under a second.  Errors: MMQ_ERR_ARG,
  * MMQ_ERR_NO_DEVICE, MMQ_ERR_CUDA, MMQ_ERR_DEVICE_TIMEOUT.
  */

@@ -7,6 +7,10 @@
 //                        TMEM accumulator, operands (zeros) in shared memory;
 //                        the issuing thread's clock64 over the loop and the
 //                        final commit gives clk per UMMA
+//   umma_pair_rate_kernel<N>  the same on 2-CTA clusters: the even CTA issues
+//                        cta_group::2 UMMAs of M = 256 (128 A rows and N / 2 B
+//                        rows in each CTA's shared memory, the rates the pair
+//                        arm's tiles of 256 weight rows x N tokens run at)
 //   mma_sync_s8_kernel   warp-level mma.sync m16n8k32 s8 -> s32, eight
 //                        independent accumulators per warp
 //   mma_sync_f16_kernel  warp-level mma.sync m16n8k16 f16 -> f32, likewise
@@ -27,6 +31,9 @@ constexpr int kUmmaIters = 4096;
 // UMMA).  The launch asks for kUmmaSmem bytes so that one CTA runs per SM.
 template <int N>
 __host__ __device__ constexpr int umma_ops_bytes() { return 16384 + N * 128; }
+// TMEM columns for an N-column accumulator: a power of two, at least 32
+template <int N>
+__host__ __device__ constexpr int tmem_cols() { return N <= 32 ? 32 : N <= 64 ? 64 : N <= 128 ? 128 : 256; }
 constexpr int kUmmaSmem = 120 * 1024;
 static_assert(umma_ops_bytes<256>() + 1024 <= kUmmaSmem, "operands fit the request");
 
@@ -45,7 +52,7 @@ __global__ void __launch_bounds__(128, 1) umma_rate_kernel(WaitCtl wctl, long lo
     fence_mbar_init();
   }
   if (threadIdx.x < 32) {
-    tmem_alloc(smem_addr(&tslot), N < 32 ? 32 : N);
+    tmem_alloc(smem_addr(&tslot), tmem_cols<N>());
     tmem_relinquish();
   }
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the zeroed operands, for the tensor core
@@ -72,7 +79,54 @@ __global__ void __launch_bounds__(128, 1) umma_rate_kernel(WaitCtl wctl, long lo
   __syncthreads();
   if (threadIdx.x < 32) {
     tc_fence_after();
-    tmem_dealloc(tbase, N < 32 ? 32 : N);
+    tmem_dealloc(tbase, tmem_cols<N>());
+  }
+}
+
+template <int N>
+__global__ void __launch_bounds__(128, 1) umma_pair_rate_kernel(WaitCtl wctl, long long *clk_per_pair) {
+  extern __shared__ uint8_t dyn[];
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t tslot;
+  const uint32_t rank = cluster_ctarank();
+  const uint32_t raw = smem_addr(dyn);
+  uint8_t *ops = dyn + (((raw + 1023u) & ~1023u) - raw);
+  for (int i = threadIdx.x; i < umma_ops_bytes<N / 2>() / 16; i += blockDim.x)
+    reinterpret_cast<uint4 *>(ops)[i] = make_uint4(0, 0, 0, 0);
+  const uint32_t b = smem_addr(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);
+    fence_mbar_init();
+  }
+  if (threadIdx.x < 32) {  // one warp of each CTA of the pair, together
+    tmem_alloc_pair(smem_addr(&tslot), tmem_cols<N>());
+    tmem_relinquish_pair();
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tbase = *reinterpret_cast<volatile uint32_t *>(&tslot);
+  if (threadIdx.x < 32) {
+    uint32_t elected;
+    asm volatile("{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}" : "=r"(elected));
+    constexpr uint32_t idesc = idesc_f16_f32(256, N);
+    const uint64_t ad = sdesc_kmajor_sw128(smem_addr(ops)), bd = sdesc_kmajor_sw128(smem_addr(ops + 16384));
+    long long t0 = 0;
+    if (rank == 0 && elected) {
+      t0 = clock64();
+      for (int i = 0; i < kUmmaIters; ++i) umma_pair_f16(tbase, ad + 2 * (i & 3), bd + 2 * (i & 3), idesc, i ? 1u : 0u);
+      umma_pair_commit(b);  // arrives on both CTAs' barrier
+    }
+    __syncwarp();
+    const bool ok = mbar_wait(b, 0, wctl, false);
+    if (rank == 0 && elected) clk_per_pair[blockIdx.x >> 1] = ok ? clock64() - t0 : -1;
+  }
+  tc_fence_before();
+  cluster_sync();  // neither CTA leaves while the other's UMMAs may still read its operands
+  if (threadIdx.x < 32) {
+    tc_fence_after();
+    tmem_dealloc_pair(tbase, tmem_cols<N>());
   }
 }
 
@@ -170,6 +224,42 @@ cudaError_t umma_rate(int sms, WaitCtl w, long long *clk, cudaStream_t s, double
   return cudaSuccess;
 }
 
+template <int N>
+cudaError_t umma_pair_rate(int sms, WaitCtl w, long long *clk, cudaStream_t s, double *mac_per_clk) {
+  auto kern = umma_pair_rate_kernel<N>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kUmmaSmem);
+  if (e != cudaSuccess) return e;
+  const int pairs = sms / 2;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * static_cast<unsigned>(pairs));
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = kUmmaSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, w, clk);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return e;
+  long long *h = new long long[pairs];
+  e = cudaMemcpy(h, clk, sizeof(long long) * pairs, cudaMemcpyDeviceToHost);
+  double sum = 0;
+  int n = 0;
+  for (int i = 0; e == cudaSuccess && i < pairs; ++i)
+    if (h[i] > 0) {
+      sum += static_cast<double>(h[i]);
+      ++n;
+    }
+  delete[] h;
+  if (e != cudaSuccess) return e;
+  *mac_per_clk = n ? 256.0 * N * 16 * kUmmaIters / (sum / n) / 2.0 : 0.0;  // per SM of the pair
+  return cudaSuccess;
+}
+
 }  // namespace
 
 cudaError_t launch_engine_probes(DevStatus *st, unsigned epoch, uint64_t limit_ns, cudaStream_t s, double *out) {
@@ -183,6 +273,13 @@ cudaError_t launch_engine_probes(DevStatus *st, unsigned epoch, uint64_t limit_n
   e = umma_rate<64>(sms, w, clk, s, &out[0]);
   if (e == cudaSuccess) e = umma_rate<128>(sms, w, clk, s, &out[1]);
   if (e == cudaSuccess) e = umma_rate<256>(sms, w, clk, s, &out[2]);
+  if (e == cudaSuccess) e = umma_rate<96>(sms, w, clk, s, &out[5]);
+  if (e == cudaSuccess) e = umma_rate<112>(sms, w, clk, s, &out[6]);
+  if (e == cudaSuccess) e = umma_pair_rate<64>(sms, w, clk, s, &out[7]);
+  if (e == cudaSuccess) e = umma_pair_rate<96>(sms, w, clk, s, &out[8]);
+  if (e == cudaSuccess) e = umma_pair_rate<112>(sms, w, clk, s, &out[9]);
+  if (e == cudaSuccess) e = umma_pair_rate<128>(sms, w, clk, s, &out[10]);
+  if (e == cudaSuccess) e = umma_pair_rate<256>(sms, w, clk, s, &out[11]);
   cudaFree(clk);
   if (e != cudaSuccess) return e;
   int *sink = nullptr;

@@ -299,11 +299,15 @@ def mmq_strerror(code: int) -> str:
 
 def mmq_probe_engine_rates(stream=None) -> dict:
     """Rates of the tensor engines on the current device (a measurement hook):
-    tcgen05 kind::f16 MACs per clock per SM at N = 64, 128, 256, and the
-    whole-GPU mma.sync s8 TOPS and f16 TFLOP/s."""
-    out = (ctypes.c_double * 5)()
+    tcgen05 kind::f16 MACs per clock per SM, M = 128 (cta_group::1) and
+    M = 256 over an SM pair (cta_group::2), at several N; the whole-GPU
+    mma.sync s8 TOPS and f16 TFLOP/s."""
+    out = (ctypes.c_double * 12)()
     rc = load().mmq_probe_engine_rates(ctypes.cast(out, ctypes.c_void_p), _stream(stream))
     if rc != MMQ_OK:
         raise MMQError(rc, "mmq_probe_engine_rates")
-    return {"umma_f16_mac_per_clk_per_sm": {"N64": out[0], "N128": out[1], "N256": out[2]},
+    return {"umma_f16_mac_per_clk_per_sm": {"N64": out[0], "N96": out[5], "N112": out[6], "N128": out[1],
+                                            "N256": out[2]},
+            "umma_pair_f16_mac_per_clk_per_sm": {"N64": out[7], "N96": out[8], "N112": out[9], "N128": out[10],
+                                                 "N256": out[11]},
             "mma_sync_s8_tops": out[3], "mma_sync_f16_tflops": out[4]}

@@ -16,7 +16,12 @@ def test_engine_rates():
     umma = r["umma_f16_mac_per_clk_per_sm"]
     assert 3600 <= umma["N128"] <= 4200, umma
     assert 3600 <= umma["N256"] <= 4200, umma
-    assert 0 < umma["N64"] < umma["N128"], umma
+    assert 0 < umma["N64"] < umma["N96"] < umma["N112"] <= umma["N128"], umma
+    # on an SM pair (M = 256) the pair arm's 112-token tiles run at the full rate
+    pair = r["umma_pair_f16_mac_per_clk_per_sm"]
+    for n in ("N112", "N128", "N256"):
+        assert 3600 <= pair[n] <= 4200, pair
+    assert 0 < pair["N64"] < pair["N112"], pair
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     # even at a 1.5 GHz SM clock the whole GPU's fp16 UMMA rate is > 10x the int8 mma.sync rate measured here
     umma_tflops_at_1p5ghz = 2 * umma["N128"] * sms * 1.5e9 / 1e12
