@@ -114,8 +114,8 @@ typedef struct mmq_weights_s *mmq_weights_t;
                               over several CTAs whose partial sums are added in a fixed
                               order (repeat calls bit-identical) */
 #define MMQ_ARM_PAIR 4     /* MMQ_ARM_SPLIT's operands and arithmetic on pairs of SMs: 2-CTA
-                              clusters run cta_group::2 UMMAs of 256 weight rows x 128 (or
-                              112) tokens, each SM staging its own 128 weight rows and half
+                              clusters run cta_group::2 UMMAs of 256 weight rows x 128 (112,
+                              96) tokens, each SM staging its own 128 weight rows and half
                               of the token rows, so a 64-K stage of the operand ring holds a
                               third less and takes two bulk copies; whole tiles; results
                               within fp32 summation of MMQ_ARM_SPLIT's (the tensor core sums

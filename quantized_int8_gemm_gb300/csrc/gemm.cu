@@ -1804,7 +1804,7 @@ __global__ void __launch_bounds__(SplitShape::kThreads, 1)
 // computes output tiles of 256 weight rows x 128 tokens with cta_group::2
 // UMMAs of M = 256, N = 128: the weights are the A operand (each CTA stages
 // its own weight tile's 128 rows) and the hi and lo activation images the B
-// operand (each CTA stages half of the tile's tp = 128 or 112 token rows, from
+// operand (each CTA stages half of the tile's tp = 128, 112 or 96 token rows, from
 // the pair layout of tiling.h).  A 64-K stage takes two bulk copies per CTA,
 // its weight K-block and its activation rows (hi and lo side by side in the
 // pair layout), so six stages are in flight: measured, three or four copies
@@ -2370,7 +2370,7 @@ struct SplitPlan {
   bool q4, wide;
   int kp;      // pieces per pieced tile (1: whole tiles only)
   int n_full;  // tiles done whole, before the pieced ones
-  int tp;      // tokens per tile (the pair arm: 128 or 112; else 128)
+  int tp;      // tokens per tile (the pair arm: 128, 112 or 96; else 128)
   int64_t n_tt, nt_pad, nsb, rows;  // rows: activation rows the prepass writes
   int n_ot, n_tiles, grid;
   size_t inv_off, part_off, cnt_off, bytes;
@@ -2436,14 +2436,16 @@ SplitPlan plan_split(const mmq_weights_s *h, int64_t nt, bool pair) {
   p.tp = kTileM;
   if (pair) {
     // the pair arm: whole tiles of 256 weight rows x tp tokens, one SM pair
-    // each; tp = 112 when it leaves fewer SM pairs idle in the busiest wave
-    // (the q-proj shapes: 70 tiles over 140 SMs instead of 56 over 112)
+    // each; tp = 112 or 96 when that leaves fewer SM pairs idle (the q-proj
+    // shapes at 512 tokens: 70 tiles over 140 SMs instead of 56 over 112)
     const int cap = p.q4 ? pair_capacity<true>(h->device) : pair_capacity<false>(h->device);
     const int64_t pairs = cap > 0 ? cap : 1, n_wp = (p.n_ot + 1) / 2;
-    int64_t best_est = -1;
-    for (int tp : {128, 112}) {
+    // waves of tiles times the tile's UMMA time: tp over the pair UMMA's
+    // measured rate at N = tp (N = 128 and 112: the full rate, 96: 0.973)
+    double best_est = -1;
+    for (int tp : {128, 112, 96}) {
       const int64_t units = (nt + tp - 1) / tp * n_wp;
-      const int64_t est = (units + pairs - 1) / pairs * tp;
+      const double est = static_cast<double>((units + pairs - 1) / pairs) * tp / (tp == 96 ? 0.973 : 1.0);
       if (best_est < 0 || est < best_est) {
         best_est = est;
         p.tp = tp;
