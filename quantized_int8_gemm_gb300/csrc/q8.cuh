@@ -40,9 +40,19 @@ __device__ __forceinline__ void q8_lane(float4 v, float &d16f, float (&q)[4]) {
   const float d = amax / 127.0f;
   const float xs[4] = {v.x, v.y, v.z, v.w};
   if (amax >= kQ8FastAmax) {
+    // q8_quot on pairs: the packed fp32x2 multiply and fmas round each lane
+    // as the scalar ones do
     const float r = __frcp_rn(d);
+    const float2 d2 = make_float2(d, d), r2 = make_float2(r, r);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) q[i] = roundf(q8_quot(xs[i], d, r));
+    for (int i = 0; i < 4; i += 2) {
+      const float2 x = make_float2(xs[i], xs[i + 1]);
+      const float2 p = __fmul2_rn(x, r2);
+      const float2 e = __ffma2_rn(make_float2(-p.x, -p.y), d2, x);
+      const float2 qq = __ffma2_rn(e, r2, p);
+      q[i] = roundf(qq.x);
+      q[i + 1] = roundf(qq.y);
+    }
   } else if (amax != 0.0f) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) q[i] = roundf(xs[i] / d);
