@@ -1508,6 +1508,32 @@ __global__ void __launch_bounds__(SplitShape::kThreads, 1)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(SplitRegs<L::kShared>::kCtl));
   if (warp == PRODUCER_WARP) {
     // ------------------------------------------------------------ producer
+    // (kKP) The weight copies of the first unit's first stages do not depend on
+    // the quantization kernel: with few token rows it holds few SMs, so this
+    // CTA may already run beside it, and they go out before the wait (their
+    // bytes expected without an arrival; the activation copies arrive later).
+    uint32_t pre = 0;
+    if constexpr (kKP) {
+      if (static_cast<int>(blockIdx.x) < n_units) {
+        const int u = blockIdx.x, og = unit_tile(u) / n_tt;
+        const int64_t sb0 = unit_sb0(u);
+        pre = static_cast<uint32_t>(min(static_cast<int64_t>(STAGES), 4 * (unit_sb1(u) - sb0)));
+        if (lane == 1) {
+          for (uint32_t q = 0; q < pre; ++q) {  // (the ring is fresh: these stages are free)
+            const int64_t sb = sb0 + q / 4;
+            const int qq = static_cast<int>(q % 4), half = qq >> 1, kb = qq & 1;
+            const bool mins = kQ4 && !SH && qq == 3;
+            mbar_expect_tx(full(static_cast<int>(q)), NW * L::kBK + (mins ? L::kMinB : 0));
+            for (int w = 0; w < NW; ++w) {
+              const uint8_t *bblk = bplane + b_block(wtile(og, w), sb, half, nsb, kQ4);
+              bulk_load(b_smem(q) + w * L::kBK, bblk + kb * L::kBK, L::kBK, full(q));
+              if (mins) bulk_load(b_smem(q) + NW * L::kBK + w * kMinBytes, bblk + kBMin, kMinBytes, full(q));
+            }
+          }
+        }
+        __syncwarp();
+      }
+    }
     griddep_wait();  // the activation blocks come from the kernel before this one
     uint32_t ks = 0, ns = 0, issued = 0, s_issued = 0, m_issued = 0;
     bool ok = true;
@@ -1553,8 +1579,10 @@ __global__ void __launch_bounds__(SplitShape::kThreads, 1)
           const int half = qq >> 1, kb = qq & 1;
           const bool mins = kQ4 && !SH && qq == 3;
           const uint8_t *ablk = aplane + as_block(tt, sb, half, nsb, kQ4);
+          const bool w_done = ks < pre;  // (kKP) its weight copies went out before the wait
           if (lane == 0) {
-            mbar_arrive_expect_tx(full(s), 2 * arow + NW * L::kBK * (kB0 ? 2 : 1) + (mins ? L::kMinA + L::kMinB : 0));
+            mbar_arrive_expect_tx(full(s), 2 * arow + (mins ? L::kMinA : 0) +
+                                               (w_done ? 0 : NW * L::kBK * (kB0 ? 2 : 1) + (mins ? L::kMinB : 0)));
             if (kKP) {  // the hi and the lo K-block's first rows
               bulk_load(a_smem(s), ablk + kb * kSplitQuarter, arow, full(s));
               bulk_load(a_smem(s) + kSplitLo, ablk + kb * kSplitQuarter + kSplitLo, arow, full(s));
@@ -1562,7 +1590,7 @@ __global__ void __launch_bounds__(SplitShape::kThreads, 1)
               bulk_load(a_smem(s), ablk + kb * kSplitQuarter, kSplitQuarter, full(s));
             }
             if (mins) bulk_load(a_smem(s) + kSplitQuarter, ablk + kSplitMin, kMinBytes, full(s));
-          } else if (lane == 1) {
+          } else if (lane == 1 && !w_done) {
             for (int w = 0; w < NW; ++w) {
               const uint8_t *bblk = bplane + b_block(wtile(og, w), sb, half, nsb, kQ4);
               bulk_load(b_smem(s) + w * L::kBK, bblk + kb * L::kBK, L::kBK, full(s));
