@@ -238,8 +238,11 @@ __global__ void __launch_bounds__(128) gemm_prepass_kernel(const uint8_t *__rest
                                                            int64_t nt, int64_t nb32,
                                                            uint8_t *__restrict__ aplane,
                                                            float *__restrict__ dap,
-                                                           float *__restrict__ invp) {
+                                                           float *__restrict__ invp,
+                                                           uint64_t *__restrict__ flags, int nflags) {
   griddep_launch_dependents();
+  if (blockIdx.x == 0)  // the GEMM's stream-K hand-off flags start clear (a graph replays its tags)
+    for (int i = threadIdx.x; i < nflags; i += blockDim.x) flags[i] = 0;
   const int64_t t = blockIdx.x;
   const bool live = t < nt;  // rows nt .. nt_pad - 1 of the last tile: a zero activation row
   const int tid = threadIdx.x;
@@ -369,9 +372,12 @@ __global__ void __launch_bounds__(32 * kQuantWarps) quantize_prepass_kernel(cons
                                                                int64_t nt, int64_t nb32,
                                                                uint8_t *__restrict__ aplane,
                                                                float *__restrict__ dap,
-                                                               float *__restrict__ invp) {
+                                                               float *__restrict__ invp,
+                                                               uint64_t *__restrict__ flags, int nflags) {
   extern __shared__ float stash[];  // [nb32] d16, then [nb32] ssum
   griddep_launch_dependents();
+  if (blockIdx.x == 0)  // the GEMM's stream-K hand-off flags start clear (a graph replays its tags)
+    for (int i = threadIdx.x; i < nflags; i += blockDim.x) flags[i] = 0;
   const int64_t t = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int part = lane & 7, grp = lane >> 3;
@@ -1251,8 +1257,8 @@ __global__ void __launch_bounds__(Shape<kRaw>::kThreads, 1)
       }
       if (!ok) break;
       if (kSK && (sb0 != 0 || sb1 != nsb)) {
-        // hand-off tag of this launch: the scratch holding the flags is not
-        // cleared, so the tag pairs the epoch with its complement
+        // hand-off tag of this launch: the flags are cleared by the kernel
+        // before this one; the tag pairs the epoch with its complement
         const uint64_t tag = (static_cast<uint64_t>(wctl.epoch) << 32) | static_cast<uint32_t>(~wctl.epoch);
         // A tile cut between CTAs.  Its owner is the CTA holding its first
         // super-block, where that CTA's range ends; the others hold the rest
@@ -2332,18 +2338,24 @@ cudaError_t launch_gemm(const mmq_weights_s *h, const uint8_t *Q, const float *X
   // a zero activation row, so the last tile's padding reads as zero.
   cudaError_t e = cudaSuccess;
   const unsigned pgrid = static_cast<unsigned>(nt_pad);
+  // (the hand-off tags repeat when a CUDA graph replays this launch, so the
+  // flags are cleared before every GEMM, by the kernel before it)
+  const int nflags = p.streamk ? p.grid : 0;
   if (X) {
     const size_t stash = static_cast<size_t>(nb32) * kStashBytesPerBlock;
     if (!q4)
-      quantize_prepass_kernel<false, false><<<pgrid, 32 * kQuantWarps, 0, s>>>(X, nt, nb32, aplane, dap, invp);
+      quantize_prepass_kernel<false, false>
+          <<<pgrid, 32 * kQuantWarps, 0, s>>>(X, nt, nb32, aplane, dap, invp, flags, nflags);
     else if (stash <= static_cast<size_t>(kStashMaxBytes))
-      quantize_prepass_kernel<true, true><<<pgrid, 32 * kQuantWarps, stash, s>>>(X, nt, nb32, aplane, dap, invp);
+      quantize_prepass_kernel<true, true>
+          <<<pgrid, 32 * kQuantWarps, stash, s>>>(X, nt, nb32, aplane, dap, invp, flags, nflags);
     else
-      quantize_prepass_kernel<true, false><<<pgrid, 32 * kQuantWarps, 0, s>>>(X, nt, nb32, aplane, dap, invp);
+      quantize_prepass_kernel<true, false>
+          <<<pgrid, 32 * kQuantWarps, 0, s>>>(X, nt, nb32, aplane, dap, invp, flags, nflags);
   } else if (q4) {
-    gemm_prepass_kernel<true><<<pgrid, 128, 0, s>>>(Q, nt, nb32, aplane, dap, invp);
+    gemm_prepass_kernel<true><<<pgrid, 128, 0, s>>>(Q, nt, nb32, aplane, dap, invp, flags, nflags);
   } else {
-    gemm_prepass_kernel<false><<<pgrid, 128, 0, s>>>(Q, nt, nb32, aplane, dap, invp);
+    gemm_prepass_kernel<false><<<pgrid, 128, 0, s>>>(Q, nt, nb32, aplane, dap, invp, flags, nflags);
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;

@@ -38,6 +38,17 @@ def test_binding_names_match_header():
     assert sorted(mmq.EXPORTS) == _declared_symbols()
 
 
+def test_binding_flag_values_match_header():
+    """The flag and arm constants the binding passes are the header's."""
+    from quantized_int8_gemm_gb300 import mmq
+    src = open(os.path.join(ROOT, "include", "mmq.h")).read()
+    defs = {m.group(1): int(m.group(2), 0)
+            for m in re.finditer(r"#define\s+(MMQ_(?:ARM|REG)_[A-Z0-9_]+)\s+(0x[0-9a-fA-F]+|[0-9]+)u?\b", src)}
+    assert {"MMQ_ARM_PAIR", "MMQ_ARM_SPLIT", "MMQ_REG_RAW"} <= set(defs)
+    for name, value in defs.items():
+        assert getattr(mmq, name) == value, name
+
+
 def test_strerror_and_argument_checks_without_gpu(lib):
     lib.mmq_strerror.restype = ctypes.c_char_p
     assert lib.mmq_strerror(0) == b"ok"
