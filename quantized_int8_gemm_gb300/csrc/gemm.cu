@@ -1358,17 +1358,31 @@ struct SplitRegs {
 
 // kB0 (q6_K with |sc| > 64): after the kN / 128 B1 K-blocks of a stage come
 // as many B0 K-blocks.
-template <bool kQ4, bool kWide, bool kB0 = false>
+// kSmall (pieces of one token tile of at most kSmallRows tokens): a stage's
+// activation region holds only those rows -- the hi K-block's, the lo
+// K-block's, (q4_K) the min image's -- so the ring holds twice as many stages;
+// the UMMA still reads 128 rows of A from the region's start, the rows beyond
+// it (the lo image, the weights) feeding output rows that are never stored.
+template <bool kQ4, bool kWide, bool kB0 = false, bool kSmall = false>
 struct SplitSmem {
   static constexpr bool kShared = kQ4 && kWide;  // min terms share the accumulator regions
   static constexpr int kN = kWide ? 256 : 128;
   static constexpr int kBK = kTileN * 64 * 2;  // one weight K-block of one tile: 16384
-  static constexpr int kMinA = kQ4 && !kShared ? kMinBytes : 0;
+  static constexpr int kSmallRows = 32;
+  // A region: hi K-block, lo K-block at kALo, (q4_K) min image at kAMin, kMinA bytes of it copied
+  static constexpr int kALo = kSmall ? kSmallRows * 128 : kSplitLo;
+  static constexpr int kAMin = kSmall ? 2 * kSmallRows * 128 : kSplitQuarter;
+  static constexpr int kMinA = kQ4 && !kShared ? (kSmall ? kSmallRows * 32 : kMinBytes) : 0;
   static constexpr int kMinB = kQ4 && !kShared ? kMinBytes * (kN / 128) : 0;
-  static constexpr int kA = kSplitQuarter + kMinA;
+  static constexpr int kA = ((kAMin + kMinA + 1023) / 1024) * 1024;
   static constexpr int kB = ((kBK * (kN / 128) * (kB0 ? 2 : 1) + kMinB + 1023) / 1024) * 1024;
   static constexpr int kStage = kA + kB;
-  static constexpr int kStages = kStage * 4 <= 200 * 1024 ? 4 : kStage * 3 <= 200 * 1024 ? 3 : 2;
+  static constexpr int kStages = kSmall ? (8 * kStage <= 210 * 1024 ? 8 : 210 * 1024 / kStage)
+                                        : kStage * 4 <= 200 * 1024 ? 4 : kStage * 3 <= 200 * 1024 ? 3 : 2;
+  static_assert(!kSmall || (!kWide && !kB0), "small activation regions: 128-row one-plane tiles");
+  // (kSmall) a UMMA's 128 rows of A from any of the region's images stay inside the stage
+  static_assert(!kSmall || kAMin + kMinBytes <= kStage, "A reads inside the stage");
+  static_assert(!kSmall || kALo + kOperandBytes / 2 <= kStage, "A reads inside the stage");
   // kShared: min operand ring, entry = A min image then kN / 128 B min images
   static constexpr int kMR = kShared ? 2 : 0;
   static constexpr int kMinEntry = kMinBytes * (1 + kN / 128);
@@ -1425,7 +1439,7 @@ __device__ __forceinline__ void fold_region(uint32_t ta, const float4 *s4, float
 // whichever CTA finishes last.  Activation K-blocks are copied only up to the
 // tile's last token row (rounded up to 8): rows beyond it feed output rows
 // that are never stored.
-template <bool kQ4, bool kWide, bool kB0, bool kKP = false>
+template <bool kQ4, bool kWide, bool kB0, bool kKP = false, bool kSmall = false>
 __global__ void __launch_bounds__(SplitShape::kThreads, 1)
     mmq_gemm_split_kernel(const uint8_t *__restrict__ aplane, const uint8_t *__restrict__ bplane,
                           const uint8_t *__restrict__ bscale, const float *__restrict__ invp, int64_t nt,
@@ -1434,7 +1448,8 @@ __global__ void __launch_bounds__(SplitShape::kThreads, 1)
                           int *__restrict__ cnt) {
   static_assert(!kB0 || !kQ4, "the B0 plane is q6_K's");
   static_assert(!kKP || !kB0, "pieces of one-plane tiles");
-  using L = SplitSmem<kQ4, kWide, kB0>;
+  static_assert(!kSmall || kKP, "small activation regions: pieces of one token tile");
+  using L = SplitSmem<kQ4, kWide, kB0, kSmall>;
   using S = SplitShape;
   constexpr int STAGES = L::kStages, NR = L::kRegions, NW = L::kN / 128;
   extern __shared__ uint8_t smem_raw[];
@@ -1591,11 +1606,11 @@ __global__ void __launch_bounds__(SplitShape::kThreads, 1)
                                                (w_done ? 0 : NW * L::kBK * (kB0 ? 2 : 1) + (mins ? L::kMinB : 0)));
             if (kKP) {  // the hi and the lo K-block's first rows
               bulk_load(a_smem(s), ablk + kb * kSplitQuarter, arow, full(s));
-              bulk_load(a_smem(s) + kSplitLo, ablk + kb * kSplitQuarter + kSplitLo, arow, full(s));
+              bulk_load(a_smem(s) + L::kALo, ablk + kb * kSplitQuarter + kSplitLo, arow, full(s));
             } else {
               bulk_load(a_smem(s), ablk + kb * kSplitQuarter, kSplitQuarter, full(s));
             }
-            if (mins) bulk_load(a_smem(s) + kSplitQuarter, ablk + kSplitMin, kMinBytes, full(s));
+            if (mins) bulk_load(a_smem(s) + L::kAMin, ablk + kSplitMin, L::kMinA, full(s));
           } else if (lane == 1 && !w_done) {
             for (int w = 0; w < NW; ++w) {
               const uint8_t *bblk = bplane + b_block(wtile(og, w), sb, half, nsb, kQ4);
@@ -1615,7 +1630,13 @@ __global__ void __launch_bounds__(SplitShape::kThreads, 1)
       }
     }
     if (!ok) {  // drain this CTA's copies still in flight
-      for (uint32_t k = issued > STAGES ? issued - STAGES : 0; k < issued; ++k)
+      // (kKP: stages whose weight copies went out before the wait but that
+      // were never armed get their arrival now, so their phase can complete)
+      if (lane == 0)
+        for (uint32_t k = issued; k < pre; ++k) mbar_arrive(full(static_cast<int>(k)));
+      __syncwarp();
+      const uint32_t last = issued > pre ? issued : pre;
+      for (uint32_t k = last > STAGES ? last - STAGES : 0; k < last; ++k)
         mbar_wait(full(k % STAGES), (k / STAGES) & 1, wctl, false);
       for (uint32_t k = s_issued > SRING ? s_issued - SRING : 0; k < s_issued; ++k)
         mbar_wait(sfull(k % SRING), (k / SRING) & 1, wctl, false);
@@ -1630,9 +1651,9 @@ __global__ void __launch_bounds__(SplitShape::kThreads, 1)
                  : "=r"(elected));
     constexpr uint32_t idesc = idesc_f16_f32(kTileM, L::kN);
     constexpr uint64_t kStageDesc = L::kStage >> 4;
-    const uint64_t ah0 = sdesc_kmajor_sw128(a_smem(0)), al0 = sdesc_kmajor_sw128(a_smem(0) + kSplitLo);
+    const uint64_t ah0 = sdesc_kmajor_sw128(a_smem(0)), al0 = sdesc_kmajor_sw128(a_smem(0) + L::kALo);
     const uint64_t b0 = sdesc_kmajor_sw128(b_smem(0));
-    const uint64_t am0 = sdesc_kmajor_sw32(SH ? m_smem(0) : a_smem(0) + kSplitQuarter);
+    const uint64_t am0 = sdesc_kmajor_sw32(SH ? m_smem(0) : a_smem(0) + L::kAMin);
     const uint64_t bm0 = sdesc_kmajor_sw32(SH ? m_smem(0) + kMinBytes : b_smem(0) + NW * L::kBK);
     uint32_t ks = 0, nr = 0;
     bool ok = true;
@@ -1794,12 +1815,58 @@ __global__ void __launch_bounds__(SplitShape::kThreads, 1)
             __stcg(dst + i * kTileM, make_float4(a.x, a.y, b.x, b.y));
           }
         }
-        __threadfence();
+        // the CTA's stores, then one thread's count with release and acquire
+        // semantics (the barrier orders the other threads' stores before it,
+        // and the last piece's reads after it)
         epi_bar();
-        if (threadIdx.x == 0) s_last = atomicAdd(cnt + pt, 1) == kp - 1;
+        if (threadIdx.x == 0) {
+          uint32_t prev;
+          asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(prev) : "l"(cnt + pt) : "memory");
+          s_last = static_cast<int>(prev) == kp - 1;
+        }
         epi_bar();
-        if (s_last && t < nt && (!kWide || og * NW + chalf < n_ot)) {
-          __threadfence();
+        const int rows_live =
+            static_cast<int>(min(static_cast<int64_t>(kTileM), nt - static_cast<int64_t>(tt) * kTileM));
+        if (s_last && !kWide && rows_live <= 8) {
+          // Few live rows (below nt): their float4 items -- at most 8 rows x
+          // 32 -- shared over the epilogue threads, one each, rows fastest;
+          // each the sum of its kp partials in piece order, the loads of up
+          // to 4 pieces in flight together
+          constexpr int kQ = CW / 4;  // float4 per row of a column half
+          const int idx = static_cast<int>(threadIdx.x);
+          if (idx < rows_live * 2 * kQ) {
+            const int r = idx % rows_live, hq = idx / rows_live, ch = hq / kQ, i = hq % kQ;
+            const float4 *src = reinterpret_cast<const float4 *>(part) +
+                                ((static_cast<int64_t>(pt) * 2 + ch) * kQ + i) * kTileM + r;
+            const int64_t pstride = static_cast<int64_t>(n_pieced) * 2 * kQ * kTileM;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int pc0 = 0; pc0 < kp; pc0 += 4) {
+              float4 v[4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                if (pc0 + j < kp) v[j] = __ldcg(src + (pc0 + j) * pstride);
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                if (pc0 + j < kp) {
+                  const float2 a = __fadd2_rn(make_float2(acc.x, acc.y), make_float2(v[j].x, v[j].y));
+                  const float2 b = __fadd2_rn(make_float2(acc.z, acc.w), make_float2(v[j].z, v[j].w));
+                  acc = make_float4(a.x, a.y, b.x, b.y);
+                }
+            }
+            const int64_t tr = static_cast<int64_t>(tt) * kTileM + r;
+            const int64_t oc = static_cast<int64_t>(og) * kTileN + ch * 64 + 4 * i;
+            float *yp = Y + tr * od + oc;
+            if ((od & 3) == 0 && oc + 4 <= od) {
+              *reinterpret_cast<float4 *>(yp) = acc;
+            } else {
+              if (oc < od) yp[0] = acc.x;
+              if (oc + 1 < od) yp[1] = acc.y;
+              if (oc + 2 < od) yp[2] = acc.z;
+              if (oc + 3 < od) yp[3] = acc.w;
+            }
+          }
+        } else if (s_last && t < nt && (!kWide || og * NW + chalf < n_ot)) {
+          // each thread its row's CW columns, all pieces' loads of a piece in flight together
 #pragma unroll
           for (int i = 0; i < CW / 2; ++i) y[i] = make_float2(0.f, 0.f);
           for (int pc = 0; pc < kp; ++pc) {
@@ -2664,7 +2731,7 @@ cudaError_t launch_gemm_split(const mmq_weights_s *h, const uint8_t *Q, const fl
   }
   const int grid = p.grid;
   auto go = [&](auto kern, int smem, int variant) -> cudaError_t {
-    static std::atomic<int> ready[10][64];  // per kernel variant: 0 unknown, 1 ready, 2 unusable
+    static std::atomic<int> ready[12][64];  // per kernel variant: 0 unknown, 1 ready, 2 unusable
     std::atomic<int> &rd = ready[variant][dev];
     int stt = rd.load();
     if (stt == 0) {
@@ -2690,8 +2757,16 @@ cudaError_t launch_gemm_split(const mmq_weights_s *h, const uint8_t *Q, const fl
                               static_cast<const float *>(invp), nt, h->od, nb32, static_cast<int>(n_tt), n_ot, Y, w,
                               static_cast<const uint8_t *>(h->b0plane), p.kp, p.n_full, part, cnt);
   };
+  // pieces of one token tile of at most 32 tokens: the stages' activation
+  // regions hold only those rows, so twice as many stages fit in the ring and
+  // go out before the wait for the quantization kernel
+  const bool small = p.kp > 1 && !wide && p.n_full == 0 && n_tt == 1 && p.rows <= SplitSmem<true, false, false, true>::kSmallRows;
   if (p.kp > 1 && wide)  // (q6_K only: the plan keeps q4_K's 256-row tiles whole)
     e = go(mmq_gemm_split_kernel<false, true, false, true>, SplitSmem<false, true>::kBytes, 9);
+  else if (small)
+    e = q4 ? go(mmq_gemm_split_kernel<true, false, false, true, true>, SplitSmem<true, false, false, true>::kBytes, 10)
+           : go(mmq_gemm_split_kernel<false, false, false, true, true>, SplitSmem<false, false, false, true>::kBytes,
+                11);
   else if (p.kp > 1)
     e = q4 ? go(mmq_gemm_split_kernel<true, false, false, true>, SplitSmem<true, false>::kBytes, 6)
            : go(mmq_gemm_split_kernel<false, false, false, true>, SplitSmem<false, false>::kBytes, 7);

@@ -700,7 +700,7 @@ def test_raw_arm_workloads_sampled_against_oracle(mmq, name):
 # --------------------------------------------------------------------------
 # few tiles (small nt): the split arm cuts each tile's super-blocks into pieces
 @pytest.mark.parametrize("name", ["q4_K", "q6_K"])
-@pytest.mark.parametrize("nt", [1, 16, 64, 100, 128, 129, 200, 256])
+@pytest.mark.parametrize("nt", [1, 16, 32, 33, 64, 100, 128, 129, 200, 256])
 def test_small_nt_pieces_against_oracle(mmq, name, nt):
     """q-proj weights (3584 x 3584) at token counts whose 128-row tiles fill
     at most half the SMs: every tile's super-blocks are shared out as pieces
