@@ -2026,6 +2026,27 @@ __global__ void __launch_bounds__(PairShape::kThreads, 1)
       // two warps, the even and the odd stages (the scale blocks with the
       // even ones); one warp's per-stage code spilled in the q4_K variant
       const int p = warp == PRODUCER_WARP ? 0 : 1;
+      // The first unit's first stages' weight copies (and min images) do not
+      // depend on the quantization kernel: they go out before the wait for
+      // it, their bytes expected without an arrival (the ring is fresh).
+      uint32_t pre = 0;
+      if (pair < n_units) {
+        const int w = wtile(pair / n_tt);
+        pre = static_cast<uint32_t>(min(static_cast<int64_t>(STAGES), 4 * nsb));
+        if (lane == 0)
+          for (uint32_t q = p; q < pre; q += 2) {
+            const int64_t sb = q / 4;
+            const int qq = static_cast<int>(q % 4), half = qq >> 1, kb = qq & 1;
+            const bool mins = kQ4 && qq == 3;
+            mbar_expect_tx(full(static_cast<int>(q)), L::kW + (mins ? kMinBytes : 0));
+            bulk_load(w_smem(static_cast<int>(q)), bplane + b_block(w, sb, half, nsb, kQ4) + kb * L::kW, L::kW,
+                      full(static_cast<int>(q)));
+            if (mins)
+              bulk_load(m_smem(static_cast<int>(sb % (kQ4 ? L::kMR : 1))), bplane + b_block(w, sb, 1, nsb, kQ4) + kBMin,
+                        kMinBytes, full(static_cast<int>(q)));
+          }
+        __syncwarp();
+      }
       griddep_wait();  // the activation blocks come from the kernel before this one
       uint32_t ks = 0, ns = 0, issued = 0, s_issued = 0;
       bool ok = true;
@@ -2043,15 +2064,16 @@ __global__ void __launch_bounds__(PairShape::kThreads, 1)
             if (lane == 0) {
               const int half = qq >> 1, kb = qq & 1;
               const bool mins = kQ4 && qq == 3;
+              const bool w_done = ks < pre;  // its weight copies went out before the wait
               // this CTA's rows of the hi and the lo K-block (and, last quarter, the min image after them)
               const uint32_t ab = 2 * pair_kb_bytes(h) + (mins ? h * 32 : 0);
-              mbar_arrive_expect_tx(full(s), L::kW + ab + (mins ? kMinBytes : 0));
-              bulk_load(w_smem(s), bplane + b_block(w, sb, half, nsb, kQ4) + kb * L::kW, L::kW, full(s));
+              mbar_arrive_expect_tx(full(s), ab + (w_done ? 0 : L::kW + (mins ? kMinBytes : 0)));
+              if (!w_done) bulk_load(w_smem(s), bplane + b_block(w, sb, half, nsb, kQ4) + kb * L::kW, L::kW, full(s));
               bulk_load(a_smem(s),
                         aplane + pair_block(tt, sb, half, nsb, kQ4, h) + rank * pair_rank_bytes(kQ4, half, h) +
                             kb * 2 * pair_kb_bytes(h),
                         ab, full(s));
-              if (mins)
+              if (mins && !w_done)
                 bulk_load(m_smem(static_cast<int>(ns % (kQ4 ? L::kMR : 1))),
                           bplane + b_block(w, sb, 1, nsb, kQ4) + kBMin, kMinBytes, full(s));
             }
@@ -2069,7 +2091,14 @@ __global__ void __launch_bounds__(PairShape::kThreads, 1)
         }
       }
       if (!ok) {  // drain this warp's copies still in flight
-        for (uint32_t k = issued > STAGES ? issued - STAGES : 0; k < issued; ++k)
+        // (stages whose weight copies went out before the wait but that were
+        // never armed get this CTA's arrival now)
+        if (lane == 0)
+          for (uint32_t k = issued; k < pre; ++k)
+            if (static_cast<int>(k & 1) == p) mbar_arrive(full(static_cast<int>(k)));
+        __syncwarp();
+        const uint32_t last = issued > pre ? issued : pre;
+        for (uint32_t k = last > STAGES ? last - STAGES : 0; k < last; ++k)
           if (static_cast<int>(k & 1) == p) mbar_wait(full(k % STAGES), (k / STAGES) & 1, wctl, false);
         for (uint32_t k = s_issued > SRING ? s_issued - SRING : 0; k < s_issued; ++k)
           mbar_wait(sfull(k % SRING), (k / SRING) & 1, wctl, false);
