@@ -730,11 +730,14 @@ def test_small_nt_pieces_against_oracle(mmq, name, nt):
 
 
 @pytest.mark.parametrize("name,od,id_,nt", [("q6_K", 3584, 18944, 16), ("q4_K", 1000, 2048, 50),
-                                            ("q6_K", 130, 512, 7)])
+                                            ("q6_K", 130, 512, 7), ("q4_K", 131, 768, 5),
+                                            ("q4_K", 257, 1024, 31)])
 def test_small_nt_pieces_other_shapes(mmq, name, od, id_, nt):
     """Pieces on the FFN-down shape (74 super-blocks per tile), a ragged od
-    (8 tiles, one super-block per piece) and a two-tile weight; from pad40
-    blocks and from fp32 X, against the oracle."""
+    (8 tiles, one super-block per piece), two- and three-tile weights with od
+    not a multiple of 4 (the last piece's sum stored element by element) and
+    up to 31 tokens (the trimmed activation regions); from pad40 blocks and
+    from fp32 X, against the oracle."""
     W = gen.weights(name, od, id_, seed=710 + nt)
     X = gen.activations(nt, id_, seed=711 + nt, outlier_p=0.01, outlier_scale=20.0)
     w = mmq.mmq_register_weights(name, torch.from_numpy(W).cuda(), od, id_)
